@@ -1,0 +1,211 @@
+"""Seeded synthetic inputs for deterministic gradient reduction.
+
+This module only draws random data: it holds none of the method's arithmetic,
+so both the CPU oracle (through the tests) and the GPU library (through the
+tests and the benchmark) can take their inputs from it. Every generator uses
+one ``torch.Generator('cpu')`` seeded per workload and draws in a fixed order;
+fp32 draws are narrowed to bf16 with torch's round-to-nearest-even. All
+tensors are CPU tensors; ``bits()`` gives the raw bf16 bit patterns as a numpy
+uint16 array for the oracle.
+
+The five workloads (shapes, distributions and draw order):
+  colsum_small   x bf16 [2048, 16] ~ U(-1, 1)                                 seed 1
+  index_add      src fp32 [262144, 128] ~ N(0, 1); idx int32 ~ U[0, 16384),
+                 then floor(0.1 N) positions (a random permutation's prefix)
+                 set to -1; out fp32 [16385, 128] zeros                      seed 2
+  dprob          dY, Y bf16 [65536, 4096] ~ N(0, 1)                          seed 3
+  colsum_strided base bf16 [4, 2048, 128] ~ N(0, 0.02^2); the view
+                 base[..., :64] (token stride 128); base[..., 64:] is then
+                 overwritten with bf16 NaN as a poison                        seed 4
+  colsum_large   x bf16 [8388608, 64] ~ N(0, 0.02^2), drawn after the
+                 strided base from the same generator                        seed 4
+  wgrad          expert of each of 32768 tokens ~ multinomial(uniform over 8),
+                 counts -> offsets; G bf16 [32768, 4096], X bf16 [32768, 2048]
+                 ~ N(0, 1), rows grouped by expert; main_grad fp32
+                 [8, 4096, 2048] ~ N(0, 1e-3^2)                              seed 5
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+BF16_NAN_BITS = 0x7FC0
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    """bf16 tensor -> numpy uint16 array of its bit patterns (shares memory)."""
+    assert t.dtype == torch.bfloat16
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def f32(t: torch.Tensor) -> np.ndarray:
+    assert t.dtype == torch.float32
+    return t.contiguous().numpy()
+
+
+def _gen(seed: int) -> torch.Generator:
+    g = torch.Generator("cpu")
+    g.manual_seed(seed)
+    return g
+
+
+def _draw(shape, dist: str, g: torch.Generator, scale: float = 1.0) -> torch.Tensor:
+    if dist == "uniform":
+        return torch.rand(shape, generator=g) * 2.0 - 1.0
+    if dist == "normal":
+        return torch.randn(shape, generator=g) * scale
+    if dist == "ternary":
+        return torch.randint(-1, 2, shape, generator=g).to(torch.float32)
+    raise ValueError(dist)
+
+
+# --------------------------------------------------------------------------
+# column sum
+# --------------------------------------------------------------------------
+
+@dataclass
+class ColsumInput:
+    base: torch.Tensor      # contiguous storage the view lives in
+    B: int
+    S: int
+    H: int
+    stride_b: int           # elements
+    stride_s: int           # elements
+    offset: int = 0         # element offset of x[0][0][0] inside base
+
+
+def colsum_input(B: int, S: int, H: int, *, seed: int, dist: str = "normal", scale: float = 1.0,
+                 dtype: torch.dtype = torch.bfloat16, token_stride: int | None = None,
+                 poison: bool = True) -> ColsumInput:
+    """x [B, S, H]; with token_stride > H the rows live in a wider base and the
+    unused columns hold NaN (bf16) or NaN (fp32) so a stray read shows."""
+    g = _gen(seed)
+    ts = H if token_stride is None else token_stride
+    assert ts >= H
+    base = _draw((B, S, ts), dist, g, scale).to(dtype)
+    if ts > H and poison:
+        base[..., H:] = float("nan")
+    return ColsumInput(base.reshape(-1), B, S, H, S * ts, ts)
+
+
+def colsum_small() -> ColsumInput:
+    return colsum_input(1, 2048, 16, seed=1, dist="uniform")
+
+
+def _strided_and_large():
+    g = _gen(4)
+    base = (torch.randn((4, 2048, 128), generator=g) * 0.02).to(torch.bfloat16)
+    base[..., 64:] = float("nan")
+    strided = ColsumInput(base.reshape(-1), 4, 2048, 64, 2048 * 128, 128)
+    return strided, g
+
+
+def colsum_strided() -> ColsumInput:
+    return _strided_and_large()[0]
+
+
+def colsum_large() -> ColsumInput:
+    _, g = _strided_and_large()
+    x = (torch.randn((8388608, 64), generator=g) * 0.02).to(torch.bfloat16)
+    return ColsumInput(x.reshape(-1), 1, 8388608, 64, 8388608 * 64, 64)
+
+
+# --------------------------------------------------------------------------
+# dprob
+# --------------------------------------------------------------------------
+
+@dataclass
+class DprobInput:
+    dY: torch.Tensor  # [M, ld] (only the first N columns are read)
+    Y: torch.Tensor
+    M: int
+    N: int
+
+
+def dprob_input(M: int, N: int, *, seed: int, dist: str = "normal",
+                dtype: torch.dtype = torch.bfloat16, ld: int | None = None) -> DprobInput:
+    g = _gen(seed)
+    ldv = N if ld is None else ld
+    dY = _draw((M, ldv), dist, g).to(dtype)
+    Y = _draw((M, ldv), dist, g).to(dtype)
+    if ldv > N:
+        dY[:, N:] = float("nan")
+        Y[:, N:] = float("nan")
+    return DprobInput(dY, Y, M, N)
+
+
+def dprob_full() -> DprobInput:
+    return dprob_input(65536, 4096, seed=3)
+
+
+# --------------------------------------------------------------------------
+# index_add
+# --------------------------------------------------------------------------
+
+@dataclass
+class IndexAddInput:
+    src: torch.Tensor   # fp32 [N, D]
+    idx: torch.Tensor   # int32 [N]
+    out: torch.Tensor   # fp32 [R+1, D]
+    R: int
+
+
+def index_add_input(N: int, D: int, R: int, *, seed: int, pad_frac: float = 0.1,
+                    dist: str = "normal", out_init: str = "zeros") -> IndexAddInput:
+    g = _gen(seed)
+    src = _draw((N, D), dist, g).to(torch.float32)
+    idx = torch.randint(0, max(R, 1), (N,), generator=g, dtype=torch.int64).to(torch.int32)
+    n_pad = int(pad_frac * N)
+    if n_pad:
+        pos = torch.randperm(N, generator=g)[:n_pad]
+        idx[pos] = -1
+    if R == 0:
+        idx[:] = -1
+    if out_init == "zeros":
+        out = torch.zeros((R + 1, D), dtype=torch.float32)
+    else:
+        out = _draw((R + 1, D), dist, g).to(torch.float32)
+    return IndexAddInput(src, idx, out, R)
+
+
+def index_add_full() -> IndexAddInput:
+    return index_add_input(262144, 128, 16384, seed=2)
+
+
+# --------------------------------------------------------------------------
+# grouped wgrad
+# --------------------------------------------------------------------------
+
+@dataclass
+class WgradInput:
+    G: torch.Tensor          # bf16 [T, N]
+    X: torch.Tensor          # bf16 [T, K]
+    offs: torch.Tensor       # int64 [E+1]
+    main_grad: torch.Tensor  # fp32 [E, N, K]
+    E: int
+
+
+def wgrad_input(E: int, T: int, N: int, K: int, *, seed: int, dist: str = "normal",
+                counts: list[int] | None = None, mg_scale: float = 1e-3) -> WgradInput:
+    g = _gen(seed)
+    if counts is None:
+        ex = torch.multinomial(torch.ones(E), T, replacement=True, generator=g)
+        cnt = torch.bincount(ex, minlength=E)
+    else:
+        assert len(counts) == E and sum(counts) == T
+        cnt = torch.tensor(counts, dtype=torch.int64)
+    offs = torch.zeros(E + 1, dtype=torch.int64)
+    offs[1:] = torch.cumsum(cnt, 0)
+    G = _draw((T, N), dist, g).to(torch.bfloat16)
+    X = _draw((T, K), dist, g).to(torch.bfloat16)
+    if dist == "ternary":
+        mg = torch.randint(-4, 5, (E, N, K), generator=g).to(torch.float32)
+    else:
+        mg = torch.randn((E, N, K), generator=g) * mg_scale
+    return WgradInput(G, X, offs, mg.to(torch.float32), E)
+
+
+def wgrad_full() -> WgradInput:
+    return wgrad_input(8, 32768, 4096, 2048, seed=5)

@@ -1,0 +1,611 @@
+/*
+ * CPU oracle for deterministic, atomic-free gradient reduction.
+ *
+ * TEST INFRASTRUCTURE ONLY. This file is the plain, slow, single-threaded
+ * statement of the bits that the GPU library must produce. Only the tests,
+ * the smoke check and the CPU-baseline leg of the benchmark load it; the
+ * library never does, and the two share no code.
+ *
+ * Arithmetic: every add and multiply below is one IEEE-754 binary32
+ * operation, rounded to nearest-even, with subnormals kept. The file must be
+ * built with -ffp-contract=off and without fast-math, so that no a*b+c is
+ * ever fused into one rounding (GCC contracts by default on aarch64).
+ *
+ * The four operations and the pages they follow:
+ *   ordered column sum   - Megatron-LM PR #8244 "ordered reduction for the fused
+ *                          pre-GDR gate backward", description: each program
+ *                          writes independent FP32 partial sums, the caller
+ *                          reduces them in order on the same stream.
+ *   ordered dprob        - cuDNN-frontend PR #521 "grouped gemm dsrelu
+ *                          deterministic dprob", commit "deterministic dprob":
+ *                          one FP32 slot per N-tile, one writer per
+ *                          (token, tile), slots reduced in a fixed order and
+ *                          accumulated into dprob.
+ *   det. index_add       - Megatron-LM PR #7441 "DSv4 --deterministic-mode",
+ *                          Source 3: stable sort by destination plus a
+ *                          segmented sum, padding routed to dummy rows.
+ *   grouped wgrad        - FlashInfer PR #8602 "fuse the fp32 weight-gradient
+ *                          accumulate into main_grad" and its follow-up #8924
+ *                          "Design and numerics": out <- RN32(out + dW) with a
+ *                          deterministic dW; the 512-token k tile is the
+ *                          weight-gradient main stage.
+ *
+ * Canonical order (the same for all four): partial sums are taken over tiles;
+ * inside a tile the leaves are summed by a fixed-width pairwise tree; the tile
+ * partials are folded in ascending tile order; the result overwrites the
+ * output or is added to it with one rounding.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define DGRO_OK 0
+#define DGRO_ERR_ARG 1
+#define DGRO_ERR_NOMEM 2
+
+/* ------------------------------------------------------------------------ */
+/* Scalars                                                                  */
+/* ------------------------------------------------------------------------ */
+
+/* bf16 -> fp32 is exact: the 16 bf16 bits are the top half of the fp32. */
+float dgro_bf16_to_f32(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+static float load_elem(const void *base, int32_t dtype, int64_t off)
+{
+    if (dtype == 1)
+        return dgro_bf16_to_f32(((const uint16_t *)base)[off]);
+    return ((const float *)base)[off];
+}
+
+/* ------------------------------------------------------------------------ */
+/* Pairwise tree and ascending fold                                          */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Pairwise summation over the fixed window [a, b) of a tile that is `width`
+ * leaves wide (width a power of two). Only leaves [0, count) exist; the rest
+ * are absent. pw([a,b)) = pw([a,m)) + pw([m,b)) with m the midpoint; a node
+ * with one absent child is its other child, unchanged; a single leaf is
+ * itself. This is textbook recursive pairwise summation (Higham, "Accuracy and
+ * Stability of Numerical Algorithms", sec. 4.2) over the tile's fixed window;
+ * the pages name a fixed-width tree but not its pairing, and this reading
+ * pairs adjacent halves. Returns 1 and writes *out when [a,b) holds a leaf.
+ */
+static int pw_node(const float *leaf, int64_t count, int64_t a, int64_t b, float *out)
+{
+    if (a >= count)
+        return 0;
+    if (b - a == 1) {
+        *out = leaf[a];
+        return 1;
+    }
+    int64_t m = a + (b - a) / 2;
+    float l = 0.0f, r = 0.0f;
+    int has_l = pw_node(leaf, count, a, m, &l);
+    int has_r = pw_node(leaf, count, m, b, &r);
+    if (has_l && has_r) {
+        *out = l + r;
+        return 1;
+    }
+    /* leaves present form a prefix, so a present node always has a left leaf */
+    *out = has_l ? l : r;
+    return has_l || has_r;
+}
+
+static int is_pow2(int64_t w) { return w > 0 && (w & (w - 1)) == 0; }
+
+/* Tile partial: pairwise tree over `count` leaves (1 <= count <= width). */
+float dgro_pairwise(const float *leaf, int64_t count, int64_t width)
+{
+    float s = 0.0f;
+    pw_node(leaf, count, 0, width, &s);
+    return s;
+}
+
+/* Ascending fold of tile partials: F = P0; F = F + Pj for j = 1 .. n-1. */
+float dgro_fold(const float *partial, int64_t n)
+{
+    float f = partial[0];
+    for (int64_t j = 1; j < n; ++j)
+        f = f + partial[j];
+    return f;
+}
+
+/* ------------------------------------------------------------------------ */
+/* 1. Ordered column sum                                                     */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * out[h] = fold_j pw_W( x[t][h] : t in tile j ),  tiles of W tokens,
+ * tokens flattened as t = b*S + s, element x[b][s][h] at
+ * b*stride_b + s*stride_s + h (elements). Megatron-LM PR #8244, description:
+ * each program writes its own FP32 partial sums (one slot row per tile) and
+ * the caller reduces them in order. With accumulate, out[h] = out[h] + F
+ * (one rounding); with T = 0, overwrite writes +0.0 and accumulate leaves
+ * out unchanged. slots (nullable) receives the [n_tiles][H] tile partials.
+ */
+int dgro_ordered_colsum(const void *x, int32_t dtype, int64_t B, int64_t S, int64_t H,
+                        int64_t stride_b, int64_t stride_s, int64_t W,
+                        float *out, int32_t accumulate, float *slots)
+{
+    if (B < 0 || S < 0 || H < 0 || !is_pow2(W) || (dtype != 0 && dtype != 1))
+        return DGRO_ERR_ARG;
+    int64_t T = B * S;
+    int64_t n_tiles = (T + W - 1) / W;
+    float *leaf = (float *)malloc((size_t)W * sizeof(float));
+    float *part = (float *)malloc((size_t)(n_tiles > 0 ? n_tiles : 1) * sizeof(float));
+    if (!leaf || !part) {
+        free(leaf);
+        free(part);
+        return DGRO_ERR_NOMEM;
+    }
+    for (int64_t h = 0; h < H; ++h) {
+        for (int64_t j = 0; j < n_tiles; ++j) {
+            int64_t t0 = j * W;
+            int64_t count = (T - t0 < W) ? (T - t0) : W;
+            for (int64_t i = 0; i < count; ++i) {
+                int64_t t = t0 + i;
+                int64_t b = t / S, s = t % S;
+                leaf[i] = load_elem(x, dtype, b * stride_b + s * stride_s + h);
+            }
+            part[j] = dgro_pairwise(leaf, count, W);
+            if (slots)
+                slots[j * H + h] = part[j];
+        }
+        if (n_tiles == 0) {
+            if (!accumulate)
+                out[h] = 0.0f;
+            continue;
+        }
+        float f = dgro_fold(part, n_tiles);
+        out[h] = accumulate ? out[h] + f : f;
+    }
+    free(leaf);
+    free(part);
+    return DGRO_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* 2. Ordered per-row dprob                                                  */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * dprob[m] = fold_j pw_W( dY[m][n] * Y[m][n] : n in N-tile j ).
+ * cuDNN-frontend PR #521, commit "deterministic dprob": dprob gets one slot per
+ * N-tile so every (token, tile_n) has one writer, and the slots are reduced in
+ * a fixed order; the reduction accumulates into dprob like the atomic path it
+ * replaces. Each leaf is one fp32 multiply of the two widened inputs, rounded
+ * on its own (never fused into the following add). Overwrite/accumulate and
+ * the empty case (N = 0) as in the column sum. slots (nullable) receives
+ * [M][n_tiles].
+ */
+int dgro_ordered_rowdot_dprob(const void *dY, const void *Y, int32_t dtype, int64_t M, int64_t N,
+                              int64_t ld_dy, int64_t ld_y, int64_t W,
+                              float *dprob, int32_t accumulate, float *slots)
+{
+    if (M < 0 || N < 0 || !is_pow2(W) || (dtype != 0 && dtype != 1))
+        return DGRO_ERR_ARG;
+    int64_t n_tiles = (N + W - 1) / W;
+    float *leaf = (float *)malloc((size_t)W * sizeof(float));
+    float *part = (float *)malloc((size_t)(n_tiles > 0 ? n_tiles : 1) * sizeof(float));
+    if (!leaf || !part) {
+        free(leaf);
+        free(part);
+        return DGRO_ERR_NOMEM;
+    }
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t j = 0; j < n_tiles; ++j) {
+            int64_t n0 = j * W;
+            int64_t count = (N - n0 < W) ? (N - n0) : W;
+            for (int64_t i = 0; i < count; ++i) {
+                float a = load_elem(dY, dtype, m * ld_dy + n0 + i);
+                float b = load_elem(Y, dtype, m * ld_y + n0 + i);
+                float p = a * b;
+                leaf[i] = p;
+            }
+            part[j] = dgro_pairwise(leaf, count, W);
+            if (slots)
+                slots[m * n_tiles + j] = part[j];
+        }
+        if (n_tiles == 0) {
+            if (!accumulate)
+                dprob[m] = 0.0f;
+            continue;
+        }
+        float f = dgro_fold(part, n_tiles);
+        dprob[m] = accumulate ? dprob[m] + f : f;
+    }
+    free(leaf);
+    free(part);
+    return DGRO_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* 3. Deterministic index_add                                                */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Megatron-LM PR #7441, Source 3 (deterministic indexer gradient): an
+ * atomic-free index_add by stable sort by destination plus a segmented sum;
+ * padding entries (-1) go to dummy rows that the caller drops.
+ *
+ *   key[i] = idx[i] if 0 <= idx[i] < R, else R (the dummy row). Entries
+ *            outside [-1, R) are also counted in *bad_count.
+ *   Stable sort of i by key (a counting sort, ties in original order) gives
+ *   perm[] and seg_start[r] (r = 0 .. R+1).
+ *   Segment r, members in original order i_0 < i_1 < ..., is cut into tiles
+ *   of W members; out[r][d] = out[r][d] + fold_tiles pw_W(src[i_k][d]).
+ *   An empty segment leaves out[r] unchanged. W = 1 is a purely sequential
+ *   fold in original order.
+ * out is [R+1][D] with row stride ld_out; src is [N][D] with row stride
+ * ld_src. perm (nullable, [N]) and seg_start (nullable, [R+2]) return the
+ * sort for integer comparisons.
+ */
+int dgro_det_index_add(float *out, int64_t R, int64_t D, int64_t ld_out,
+                       const float *src, int64_t ld_src, const int32_t *idx, int64_t N,
+                       int64_t W, int64_t *bad_count, int32_t *perm_out, int32_t *seg_start_out)
+{
+    if (R < 0 || D < 0 || N < 0 || !is_pow2(W))
+        return DGRO_ERR_ARG;
+    int64_t nkeys = R + 1;
+    int64_t *count = (int64_t *)calloc((size_t)nkeys + 1, sizeof(int64_t));
+    int64_t *start = (int64_t *)calloc((size_t)nkeys + 1, sizeof(int64_t));
+    int64_t *cursor = (int64_t *)calloc((size_t)nkeys + 1, sizeof(int64_t));
+    int64_t *key = (int64_t *)malloc((size_t)(N > 0 ? N : 1) * sizeof(int64_t));
+    int64_t *perm = (int64_t *)malloc((size_t)(N > 0 ? N : 1) * sizeof(int64_t));
+    float *leaf = (float *)malloc((size_t)W * sizeof(float));
+    float *part = (float *)malloc((size_t)(N / W + 2) * sizeof(float));
+    if (!count || !start || !cursor || !key || !perm || !leaf || !part) {
+        free(count); free(start); free(cursor); free(key); free(perm); free(leaf); free(part);
+        return DGRO_ERR_NOMEM;
+    }
+    int64_t bad = 0;
+    for (int64_t i = 0; i < N; ++i) {
+        int64_t v = idx[i];
+        if (v >= 0 && v < R) {
+            key[i] = v;
+        } else {
+            key[i] = R;
+            if (v != -1)
+                ++bad;
+        }
+        ++count[key[i]];
+    }
+    /* counting sort: exclusive prefix of the counts, then place in order */
+    for (int64_t r = 0; r < nkeys; ++r)
+        start[r + 1] = start[r] + count[r];
+    for (int64_t r = 0; r < nkeys; ++r)
+        cursor[r] = start[r];
+    for (int64_t i = 0; i < N; ++i)
+        perm[cursor[key[i]]++] = i;
+
+    for (int64_t r = 0; r < nkeys; ++r) {
+        int64_t n_r = count[r];
+        if (n_r == 0)
+            continue;
+        int64_t n_tiles = (n_r + W - 1) / W;
+        for (int64_t d = 0; d < D; ++d) {
+            for (int64_t j = 0; j < n_tiles; ++j) {
+                int64_t k0 = j * W;
+                int64_t cnt = (n_r - k0 < W) ? (n_r - k0) : W;
+                for (int64_t k = 0; k < cnt; ++k)
+                    leaf[k] = src[perm[start[r] + k0 + k] * ld_src + d];
+                part[j] = dgro_pairwise(leaf, cnt, W);
+            }
+            float f = dgro_fold(part, n_tiles);
+            out[r * ld_out + d] = out[r * ld_out + d] + f;
+        }
+    }
+    if (bad_count)
+        *bad_count = bad;
+    if (perm_out)
+        for (int64_t i = 0; i < N; ++i)
+            perm_out[i] = (int32_t)perm[i];
+    if (seg_start_out)
+        for (int64_t r = 0; r <= nkeys; ++r)
+            seg_start_out[r] = (int32_t)start[r];
+    free(count); free(start); free(cursor); free(key); free(perm); free(leaf); free(part);
+    return DGRO_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* 4. Split-K grouped weight gradient accumulated into main_grad             */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Model of one tensor-core K=16 step, D = C + sum_k A_k B_k, for one output
+ * element with bf16 A, B and an fp32 accumulator.
+ *
+ * The pages fix FP32 accumulation and a fixed split order but say nothing
+ * about how the tensor core adds the 16 products of one step. The structure
+ * below follows the published method for describing tensor-core dot products
+ * (Fasi, Higham, Mikaitis and Pranesh, "Numerical behavior of NVIDIA tensor
+ * cores", PeerJ Computer Science 7:e330, 2021):
+ *   - each product A_k B_k is exact (8-bit x 8-bit significands);
+ *   - the terms of one fused group (up to `group` products, plus the
+ *     accumulator when acc_in_sum) are aligned to the largest leading-bit
+ *     exponent among them, keeping `frac_bits` bits below it; bits below that
+ *     are dropped (truncation of the magnitude);
+ *   - the aligned terms are added exactly and the sum is rounded once to fp32,
+ *     toward zero (final_rn = 0) or to nearest-even (final_rn = 1);
+ *   - when acc_in_sum = 0 the products are fused first and the accumulator is
+ *     added afterwards by an ordinary fp32 add.
+ * The parameters are properties of the hardware, set from designed
+ * experiments on it; dgro_tc_default_model() returns the values in use.
+ */
+typedef struct {
+    int32_t group;      /* products per fused group: 16 = the whole K16 step */
+    int32_t frac_bits;  /* bits kept below the leading bit of the largest term */
+    int32_t acc_in_sum; /* 1: the accumulator is a term of the first group */
+    int32_t final_rn;   /* 1: round to nearest-even; 0: toward zero */
+} dgro_tc_model;
+
+void dgro_tc_default_model(dgro_tc_model *m)
+{
+    m->group = 16;
+    m->frac_bits = 25;
+    m->acc_in_sum = 1;
+    m->final_rn = 0;
+}
+
+/* a finite value as sign * sig * 2^exp with an integer significand */
+typedef struct {
+    int neg;
+    uint64_t sig;
+    int exp;
+} term_t;
+
+static term_t term_from_f32(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    term_t t;
+    t.neg = (int)(u >> 31);
+    int e = (int)((u >> 23) & 0xff);
+    uint32_t m = u & 0x7fffff;
+    if (e == 0) {
+        t.sig = m;
+        t.exp = -149;
+    } else {
+        t.sig = (uint64_t)m | 0x800000u;
+        t.exp = e - 150;
+    }
+    return t;
+}
+
+static int msb64(uint64_t v)
+{
+    int n = -1;
+    while (v) {
+        v >>= 1;
+        ++n;
+    }
+    return n;
+}
+
+/* exact product of two bf16 values as a term */
+static term_t term_product(uint16_t a, uint16_t b)
+{
+    term_t ta = term_from_f32(dgro_bf16_to_f32(a));
+    term_t tb = term_from_f32(dgro_bf16_to_f32(b));
+    term_t p;
+    p.neg = ta.neg ^ tb.neg;
+    p.sig = ta.sig * tb.sig;
+    p.exp = ta.exp + tb.exp;
+    return p;
+}
+
+/* round sign * mag * 2^q to the nearest fp32 (toward zero or to nearest-even) */
+static float round_to_f32(int neg, unsigned __int128 mag, int q, int rn)
+{
+    if (mag == 0)
+        return neg ? -0.0f : 0.0f;
+    int top = 0;
+    unsigned __int128 v = mag;
+    while (v >> 1) {
+        v >>= 1;
+        ++top;
+    }
+    int lead = top + q;                     /* exponent of the leading bit */
+    int lsb = lead - 23;                    /* weight of the last kept bit */
+    if (lsb < -149)
+        lsb = -149;                         /* subnormal range */
+    unsigned __int128 kept;
+    int shift = lsb - q;
+    if (shift <= 0) {
+        kept = mag << (-shift);
+    } else {
+        kept = mag >> shift;
+        unsigned __int128 rem = mag - (kept << shift);
+        unsigned __int128 half = (unsigned __int128)1 << (shift - 1);
+        if (rn && (rem > half || (rem == half && (kept & 1))))
+            kept += 1;
+    }
+    /* kept * 2^lsb; renormalise a carry out of 24 bits */
+    uint64_t k = (uint64_t)kept;
+    if (k >> 24) {
+        k >>= 1;
+        lsb += 1;
+    }
+    uint32_t bits;
+    if (k < 0x800000u) {                    /* subnormal: lsb == -149 */
+        bits = (uint32_t)k;
+    } else {
+        int e = lsb + 150;
+        if (e >= 255)
+            bits = 0x7f800000u;             /* overflow: not reached by the tests */
+        else
+            bits = ((uint32_t)e << 23) | ((uint32_t)k & 0x7fffffu);
+    }
+    bits |= (uint32_t)neg << 31;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return f;
+}
+
+/* one fused group: terms aligned to the largest, truncated, summed, rounded */
+static float fused_sum(const term_t *t, int n, const dgro_tc_model *m)
+{
+    int ref = -100000, any = 0;
+    for (int i = 0; i < n; ++i) {
+        if (t[i].sig == 0)
+            continue;
+        int lead = msb64(t[i].sig) + t[i].exp;
+        if (!any || lead > ref)
+            ref = lead;
+        any = 1;
+    }
+    if (!any)
+        return 0.0f;
+    int q = ref - m->frac_bits;             /* weight of the last kept bit */
+    __int128 s = 0;
+    for (int i = 0; i < n; ++i) {
+        if (t[i].sig == 0)
+            continue;
+        unsigned __int128 v;
+        int sh = t[i].exp - q;
+        if (sh >= 0)
+            v = (unsigned __int128)t[i].sig << sh;
+        else if (-sh >= 64)
+            v = 0;
+        else
+            v = (unsigned __int128)(t[i].sig >> (-sh));
+        s += t[i].neg ? -(__int128)v : (__int128)v;
+    }
+    int neg = s < 0;
+    unsigned __int128 mag = neg ? (unsigned __int128)(-s) : (unsigned __int128)s;
+    return round_to_f32(neg, mag, q, m->final_rn);
+}
+
+/*
+ * One K16 tensor-core step for one element: acc' = C + sum_{k<16} a_k b_k,
+ * with C = acc when has_acc, else the step starts from nothing (the first
+ * step of a chunk, accumulator input disabled).
+ */
+float dgro_tc_k16(float acc, int32_t has_acc, const uint16_t *a, const uint16_t *b,
+                  const dgro_tc_model *m)
+{
+    term_t t[17];
+    int g = m->group;
+    float c = acc;
+    int have_c = has_acc;
+    for (int k0 = 0; k0 < 16; k0 += g) {
+        int n = 0;
+        if (have_c && m->acc_in_sum)
+            t[n++] = term_from_f32(c);
+        for (int k = k0; k < k0 + g && k < 16; ++k)
+            t[n++] = term_product(a[k], b[k]);
+        float s = fused_sum(t, n, m);
+        if (have_c && !m->acc_in_sum)
+            s = c + s;
+        c = s;
+        have_c = 1;
+    }
+    return c;
+}
+
+/* batch form of dgro_tc_k16 for model checks: a, b are [n][16] */
+void dgro_tc_k16_batch(int64_t n, const float *acc, const int32_t *has_acc,
+                       const uint16_t *a, const uint16_t *b, const dgro_tc_model *m,
+                       float *res)
+{
+    for (int64_t i = 0; i < n; ++i)
+        res[i] = dgro_tc_k16(acc[i], has_acc[i], a + 16 * i, b + 16 * i, m);
+}
+
+/*
+ * One chunk partial p_c for element (n, k): the chunk's tokens
+ * [t0, t0 + v) in steps of 16, ascending; tokens past v are zero; a step
+ * lying wholly past v is not taken; the first step starts from nothing.
+ */
+static float chunk_partial(const uint16_t *G, const uint16_t *X, int64_t N, int64_t K,
+                           int64_t t0, int64_t v, int64_t n, int64_t k, const dgro_tc_model *m)
+{
+    uint16_t a[16], b[16];
+    float acc = 0.0f;
+    int64_t steps = (v + 15) / 16;
+    for (int64_t s = 0; s < steps; ++s) {
+        for (int j = 0; j < 16; ++j) {
+            int64_t r = 16 * s + j;
+            if (r < v) {
+                a[j] = G[(t0 + r) * N + n];
+                b[j] = X[(t0 + r) * K + k];
+            } else {
+                a[j] = 0;
+                b[j] = 0;
+            }
+        }
+        acc = dgro_tc_k16(acc, s > 0, a, b, m);
+    }
+    return acc;
+}
+
+/*
+ * dW_e[n][k] = fold_c p_c (chunks of `chunk` tokens from the expert's first
+ * token, ascending), then main_grad[e][n][k] = main_grad + dW_e (one fp32
+ * rounding). FlashInfer PR #8924, "Design and numerics": for an fp32 out the
+ * result is RN32(out + dW) of the deterministic dW; PR #8602: an empty group
+ * leaves out bitwise unchanged. With sequential_into_out = 1 the partials are
+ * instead added to main_grad one by one (the rejected alternative reading,
+ * kept for comparison tests).
+ * G is [T][N], X is [T][K] (bf16 bits, rows grouped by expert), offs [E+1].
+ */
+static float wgrad_element(const uint16_t *G, const uint16_t *X, const int64_t *offs,
+                           int64_t N, int64_t K, int64_t chunk, int64_t e, int64_t n, int64_t k,
+                           float mg, int32_t sequential_into_out, const dgro_tc_model *m)
+{
+    int64_t t_begin = offs[e], t_end = offs[e + 1];
+    int64_t te = t_end - t_begin;
+    if (te <= 0)
+        return mg;
+    int64_t n_chunks = (te + chunk - 1) / chunk;
+    float f = 0.0f;
+    for (int64_t c = 0; c < n_chunks; ++c) {
+        int64_t t0 = t_begin + c * chunk;
+        int64_t v = (t_end - t0 < chunk) ? (t_end - t0) : chunk;
+        float p = chunk_partial(G, X, N, K, t0, v, n, k, m);
+        if (sequential_into_out)
+            mg = mg + p;
+        else
+            f = (c == 0) ? p : f + p;
+    }
+    return sequential_into_out ? mg : mg + f;
+}
+
+int dgro_grouped_wgrad_accumulate(const uint16_t *G, const uint16_t *X, const int64_t *offs,
+                                  int64_t E, int64_t N, int64_t K, float *main_grad,
+                                  int64_t chunk, int32_t sequential_into_out,
+                                  const dgro_tc_model *m)
+{
+    if (E < 0 || N < 0 || K < 0 || chunk <= 0 || chunk % 16 != 0)
+        return DGRO_ERR_ARG;
+    for (int64_t e = 0; e < E; ++e)
+        for (int64_t n = 0; n < N; ++n)
+            for (int64_t k = 0; k < K; ++k) {
+                float *o = &main_grad[(e * N + n) * K + k];
+                *o = wgrad_element(G, X, offs, N, K, chunk, e, n, k, *o, sequential_into_out, m);
+            }
+    return DGRO_OK;
+}
+
+/* the same for a list of elements (e, n, k): res[i] = updated main_grad value */
+int dgro_wgrad_elements(const uint16_t *G, const uint16_t *X, const int64_t *offs,
+                        int64_t N, int64_t K, const float *main_grad_in, int64_t chunk,
+                        int64_t count, const int64_t *e_idx, const int64_t *n_idx,
+                        const int64_t *k_idx, const dgro_tc_model *m, float *res)
+{
+    if (N < 0 || K < 0 || chunk <= 0 || chunk % 16 != 0)
+        return DGRO_ERR_ARG;
+    for (int64_t i = 0; i < count; ++i) {
+        int64_t e = e_idx[i], n = n_idx[i], k = k_idx[i];
+        float mg = main_grad_in[i];
+        res[i] = wgrad_element(G, X, offs, N, K, chunk, e, n, k, mg, 0, m);
+    }
+    return DGRO_OK;
+}
