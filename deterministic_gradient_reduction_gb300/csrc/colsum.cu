@@ -1,0 +1,362 @@
+// Ordered column sum: out[h] = fold_j pw_W(x[t][h] : t in tile j).
+//
+// Megatron-LM PR #8244 (ordered reduction for the fused pre-GDR gate
+// backward), description: every program writes its own FP32 partial sums and
+// the caller reduces them in order on the same stream. Here both halves run in
+// ONE launch:
+//   - producer CTAs, one per (tile of W tokens, block of columns): 16-byte
+//     vector loads, the pairwise tree of the tile (in registers over the rows a
+//     thread owns, then across threads in shared memory, always over aligned
+//     sub-windows so the tree is exactly the canonical one), one FP32 slot row
+//     per tile, then a release increment of the ready counter of its group of
+//     32 tiles;
+//   - folder CTAs (the first blockIdx values), one per block of FC columns:
+//     they wait (bounded) for each batch of tiles to be ready, stage the slots
+//     through shared memory with many loader warps, and fold them in ascending
+//     tile order on one thread per column. The fold overlaps the stream, so a
+//     long dependent chain of adds (65,536 tiles for 1 GiB of bf16 at H = 64)
+//     hides under the HBM time instead of following it.
+// Producers never wait, so the folders' waits always end.
+#include "dgr_common.cuh"
+
+namespace dgr {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kGroupTiles = 32;                 // tiles per ready counter
+constexpr int kFolderSmemBytes = 32 * 1024;     // double-buffered slot batches
+constexpr int kMaxFolders = 64;
+
+struct ColsumParams {
+    const char *x;
+    int64_t stride_b, stride_s;  // elements
+    int32_t S;
+    int32_t T;
+    int32_t H;
+    int32_t W;                   // tile rows (power of two)
+    int32_t n_tiles;
+    int32_t flat;                // tokens are at t * stride_s
+    // producer mapping
+    int32_t RG, CB, V, n_pcb;
+    // folder mapping
+    int32_t FC, n_fcb, batch;
+    float *out;
+    int32_t accumulate;
+    float *slots;                // [n_fcb][n_tiles][FC]
+    int32_t *counters;           // [n_groups]
+    WsHeader *hdr;
+};
+
+template <int DT>
+struct Elem;
+template <>
+struct Elem<DGR_DTYPE_BF16> {
+    static constexpr int kSize = 2;
+    static __device__ __forceinline__ float load1(const char *p) {
+        return bf16_bits_to_f32(*reinterpret_cast<const uint16_t *>(p));
+    }
+    static __device__ __forceinline__ void unpack(const uint4 &v, float *f) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+};
+template <>
+struct Elem<DGR_DTYPE_F32> {
+    static constexpr int kSize = 4;
+    static __device__ __forceinline__ float load1(const char *p) {
+        return *reinterpret_cast<const float *>(p);
+    }
+    static __device__ __forceinline__ void unpack(const uint4 &v, float *f) {
+        f[0] = __uint_as_float(v.x);
+        f[1] = __uint_as_float(v.y);
+        f[2] = __uint_as_float(v.z);
+        f[3] = __uint_as_float(v.w);
+    }
+};
+
+__device__ __forceinline__ int64_t token_offset(const ColsumParams &p, int32_t t) {
+    if (p.flat) return static_cast<int64_t>(t) * p.stride_s;
+    const int32_t b = t / p.S;
+    const int32_t s = t - b * p.S;
+    return static_cast<int64_t>(b) * p.stride_b + static_cast<int64_t>(s) * p.stride_s;
+}
+
+// One producer unit: the tile partials of tile j for column vectors
+// [cv0, cv0 + CB). VE = elements per vector (8 bf16 or 4 fp32 for 16-byte
+// loads, 1 for the scalar path); RPT = rows a thread owns.
+template <int DT, int VE, int RPT>
+__device__ void produce(const ColsumParams &p, int unit, float *sm) {
+    using E = Elem<DT>;
+    const int j = unit / p.n_pcb;
+    const int pcb = unit - j * p.n_pcb;
+    const int tid = threadIdx.x;
+    const int g = tid / p.CB;          // row group
+    const int v = tid - g * p.CB;      // column vector within the block
+    const int cv0 = pcb * p.CB;
+    const int cb_here = min(p.CB, p.V - cv0);
+    const int64_t t0 = static_cast<int64_t>(j) * p.W;
+    const int count = static_cast<int>(min(static_cast<int64_t>(p.W), p.T - t0));
+    const int groups_present = (count + RPT - 1) / RPT;
+    const bool active = g < p.RG && v < cb_here;
+    const int nrows = active ? max(0, min(RPT, count - g * RPT)) : 0;
+
+    float leaf[RPT][VE];
+    if (nrows > 0) {
+        const int c0 = (cv0 + v) * VE;
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            if (r < nrows) {
+                const int32_t t = static_cast<int32_t>(t0) + g * RPT + r;
+                const char *src = p.x + (token_offset(p, t) + c0) * E::kSize;
+                if constexpr (VE == 1) {
+                    leaf[r][0] = E::load1(src);
+                } else {
+                    E::unpack(ldg_nc_v4(src), leaf[r]);
+                }
+            }
+        }
+        // in-register levels of the tree: aligned windows of 2s rows
+#pragma unroll
+        for (int s = 1; s < RPT; s *= 2) {
+#pragma unroll
+            for (int r = 0; r + s < RPT; r += 2 * s) {
+                if (r + s < nrows) {
+#pragma unroll
+                    for (int e = 0; e < VE; ++e) leaf[r][e] = __fadd_rn(leaf[r][e], leaf[r + s][e]);
+                }
+            }
+        }
+        float *dst = sm + (g * p.CB + v) * VE;
+#pragma unroll
+        for (int e = 0; e < VE; ++e) dst[e] = leaf[0][e];
+    }
+    __syncthreads();
+    // shared-memory levels: row group g absorbs g + s when both are present
+    for (int s = 1; s < p.RG; s *= 2) {
+        if (active && (g % (2 * s)) == 0 && g + s < groups_present) {
+            float *a = sm + (g * p.CB + v) * VE;
+            const float *b = sm + ((g + s) * p.CB + v) * VE;
+#pragma unroll
+            for (int e = 0; e < VE; ++e) a[e] = __fadd_rn(a[e], b[e]);
+        }
+        __syncthreads();
+    }
+    if (active && g == 0) {
+        const float *root = sm + v * VE;
+#pragma unroll
+        for (int e = 0; e < VE; ++e) {
+            const int c = (cv0 + v) * VE + e;
+            if (c < p.H) {
+                const int f = c / p.FC;
+                p.slots[(static_cast<int64_t>(f) * p.n_tiles + j) * p.FC + (c - f * p.FC)] = root[e];
+            }
+        }
+        __threadfence();
+    }
+    __syncthreads();
+    if (tid == 0) atomicAdd(&p.counters[j / kGroupTiles], 1);
+}
+
+// One folder CTA: columns [f*FC, f*FC + FC), all tiles in ascending order.
+__device__ void fold(const ColsumParams &p, int f, float *sm) {
+    __shared__ int abort_flag;
+    __shared__ int ticket;
+    const int tid = threadIdx.x;
+    const int chain_threads = ((p.FC + 31) / 32) * 32;
+    const int loader_threads = kThreads - chain_threads;
+    const int ltid = tid - chain_threads;  // loader index (>= 0 for loaders)
+    const int n_batches = (p.n_tiles + p.batch - 1) / p.batch;
+    const float *src = p.slots + static_cast<int64_t>(f) * p.n_tiles * p.FC;
+    const int col = f * p.FC + tid;
+    if (tid == 0) abort_flag = 0;
+    __syncthreads();
+
+    // Loaders: wait for batch i's tile groups, then copy its slots to buffer i%2.
+    auto load = [&](int i) {
+        const int j0 = i * p.batch;
+        const int j1 = min(j0 + p.batch, p.n_tiles);
+        if (ltid == 0) {
+            for (int grp = j0 / kGroupTiles; grp <= (j1 - 1) / kGroupTiles; ++grp) {
+                const int tiles_in_group = min(kGroupTiles, p.n_tiles - grp * kGroupTiles);
+                if (!wait_counter_geq(&p.counters[grp], tiles_in_group * p.n_pcb)) {
+                    record_error(p.hdr, DGR_ERR_TIMEOUT, 1);
+                    abort_flag = 1;
+                    break;
+                }
+            }
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(loader_threads) : "memory");
+        if (abort_flag) return;
+        const int n4 = (j1 - j0) * p.FC / 4;
+        const float4 *s4 = reinterpret_cast<const float4 *>(src + static_cast<int64_t>(j0) * p.FC);
+        float4 *d4 = reinterpret_cast<float4 *>(sm + (i & 1) * p.batch * p.FC);
+        for (int q = ltid; q < n4; q += loader_threads) d4[q] = __ldcg(s4 + q);
+    };
+
+    if (ltid >= 0) load(0);
+    __syncthreads();
+    float F = 0.0f;
+    for (int i = 0; i < n_batches; ++i) {
+        if (abort_flag) break;
+        if (ltid >= 0) {
+            if (i + 1 < n_batches) load(i + 1);
+        } else if (tid < p.FC && col < p.H) {
+            const float *b = sm + (i & 1) * p.batch * p.FC + tid;
+            const int cnt = min(p.batch, p.n_tiles - i * p.batch);
+            int k = 0;
+            if (i == 0) {
+                F = b[0];
+                k = 1;
+            }
+#pragma unroll 16
+            for (; k < cnt; ++k) F = __fadd_rn(F, b[k * p.FC]);
+        }
+        __syncthreads();
+    }
+    if (abort_flag) return;
+    if (tid < p.FC && col < p.H) p.out[col] = p.accumulate ? __fadd_rn(p.out[col], F) : F;
+
+    // The last folder to finish resets the ready counters for the next call:
+    // every producer has published by now (all groups were consumed).
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        ticket = atomicAdd(&p.hdr->pad[0], 1);
+    }
+    __syncthreads();
+    if (ticket == p.n_fcb - 1) {
+        const int n_groups = (p.n_tiles + kGroupTiles - 1) / kGroupTiles;
+        for (int q = tid; q < n_groups; q += kThreads) p.counters[q] = 0;
+        if (tid == 0) p.hdr->pad[0] = 0;
+    }
+}
+
+template <int DT, int VE, int RPT>
+__global__ void __launch_bounds__(kThreads) colsum_kernel(const ColsumParams p) {
+    extern __shared__ __align__(16) float smem[];
+    if (static_cast<int>(blockIdx.x) < p.n_fcb) {
+        fold(p, blockIdx.x, smem);
+    } else {
+        produce<DT, VE, RPT>(p, blockIdx.x - p.n_fcb, smem);
+    }
+}
+
+template <int DT, int VE>
+dgr_status launch_rpt(const ColsumParams &p, int rpt, int grid, cudaStream_t st) {
+    switch (rpt) {
+        case 1: colsum_kernel<DT, VE, 1><<<grid, kThreads, kFolderSmemBytes, st>>>(p); break;
+        case 2: colsum_kernel<DT, VE, 2><<<grid, kThreads, kFolderSmemBytes, st>>>(p); break;
+        case 4: colsum_kernel<DT, VE, 4><<<grid, kThreads, kFolderSmemBytes, st>>>(p); break;
+        case 8: colsum_kernel<DT, VE, 8><<<grid, kThreads, kFolderSmemBytes, st>>>(p); break;
+        case 16: colsum_kernel<DT, VE, 16><<<grid, kThreads, kFolderSmemBytes, st>>>(p); break;
+        default: return DGR_ERR_INVALID_ARG;
+    }
+    return launch_status();
+}
+
+struct Layout {
+    int32_t n_tiles, n_groups, FC, n_fcb;
+    size_t counters_off, slots_off, total;
+};
+
+Layout colsum_layout(int64_t T, int64_t H, int32_t W) {
+    Layout L{};
+    L.n_tiles = static_cast<int32_t>((T + W - 1) / W);
+    L.n_groups = (L.n_tiles + kGroupTiles - 1) / kGroupTiles;
+    const int64_t fcb8 = (H + 7) / 8;
+    L.FC = static_cast<int32_t>(8 * ((fcb8 + kMaxFolders - 1) / kMaxFolders));
+    if (L.FC < 8) L.FC = 8;
+    L.n_fcb = static_cast<int32_t>((H + L.FC - 1) / L.FC);
+    L.counters_off = sizeof(WsHeader);
+    L.slots_off = L.counters_off + align_up(static_cast<size_t>(L.n_groups) * 4);
+    L.total = L.slots_off + align_up(static_cast<size_t>(L.n_fcb) * L.n_tiles * L.FC * 4);
+    return L;
+}
+
+}  // namespace
+}  // namespace dgr
+
+using namespace dgr;
+
+extern "C" size_t dgr_colsum_workspace_bytes(int64_t T, int64_t H, int32_t tile_rows) {
+    if (T < 0 || H < 0 || H > 4096 || T > INT32_MAX || !is_pow2(tile_rows) || tile_rows > 4096) return 0;
+    return colsum_layout(T, H, tile_rows).total;
+}
+
+extern "C" dgr_status dgr_ordered_colsum(const void *x, int32_t dtype, int64_t B, int64_t S, int64_t H,
+                                         int64_t stride_b, int64_t stride_s, float *out,
+                                         int32_t accumulate, int32_t tile_rows, void *ws, size_t ws_bytes,
+                                         void *stream) {
+    if (dtype != DGR_DTYPE_BF16 && dtype != DGR_DTYPE_F32) return DGR_ERR_INVALID_ARG;
+    if (B < 0 || S < 0 || H < 0 || stride_b < 0 || stride_s < 0) return DGR_ERR_INVALID_ARG;
+    if (!is_pow2(tile_rows) || tile_rows > 4096) return DGR_ERR_INVALID_ARG;
+    if (H > 4096 || (S > 0 && B > INT32_MAX / S)) return DGR_ERR_UNSUPPORTED;
+    const int64_t T = B * S;
+    if (H == 0) return DGR_OK;
+    if (!out || (T > 0 && !x)) return DGR_ERR_INVALID_ARG;
+    if (!aligned(out, 4)) return DGR_ERR_MISALIGNED;
+    const Layout L = colsum_layout(T, H, tile_rows);
+    if (T > 0) {
+        if (!ws) return DGR_ERR_INVALID_ARG;
+        if (ws_bytes < L.total) return DGR_ERR_WORKSPACE_TOO_SMALL;
+        if (!aligned(ws, kAlign)) return DGR_ERR_MISALIGNED;
+    }
+    const int esize = dtype == DGR_DTYPE_BF16 ? 2 : 4;
+    if (x && !aligned(x, esize)) return DGR_ERR_MISALIGNED;
+    const int64_t x_extent = T > 0 ? ((B - 1) * stride_b + (S - 1) * stride_s + H) * esize : 0;
+    if (ranges_overlap(out, H * 4, x, x_extent)) return DGR_ERR_ALIAS;
+    if (T > 0 && ranges_overlap(out, H * 4, ws, L.total)) return DGR_ERR_ALIAS;
+    dgr_status st = check_device();
+    if (st != DGR_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        if (accumulate) return DGR_OK;
+        return cudaMemsetAsync(out, 0, H * 4, s) == cudaSuccess ? DGR_OK : DGR_ERR_CUDA;
+    }
+
+    ColsumParams p{};
+    p.x = static_cast<const char *>(x);
+    p.stride_b = stride_b;
+    p.stride_s = stride_s;
+    p.S = static_cast<int32_t>(S);
+    p.T = static_cast<int32_t>(T);
+    p.H = static_cast<int32_t>(H);
+    p.W = tile_rows;
+    p.n_tiles = L.n_tiles;
+    p.flat = (B == 1 || stride_b == S * stride_s) ? 1 : 0;
+    const int vec = 16 / esize;
+    const bool vec_ok = aligned(x, 16) && (H % vec) == 0 && (stride_s * esize) % 16 == 0 &&
+                        (stride_b * esize) % 16 == 0;
+    const int VE = vec_ok ? vec : 1;
+    p.V = static_cast<int32_t>((H + VE - 1) / VE);
+    p.CB = p.V < 32 ? p.V : 32;
+    int rpt = 1;
+    while (rpt < 16 && rpt < tile_rows && (tile_rows / rpt) * p.CB > kThreads) rpt *= 2;
+    if ((tile_rows / rpt) * p.CB > kThreads) p.CB = kThreads / (tile_rows / rpt);
+    p.RG = tile_rows / rpt;
+    p.n_pcb = (p.V + p.CB - 1) / p.CB;
+    p.FC = L.FC;
+    p.n_fcb = L.n_fcb;
+    p.batch = kFolderSmemBytes / (2 * p.FC * 4);
+    p.out = out;
+    p.accumulate = accumulate ? 1 : 0;
+    char *w = static_cast<char *>(ws);
+    p.hdr = reinterpret_cast<WsHeader *>(w);
+    p.counters = reinterpret_cast<int32_t *>(w + L.counters_off);
+    p.slots = reinterpret_cast<float *>(w + L.slots_off);
+    // producer scratch: RG * CB * VE floats must fit the launch's shared memory
+    if (static_cast<size_t>(p.RG) * p.CB * VE * 4 > static_cast<size_t>(kFolderSmemBytes))
+        return DGR_ERR_UNSUPPORTED;
+    const int64_t grid = static_cast<int64_t>(p.n_fcb) + static_cast<int64_t>(L.n_tiles) * p.n_pcb;
+    if (grid > INT32_MAX) return DGR_ERR_UNSUPPORTED;
+    if (dtype == DGR_DTYPE_BF16) {
+        return VE == 8 ? launch_rpt<DGR_DTYPE_BF16, 8>(p, rpt, static_cast<int>(grid), s)
+                       : launch_rpt<DGR_DTYPE_BF16, 1>(p, rpt, static_cast<int>(grid), s);
+    }
+    return VE == 4 ? launch_rpt<DGR_DTYPE_F32, 4>(p, rpt, static_cast<int>(grid), s)
+                   : launch_rpt<DGR_DTYPE_F32, 1>(p, rpt, static_cast<int>(grid), s);
+}

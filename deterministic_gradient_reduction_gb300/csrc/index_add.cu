@@ -1,0 +1,612 @@
+// Deterministic index_add: stable radix sort by destination, then segmented
+// pairwise sums in original order, padding routed to the dummy row R.
+//
+// Megatron-LM PR #7441 (DSv4 --deterministic-mode), Source 3: the atomic-free
+// dK is an index_add done as a stable sort plus a (prefix) sum, with padding
+// slots spread over dummy rows that the caller drops. Four launches:
+//   K1 count   - map idx to keys (idx outside [0, R) -> R; outside [-1, R) is
+//                counted), per-block histograms of the key's high byte; the
+//                last block to finish scans them (digit-major) into per-block
+//                scatter offsets and bucket starts.
+//   K2 scatter - stable scatter by the high byte: inside a block, elements are
+//                ranked in original order with warp match/ballot and per-warp
+//                digit counters, so equal digits keep their input order.
+//   K3 bucket  - one block per high-byte bucket: counting sort by the low byte
+//                (stable, same ranking), which also yields seg_start[] for the
+//                bucket's 256 keys; a bucket holding one key is copied as is.
+//   K4 segsum  - one warp per destination row sums its members (in original
+//                order) by the pairwise tree over tiles of 128 members and folds
+//                the tiles in order, then out[r] += sum with one rounding.
+//                Rows with more than 8 tiles are split: one warp per 32-member
+//                quarter of each tile writes a slot, and the last warp to
+//                arrive (an integer ticket) folds them in tile order.
+// Integer atomics only count; no floating-point value depends on timing.
+#include "dgr_common.cuh"
+
+namespace dgr {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kItems = 8;
+constexpr int kBlockElems = kThreads * kItems;  // 2048 elements per sort block
+constexpr int kDigits = 256;
+constexpr int kSegTile = 128;
+constexpr int kWarpMaxTiles = 8;                // rows up to 1024 members: one warp
+constexpr int kSub = 32;                         // split-row work unit (a quarter tile)
+constexpr int kStackLevels = 5;                  // group stack depth for 16 groups of 8
+
+struct IdxParams {
+    const int32_t *idx;
+    int32_t N, R, D;
+    int32_t nb;             // sort blocks
+    int32_t n_buckets;      // high-byte buckets covering keys 0..R
+    int32_t n_pblk;         // 128-position blocks (split-row warps = 4 * n_pblk)
+    int32_t seg_tile;
+    const float *src;
+    int64_t ld_src;
+    float *out;
+    int64_t ld_out;
+    int32_t *bad_count;
+    int32_t *keys_a, *vals_a, *perm, *skey, *hist, *offs, *bucket_start, *seg_start, *tickets;
+    float *slots;
+    WsHeader *hdr;
+};
+
+__device__ __forceinline__ int32_t map_key(int32_t v, int32_t R, bool &bad) {
+    if (v >= 0 && v < R) return v;
+    bad = (v != -1);
+    return R;
+}
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// ---------------------------------------------------------------------------
+// K1: high-byte histograms per block; the last block scans them.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) count_kernel(const IdxParams p) {
+    __shared__ int32_t h[kDigits];
+    __shared__ int32_t base[kDigits + 1];
+    __shared__ int32_t bad_block;
+    __shared__ int is_last;
+    const int tid = threadIdx.x;
+    const int b = blockIdx.x;
+    h[tid] = 0;
+    if (tid == 0) bad_block = 0;
+    __syncthreads();
+    int my_bad = 0;
+    for (int i = tid; i < kBlockElems; i += kThreads) {
+        const int64_t e = static_cast<int64_t>(b) * kBlockElems + i;
+        if (e < p.N) {
+            bool bad = false;
+            const int32_t k = map_key(p.idx[e], p.R, bad);
+            my_bad += bad ? 1 : 0;
+            atomicAdd(&h[k >> 8], 1);
+        }
+    }
+    if (my_bad) atomicAdd(&bad_block, my_bad);
+    __syncthreads();
+    p.hist[static_cast<int64_t>(tid) * p.nb + b] = h[tid];
+    if (tid == 0 && bad_block) atomicAdd(&p.hdr->pad[2], bad_block);
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) is_last = atomicAdd(&p.hdr->pad[1], 1) == p.nb - 1;
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    // digit-major exclusive scan: offs[d][b] = sum of digits < d + counts of d in blocks < b
+    int32_t total = 0;
+    for (int bb = 0; bb < p.nb; ++bb) total += __ldcg(&p.hist[static_cast<int64_t>(tid) * p.nb + bb]);
+    h[tid] = total;
+    __syncthreads();
+    if (tid == 0) {
+        int32_t run = 0;
+        for (int d = 0; d < kDigits; ++d) {
+            base[d] = run;
+            run += h[d];
+        }
+        base[kDigits] = run;
+    }
+    __syncthreads();
+    int32_t run = base[tid];
+    for (int bb = 0; bb < p.nb; ++bb) {
+        const int64_t q = static_cast<int64_t>(tid) * p.nb + bb;
+        p.offs[q] = run;
+        run += __ldcg(&p.hist[q]);
+    }
+    p.bucket_start[tid] = base[tid];
+    if (tid == 0) {
+        p.bucket_start[kDigits] = base[kDigits];
+        const int32_t bad = atomicAdd(&p.hdr->pad[2], 0);
+        if (p.bad_count) *p.bad_count = bad;
+        p.hdr->pad[2] = 0;
+        p.hdr->pad[1] = 0;
+    }
+}
+
+// Stable in-block ranking: warp w owns elements [w*256, w*256 + 256) of the
+// block in 8 rounds of 32 (round-major, lane order = element order). Returns
+// each element's rank among equal digits inside its warp; cnt[w][d] ends as
+// the warp's digit counts.
+__device__ __forceinline__ void warp_rank(int digit, bool valid, int32_t (*cnt)[kDigits], int w, int32_t &rank) {
+    const int d = valid ? digit : kDigits;  // invalid lanes match each other only
+    const unsigned peers = __match_any_sync(0xffffffffu, d);
+    const int before = __popc(peers & lanemask_lt());
+    const int32_t base = valid ? cnt[w][d] : 0;
+    __syncwarp();
+    if (valid && before == 0) cnt[w][d] = base + __popc(peers);
+    __syncwarp();
+    rank = base + before;
+}
+
+// ---------------------------------------------------------------------------
+// K2: stable scatter by the high byte.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) scatter_high_kernel(const IdxParams p) {
+    __shared__ int32_t cnt[kWarps][kDigits];
+    __shared__ int32_t pre[kWarps][kDigits];
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+    const int b = blockIdx.x;
+    for (int q = tid; q < kWarps * kDigits; q += kThreads) (&cnt[0][0])[q] = 0;
+    __syncthreads();
+    int32_t key[kItems], rank[kItems];
+#pragma unroll
+    for (int r = 0; r < kItems; ++r) {
+        const int64_t e = static_cast<int64_t>(b) * kBlockElems + w * (kItems * 32) + r * 32 + lane;
+        const bool valid = e < p.N;
+        bool bad = false;
+        key[r] = valid ? map_key(p.idx[e], p.R, bad) : -1;
+        warp_rank(valid ? (key[r] >> 8) : 0, valid, cnt, w, rank[r]);
+    }
+    __syncthreads();
+    {
+        int32_t run = 0;
+        for (int ww = 0; ww < kWarps; ++ww) {
+            pre[ww][tid] = run;
+            run += cnt[ww][tid];
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < kItems; ++r) {
+        const int64_t e = static_cast<int64_t>(b) * kBlockElems + w * (kItems * 32) + r * 32 + lane;
+        if (e < p.N) {
+            const int d = key[r] >> 8;
+            const int32_t pos = p.offs[static_cast<int64_t>(d) * p.nb + b] + pre[w][d] + rank[r];
+            p.keys_a[pos] = key[r];
+            p.vals_a[pos] = static_cast<int32_t>(e);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// K3: per bucket, stable counting sort by the low byte, and segment starts.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) bucket_kernel(const IdxParams p) {
+    __shared__ int32_t h[kDigits];
+    __shared__ int32_t base[kDigits];
+    __shared__ int32_t cnt[kWarps][kDigits];
+    __shared__ int32_t pre[kWarps][kDigits];
+    __shared__ int uniform;
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+    const int d = blockIdx.x;
+    const int32_t bs = p.bucket_start[d];
+    const int32_t be = p.bucket_start[d + 1];
+    h[tid] = 0;
+    if (tid == 0) uniform = 0;
+    __syncthreads();
+    for (int32_t i = bs + tid; i < be; i += kThreads) atomicAdd(&h[p.keys_a[i] & 255], 1);
+    __syncthreads();
+    if (tid == 0) {
+        int32_t run = 0;
+        for (int q = 0; q < kDigits; ++q) {
+            const int32_t c = h[q];
+            base[q] = bs + run;
+            if (c == be - bs && c > 0) uniform = 1;
+            run += c;
+        }
+    }
+    __syncthreads();
+    const int32_t k = d * 256 + tid;
+    if (k <= p.R) p.seg_start[k] = base[tid];
+    if (k == p.R) p.seg_start[p.R + 1] = p.N;
+    if (uniform) {  // one key: the stable order is the input order
+        for (int32_t i = bs + tid; i < be; i += kThreads) {
+            p.perm[i] = p.vals_a[i];
+            p.skey[i] = p.keys_a[i];
+        }
+        return;
+    }
+    for (int32_t c0 = bs; c0 < be; c0 += kBlockElems) {
+        for (int q = tid; q < kWarps * kDigits; q += kThreads) (&cnt[0][0])[q] = 0;
+        __syncthreads();
+        int32_t key[kItems], val[kItems], rank[kItems];
+#pragma unroll
+        for (int r = 0; r < kItems; ++r) {
+            const int32_t e = c0 + w * (kItems * 32) + r * 32 + lane;
+            const bool valid = e < be;
+            key[r] = valid ? p.keys_a[e] : 0;
+            val[r] = valid ? p.vals_a[e] : 0;
+            warp_rank(key[r] & 255, valid, cnt, w, rank[r]);
+        }
+        __syncthreads();
+        {
+            int32_t run = 0;
+            for (int ww = 0; ww < kWarps; ++ww) {
+                pre[ww][tid] = run;
+                run += cnt[ww][tid];
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int r = 0; r < kItems; ++r) {
+            const int32_t e = c0 + w * (kItems * 32) + r * 32 + lane;
+            if (e < be) {
+                const int lo = key[r] & 255;
+                const int32_t pos = base[lo] + pre[w][lo] + rank[r];
+                p.perm[pos] = val[r];
+                p.skey[pos] = key[r];
+            }
+        }
+        __syncthreads();
+        {
+            int32_t add = 0;
+            for (int ww = 0; ww < kWarps; ++ww) add += cnt[ww][tid];
+            base[tid] += add;
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// K4: segmented sums.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float4 f4add(float4 a, float4 b) {
+    return make_float4(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y), __fadd_rn(a.z, b.z), __fadd_rn(a.w, b.w));
+}
+
+__device__ __forceinline__ float4 ld_src4(const IdxParams &p, int32_t row, int col) {
+    const uint4 u = ldg_nc_v4(p.src + static_cast<int64_t>(row) * p.ld_src + col);
+    return make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w));
+}
+
+// Pairwise tree over the members [q0, q0 + cnt) of a window of 8..128
+// members (cnt <= 128), in sorted-position order (= original order within a
+// row). The window's width does not matter: leaves past cnt are absent, and
+// an absent right half passes its left half up unchanged. Each lane sums its 4 columns starting at `col` (col < 0: the
+// lane only joins the shuffles). Groups of 8 members are summed in registers;
+// a binary-counter stack over groups (in this warp's shared-memory rows `stk`)
+// gives the higher levels; absent members (past cnt) are skipped, which is the
+// canonical tail rule.
+__device__ __forceinline__ float4 window_sum(const IdxParams &p, int32_t q0, int cnt, int col, int lane,
+                                          float4 (*stk)[32]) {
+    constexpr int kM = kSegTile / 32;
+    int32_t pidx[kM];
+#pragma unroll
+    for (int m = 0; m < kM; ++m) {
+        const int j = m * 32 + lane;
+        pidx[m] = (j < cnt) ? p.perm[q0 + j] : 0;
+    }
+    const int n_groups = (cnt + 7) / 8;
+#pragma unroll 1
+    for (int gi = 0; gi < n_groups; ++gi) {
+        int32_t mine = pidx[0];
+#pragma unroll
+        for (int m = 1; m < kM; ++m)
+            if ((gi >> 2) == m) mine = pidx[m];
+        float4 v[8];
+        const int nu = min(8, cnt - gi * 8);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int32_t row = __shfl_sync(0xffffffffu, mine, (gi & 3) * 8 + u);
+            if (u < nu && col >= 0) v[u] = ld_src4(p, row, col);
+        }
+#pragma unroll
+        for (int s = 1; s < 8; s *= 2) {
+#pragma unroll
+            for (int r = 0; r + s < 8; r += 2 * s)
+                if (r + s < nu) v[r] = f4add(v[r], v[r + s]);
+        }
+        // push group gi: carry through the levels where gi has a one bit
+        float4 cur = v[0];
+        int l = 0;
+        while ((gi >> l) & 1) {
+            cur = f4add(stk[l][lane], cur);
+            ++l;
+        }
+        stk[l][lane] = cur;
+    }
+    // ragged end: combine the complete blocks of the set bits of n_groups,
+    // smallest first, each larger (earlier) block on the left
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    bool have = false;
+    for (int l = 0; (n_groups >> l) != 0; ++l) {
+        if ((n_groups >> l) & 1) {
+            acc = have ? f4add(stk[l][lane], acc) : stk[l][lane];
+            have = true;
+        }
+    }
+    return acc;
+}
+
+__device__ __forceinline__ void add_out(const IdxParams &p, int32_t r, int col, float4 F) {
+    float4 *o = reinterpret_cast<float4 *>(p.out + static_cast<int64_t>(r) * p.ld_out + col);
+    const float4 a = *o;
+    *o = f4add(a, F);
+}
+
+// Sub-slot of quarter q of the tile starting at sorted position p0 (tile index t):
+// within a 128-position block at most two split-row tiles start, the last tile
+// of one row and the first of the next, so the parity bit keeps them apart.
+__device__ __forceinline__ int64_t sub_slot(int32_t p0, int32_t t, int q) {
+    return (static_cast<int64_t>(p0 >> 7) * 2 + (t == 0 ? 1 : 0)) * 4 + q;
+}
+
+__device__ void split_row_unit(const IdxParams &p, int32_t unit, int lane, float4 (*stk)[32]) {
+    const int32_t pb = unit >> 2;
+    const int q = unit & 3;
+    for (int m = 0; m < 4; ++m) {
+        const int32_t pos = pb * 128 + m * 32 + lane;
+        bool start = false;
+        int32_t key = 0, s = 0, e = 0;
+        if (pos < p.N) {
+            key = p.skey[pos];
+            s = p.seg_start[key];
+            e = p.seg_start[key + 1];
+            start = (e - s > kWarpMaxTiles * kSegTile) && (((pos - s) & (kSegTile - 1)) == 0);
+        }
+        unsigned mask = __ballot_sync(0xffffffffu, start);
+        while (mask) {
+            const int src_lane = __ffs(mask) - 1;
+            mask &= mask - 1;
+            const int32_t p0 = __shfl_sync(0xffffffffu, pos, src_lane);
+            const int32_t k = __shfl_sync(0xffffffffu, key, src_lane);
+            const int32_t s0 = __shfl_sync(0xffffffffu, s, src_lane);
+            const int32_t e0 = __shfl_sync(0xffffffffu, e, src_lane);
+            const int32_t t = (p0 - s0) >> 7;
+            const int cnt_tile = min(kSegTile, e0 - p0);
+            const int cnt = min(kSub, cnt_tile - q * kSub);
+            const int32_t n_tiles = (e0 - s0 + kSegTile - 1) / kSegTile;
+            if (cnt > 0) {
+                for (int c0 = 0; c0 < p.D; c0 += 128) {
+                    const int col = c0 + lane * 4;
+                    const float4 v = window_sum(p, p0 + q * kSub, cnt, col < p.D ? col : -1, lane, stk);
+                    if (col < p.D)
+                        *reinterpret_cast<float4 *>(p.slots + sub_slot(p0, t, q) * p.D + col) = v;
+                }
+            }
+            __threadfence();
+            __syncwarp();
+            int tk = 0;
+            if (lane == 0) tk = atomicAdd(&p.tickets[k], 1);
+            tk = __shfl_sync(0xffffffffu, tk, 0);
+            // every quarter of every tile arrives once, present or not
+            if (tk != n_tiles * 4 - 1) continue;
+            __threadfence();
+            for (int c0 = 0; c0 < p.D; c0 += 128) {
+                const int col = c0 + lane * 4;
+                if (col >= p.D) continue;
+                float4 F = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int32_t tt = 0; tt < n_tiles; ++tt) {
+                    const int32_t pt = s0 + tt * kSegTile;
+                    const int ct = min(kSegTile, e0 - pt);
+                    float4 sq[4];
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq)
+                        if (qq * kSub < ct)
+                            sq[qq] = __ldcg(reinterpret_cast<const float4 *>(p.slots + sub_slot(pt, tt, qq) * p.D + col));
+                    // the top two levels of the tile's tree over its quarters
+                    float4 a = sq[0];
+                    if (ct > 32) a = f4add(a, sq[1]);
+                    if (ct > 64) {
+                        float4 c = sq[2];
+                        if (ct > 96) c = f4add(c, sq[3]);
+                        a = f4add(a, c);
+                    }
+                    F = (tt == 0) ? a : f4add(F, a);
+                }
+                add_out(p, k, col, F);
+            }
+            if (lane == 0) p.tickets[k] = 0;
+        }
+    }
+}
+
+__device__ void row_unit(const IdxParams &p, int32_t r, int lane, float4 (*stk)[32]) {
+    const int32_t s = p.seg_start[r];
+    const int32_t e = p.seg_start[r + 1];
+    const int32_t n = e - s;
+    if (n <= 0) return;
+    if (p.seg_tile == 1) {  // purely sequential fold in original order
+        for (int c0 = 0; c0 < p.D; c0 += 128) {
+            const int col = c0 + lane * 4;
+            float4 F = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int32_t q0 = 0; q0 < n; q0 += 32) {
+                const int32_t mine = (q0 + lane < n) ? p.perm[s + q0 + lane] : 0;
+                const int cnt = min(32, n - q0);
+#pragma unroll 4
+                for (int u = 0; u < cnt; ++u) {
+                    const int32_t row = __shfl_sync(0xffffffffu, mine, u);
+                    if (col < p.D) {
+                        const float4 v = ld_src4(p, row, col);
+                        F = (q0 + u == 0) ? v : f4add(F, v);
+                    }
+                }
+            }
+            if (col < p.D) add_out(p, r, col, F);
+        }
+        return;
+    }
+    const int W = p.seg_tile;
+    const int32_t n_tiles = (n + W - 1) / W;
+    if (W == kSegTile && n_tiles > kWarpMaxTiles) return;  // split-row units handle it
+    for (int c0 = 0; c0 < p.D; c0 += 128) {
+        const int col = c0 + lane * 4;
+        const int lcol = col < p.D ? col : -1;
+        float4 F = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int32_t t = 0; t < n_tiles; ++t) {
+            const int cnt = min(W, n - t * W);
+            const float4 P = window_sum(p, s + t * W, cnt, lcol, lane, stk);
+            F = (t == 0) ? P : f4add(F, P);
+        }
+        if (col < p.D) add_out(p, r, col, F);
+    }
+}
+
+// Small widths (2, 4): a tree over 2 or 4 members, per lane, no stack.
+__device__ void row_unit_small(const IdxParams &p, int32_t r, int lane) {
+    const int32_t s = p.seg_start[r];
+    const int32_t e = p.seg_start[r + 1];
+    const int32_t n = e - s;
+    if (n <= 0) return;
+    const int W = p.seg_tile;
+    for (int c0 = 0; c0 < p.D; c0 += 128) {
+        const int col = c0 + lane * 4;
+        float4 F = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int32_t t0 = 0; t0 < n; t0 += W) {
+            const int cnt = min(W, n - t0);
+            float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0, v2 = v0, v3 = v0;
+            if (col < p.D) {
+                v0 = ld_src4(p, p.perm[s + t0], col);
+                if (cnt > 1) v1 = ld_src4(p, p.perm[s + t0 + 1], col);
+                if (cnt > 2) v2 = ld_src4(p, p.perm[s + t0 + 2], col);
+                if (cnt > 3) v3 = ld_src4(p, p.perm[s + t0 + 3], col);
+                if (cnt > 1) v0 = f4add(v0, v1);
+                if (cnt > 3) v2 = f4add(v2, v3);
+                if (cnt > 2) v0 = f4add(v0, v2);
+                F = (t0 == 0) ? v0 : f4add(F, v0);
+            }
+        }
+        if (col < p.D) add_out(p, r, col, F);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 3) segsum_kernel(const IdxParams p) {
+    __shared__ float4 stack[kWarps][kStackLevels][32];
+    const int lane = threadIdx.x & 31;
+    float4 (*stk)[32] = stack[threadIdx.x >> 5];
+    const int64_t wg = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+    const int64_t n_split = (p.seg_tile == kSegTile) ? static_cast<int64_t>(p.n_pblk) * 4 : 0;
+    if (wg < n_split) {
+        split_row_unit(p, static_cast<int32_t>(wg), lane, stk);
+        return;
+    }
+    const int64_t r = wg - n_split;
+    if (r > p.R) return;
+    if (p.seg_tile == 2 || p.seg_tile == 4) row_unit_small(p, static_cast<int32_t>(r), lane);
+    else row_unit(p, static_cast<int32_t>(r), lane, stk);
+}
+
+struct IdxLayout {
+    int32_t nb, n_buckets, n_pblk;
+    size_t keys_a, vals_a, perm, skey, hist, offs, bucket_start, seg_start, tickets, slots, total;
+};
+
+IdxLayout idx_layout(int64_t N, int64_t R, int64_t D) {
+    IdxLayout L{};
+    L.nb = static_cast<int32_t>((N + kBlockElems - 1) / kBlockElems);
+    L.n_buckets = static_cast<int32_t>((R + 1 + 255) / 256);
+    L.n_pblk = static_cast<int32_t>((N + 127) / 128);
+    size_t o = sizeof(WsHeader);
+    auto take = [&](size_t bytes) {
+        size_t at = o;
+        o += align_up(bytes);
+        return at;
+    };
+    L.keys_a = take(N * 4);
+    L.vals_a = take(N * 4);
+    L.perm = take(N * 4);
+    L.skey = take(N * 4);
+    L.hist = take(static_cast<size_t>(kDigits) * L.nb * 4);
+    L.offs = take(static_cast<size_t>(kDigits) * L.nb * 4);
+    L.bucket_start = take((kDigits + 1) * 4);
+    L.seg_start = take((R + 2) * 4);
+    L.tickets = take((R + 1) * 4);
+    L.slots = take(static_cast<size_t>(L.n_pblk) * 8 * D * 4);
+    L.total = o;
+    return L;
+}
+
+}  // namespace
+}  // namespace dgr
+
+using namespace dgr;
+
+extern "C" size_t dgr_index_add_workspace_bytes(int64_t N, int64_t R, int64_t D) {
+    if (N < 0 || R < 0 || D < 0 || R + 1 > 65536 || N > INT32_MAX || D > 4096) return 0;
+    return idx_layout(N, R, D).total;
+}
+
+extern "C" dgr_status dgr_det_index_add(float *out, int64_t R, int64_t D, int64_t ld_out, const float *src,
+                                        int64_t ld_src, const int32_t *idx, int64_t N, int32_t seg_tile,
+                                        int32_t *bad_count, void *ws, size_t ws_bytes, void *stream) {
+    if (R < 0 || D < 0 || N < 0) return DGR_ERR_INVALID_ARG;
+    if (!is_pow2(seg_tile) || seg_tile > kSegTile) return DGR_ERR_INVALID_ARG;
+    if (R + 1 > 65536 || N > INT32_MAX || D > 4096) return DGR_ERR_UNSUPPORTED;
+    if (!out || (N > 0 && (!src || !idx))) return DGR_ERR_INVALID_ARG;
+    if (ld_out < D || (N > 0 && ld_src < D)) return DGR_ERR_INVALID_ARG;
+    if ((D % 4) != 0 || (ld_out % 4) != 0 || (ld_src % 4) != 0 || !aligned(out, 16) ||
+        (src && !aligned(src, 16)) || (idx && !aligned(idx, 4)) || (bad_count && !aligned(bad_count, 4)))
+        return DGR_ERR_MISALIGNED;
+    const IdxLayout L = idx_layout(N, R, D);
+    if (N > 0) {
+        if (!ws) return DGR_ERR_INVALID_ARG;
+        if (ws_bytes < L.total) return DGR_ERR_WORKSPACE_TOO_SMALL;
+        if (!aligned(ws, kAlign)) return DGR_ERR_MISALIGNED;
+    }
+    const size_t ext_out = static_cast<size_t>((R * ld_out + D) * 4);
+    const size_t ext_src = N > 0 ? static_cast<size_t>(((N - 1) * ld_src + D) * 4) : 0;
+    if (ranges_overlap(out, ext_out, src, ext_src) || ranges_overlap(out, ext_out, idx, N * 4) ||
+        ranges_overlap(out, ext_out, bad_count, bad_count ? 4 : 0) ||
+        (N > 0 && ranges_overlap(out, ext_out, ws, L.total)))
+        return DGR_ERR_ALIAS;
+    dgr_status st = check_device();
+    if (st != DGR_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (N == 0) {
+        if (bad_count && cudaMemsetAsync(bad_count, 0, 4, s) != cudaSuccess) return DGR_ERR_CUDA;
+        return DGR_OK;
+    }
+    IdxParams p{};
+    p.idx = idx;
+    p.N = static_cast<int32_t>(N);
+    p.R = static_cast<int32_t>(R);
+    p.D = static_cast<int32_t>(D);
+    p.nb = L.nb;
+    p.n_buckets = L.n_buckets;
+    p.n_pblk = L.n_pblk;
+    p.seg_tile = seg_tile;
+    p.src = src;
+    p.ld_src = ld_src;
+    p.out = out;
+    p.ld_out = ld_out;
+    p.bad_count = bad_count;
+    char *w = static_cast<char *>(ws);
+    p.hdr = reinterpret_cast<WsHeader *>(w);
+    p.keys_a = reinterpret_cast<int32_t *>(w + L.keys_a);
+    p.vals_a = reinterpret_cast<int32_t *>(w + L.vals_a);
+    p.perm = reinterpret_cast<int32_t *>(w + L.perm);
+    p.skey = reinterpret_cast<int32_t *>(w + L.skey);
+    p.hist = reinterpret_cast<int32_t *>(w + L.hist);
+    p.offs = reinterpret_cast<int32_t *>(w + L.offs);
+    p.bucket_start = reinterpret_cast<int32_t *>(w + L.bucket_start);
+    p.seg_start = reinterpret_cast<int32_t *>(w + L.seg_start);
+    p.tickets = reinterpret_cast<int32_t *>(w + L.tickets);
+    p.slots = reinterpret_cast<float *>(w + L.slots);
+    count_kernel<<<L.nb, kThreads, 0, s>>>(p);
+    scatter_high_kernel<<<L.nb, kThreads, 0, s>>>(p);
+    bucket_kernel<<<L.n_buckets, kThreads, 0, s>>>(p);
+    if (D > 0) {
+        const int64_t n_split = seg_tile == kSegTile ? static_cast<int64_t>(L.n_pblk) * 4 : 0;
+        const int64_t warps = n_split + R + 1;
+        const int64_t grid = (warps + kWarps - 1) / kWarps;
+        if (grid > INT32_MAX) return DGR_ERR_UNSUPPORTED;
+        segsum_kernel<<<static_cast<unsigned>(grid), kThreads, 0, s>>>(p);
+    }
+    return launch_status();
+}

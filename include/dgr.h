@@ -1,0 +1,197 @@
+/*
+ * dgr.h - deterministic, atomic-free gradient reduction on GB300 (sm_103a).
+ *
+ * A small C ABI over hand-written CUDA kernels. Every reduction writes FP32
+ * partial sums with exactly one writer per partial, then reduces them in one
+ * canonical order: a fixed-width pairwise tree inside each tile (adjacent
+ * halves; leaves past a ragged end are absent), the tile partials folded in
+ * ascending tile order, and the result either written or added to the output
+ * with one IEEE binary32 rounding. Results are therefore bitwise identical
+ * from run to run, whatever the launch order, grid size or concurrent streams.
+ *
+ * Conventions for every entry point:
+ *   - Pointers are DEVICE pointers unless stated otherwise; the caller owns
+ *     every buffer (inputs, outputs, workspace). The library allocates no
+ *     memory and keeps no state between calls.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream). All work is enqueued on it; nothing synchronises the host.
+ *   - Arguments are checked on the host before anything is launched; a bad
+ *     argument returns an error code and launches nothing.
+ *   - Workspaces: query the size with the matching *_workspace_bytes() call,
+ *     allocate at least that many bytes (256-byte aligned) and ZERO them once
+ *     before first use. Every successful call leaves its workspace ready for
+ *     the next call (all counters back to zero). One workspace must not be used
+ *     by two calls that can run at the same time on the GPU.
+ *   - Device-side anomalies (a bounded wait that ran out) are recorded in the
+ *     workspace's status word, read with dgr_read_device_status(). After such
+ *     an error the outputs of that call are unspecified and the workspace must
+ *     be zeroed again before reuse.
+ *   - Floating point: binary32 round-to-nearest-even, subnormals kept, no
+ *     fused multiply-add anywhere in a reduction.
+ *   - Only devices of compute capability 10.3 (sm_103a, GB300) are supported;
+ *     on others every launching entry returns DGR_ERR_UNSUPPORTED.
+ */
+#ifndef DGR_H
+#define DGR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t dgr_status;
+
+#define DGR_OK 0
+#define DGR_ERR_INVALID_ARG 1          /* a size, stride, flag or pointer is invalid */
+#define DGR_ERR_UNSUPPORTED 2          /* device is not sm_103a, or a size is beyond a stated limit */
+#define DGR_ERR_WORKSPACE_TOO_SMALL 3  /* ws_bytes below the *_workspace_bytes() figure */
+#define DGR_ERR_ALIAS 4                /* an output overlaps an input or the workspace */
+#define DGR_ERR_MISALIGNED 5           /* a pointer or stride breaks a stated alignment */
+#define DGR_ERR_CUDA 6                 /* a CUDA runtime call failed (launch, attribute) */
+#define DGR_ERR_TIMEOUT 7              /* device status: a bounded wait ran out */
+
+#define DGR_DTYPE_F32 0
+#define DGR_DTYPE_BF16 1
+
+/* Human-readable name of a status code (static storage). */
+const char *dgr_status_string(dgr_status s);
+
+/* Library ABI version (major * 100 + minor). */
+int32_t dgr_version(void);
+
+/* DGR_OK when `device` is a compute capability 10.3 GPU, else DGR_ERR_UNSUPPORTED. */
+dgr_status dgr_device_supported(int32_t device);
+
+/*
+ * Copies the status word of a workspace to *status (host pointer) after
+ * synchronising `stream`; with clear != 0 it then zeroes the word.
+ * DGR_OK in *status means no device-side error was recorded.
+ */
+dgr_status dgr_read_device_status(const void *ws, int32_t clear, int32_t *status, void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* 1. Ordered column sum                                                     */
+/* ------------------------------------------------------------------------ */
+/*
+ * Megatron-LM PR #8244 ("ordered reduction for the fused pre-GDR gate
+ * backward"), description: each program writes independent FP32 partial sums
+ * (here one slot row per tile of `tile_rows` tokens) and the caller reduces
+ * them in order on the same stream - the A_log / dt_bias-style bias gradient.
+ *
+ *   out[h] = fold_j pw_W( x[t][h] : t in tile j ),   W = tile_rows,
+ *   tokens flattened t = b*S + s, x[b][s][h] at element offset
+ *   b*stride_b + s*stride_s + h (the last dimension is contiguous).
+ *
+ * x:        [B, S, H] elements of `dtype` (DGR_DTYPE_BF16 or DGR_DTYPE_F32).
+ * out:      [H] fp32. accumulate = 0 overwrites, else out[h] = out[h] + F.
+ *           With B*S = 0 overwrite writes +0.0 and accumulate leaves out.
+ * tile_rows: power of two, 1 .. 4096 (128 is the canonical tile).
+ * Limits:   H <= 4096; B*S <= 2^31 - 1.
+ * Alignment: 16-byte vector loads are used when x, stride_b, stride_s and H
+ *           allow it; otherwise a scalar path runs (same bits).
+ * ws:       dgr_colsum_workspace_bytes(B*S, H, tile_rows) bytes, zeroed once.
+ *           Holds the [tiles, H] FP32 slots and the ready counters.
+ * out must not overlap x or ws.
+ */
+size_t dgr_colsum_workspace_bytes(int64_t T, int64_t H, int32_t tile_rows);
+dgr_status dgr_ordered_colsum(const void *x, int32_t dtype, int64_t B, int64_t S, int64_t H,
+                              int64_t stride_b, int64_t stride_s, float *out, int32_t accumulate,
+                              int32_t tile_rows, void *ws, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* 2. Ordered per-row dprob                                                  */
+/* ------------------------------------------------------------------------ */
+/*
+ * cuDNN-frontend PR #521 ("grouped gemm dsrelu deterministic dprob"), commit
+ * "deterministic dprob": dprob gets one FP32 slot per N-tile, so each
+ * (token, tile_n) pair has exactly one writer; the slots are reduced in a
+ * fixed order and the reduction accumulates into dprob.
+ *
+ *   dprob[m] = fold_j pw_W( dY[m][n] * Y[m][n] : n in tile j ),  W = tile_n,
+ *   each product one fp32 multiply of the widened inputs, rounded on its own.
+ *
+ * dY, Y:    [M, N] row-major with leading dimensions ld_dy, ld_y (elements).
+ * dprob:    [M] fp32; accumulate as for the column sum; N = 0 gives +0.0 /
+ *           leaves dprob.
+ * tile_n:   128 (the only width of the fused kernel).
+ * slots:    NULL, or [M, ceil(N/tile_n)] fp32 receiving the tile partials
+ *           (the low-level form of the page's class API).
+ * Limits:   M <= 2^31 - 1, N <= 65536. Vector loads need 16-byte aligned rows.
+ * ws:       dgr_rowdot_workspace_bytes() bytes (0: the fold stays on chip; ws
+ *           may then be NULL).
+ * dprob and slots must not overlap dY, Y or each other.
+ */
+size_t dgr_rowdot_workspace_bytes(int64_t M, int64_t N, int32_t tile_n);
+dgr_status dgr_ordered_rowdot_dprob(const void *dY, const void *Y, int32_t dtype, int64_t M, int64_t N,
+                                    int64_t ld_dy, int64_t ld_y, float *dprob, int32_t accumulate,
+                                    int32_t tile_n, float *slots, void *ws, size_t ws_bytes,
+                                    void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* 3. Deterministic index_add                                                */
+/* ------------------------------------------------------------------------ */
+/*
+ * Megatron-LM PR #7441 ("DSv4 --deterministic-mode"), Source 3: an
+ * atomic-free index_add of gradient rows by a stable sort by destination and a
+ * segmented sum, padding routed to a dummy row the caller drops.
+ *
+ *   key[i] = idx[i] if 0 <= idx[i] < R, else R (the dummy row);
+ *   a stable sort orders the rows of each destination by original index;
+ *   destination r's members, in that order, are cut into tiles of seg_tile
+ *   and out[r][d] = out[r][d] + fold_tiles pw_{seg_tile}( src[i][d] ).
+ *   Rows with no member are not touched.
+ *
+ * out:      [R+1, D] fp32, row stride ld_out (elements); row R is the dummy.
+ * src:      [N, D] fp32, row stride ld_src. idx: [N] int32.
+ * seg_tile: power of two, 1 .. 128 (128 canonical; 1 = plain sequential).
+ * bad_count: NULL, or one device int32 that receives (overwrites) the number
+ *           of idx entries outside [-1, R); those rows go to the dummy row.
+ * Limits:   R + 1 <= 65536, N <= 2^31 - 1, D <= 4096. Rows of out and src
+ *           need 16-byte alignment (ld_* and D multiples of 4).
+ * ws:       dgr_index_add_workspace_bytes(N, R, D) bytes, zeroed once.
+ * out must not overlap src, idx, bad_count or ws.
+ */
+size_t dgr_index_add_workspace_bytes(int64_t N, int64_t R, int64_t D);
+dgr_status dgr_det_index_add(float *out, int64_t R, int64_t D, int64_t ld_out, const float *src,
+                             int64_t ld_src, const int32_t *idx, int64_t N, int32_t seg_tile,
+                             int32_t *bad_count, void *ws, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* 4. Split-K grouped weight gradient, accumulated into fp32 main_grad       */
+/* ------------------------------------------------------------------------ */
+/*
+ * FlashInfer PR #8602 ("fuse the fp32 weight-gradient accumulate into
+ * main_grad") and its follow-up #8924 ("Design and numerics"): out[e] gets
+ * G_e^T X_e added; the deterministic form computes dW with a fixed split
+ * order and then one RN32(out + dW); an empty group leaves out bitwise
+ * unchanged. The 512-token k tile is the weight-gradient main stage.
+ *
+ *   for expert e (tokens offs[e] .. offs[e+1]-1), chunk c of chunk_tokens
+ *   tokens from the expert's first token (the last chunk zero-filled):
+ *     p_c[n][k] = sum over the chunk of G[t][n] * X[t][k] on the tensor cores,
+ *                 from a fresh accumulator, K16 steps in ascending token order;
+ *   dW = fold_c p_c (ascending, starting from p_0);
+ *   main_grad[e][n][k] = main_grad[e][n][k] + dW[n][k]   (one rounding).
+ *
+ * G:        [T_total, N] bf16 row-major; X: [T_total, K] bf16 row-major.
+ * d_offs:   [E+1] int64 DEVICE array, non-decreasing, d_offs[0] = 0,
+ *           d_offs[E] = T_total (not read by the host: no synchronisation).
+ * main_grad: [E, N, K] fp32, dense.
+ * chunk_tokens: 512.
+ * Limits:   N a multiple of 128, K a multiple of 256, E >= 1, T_total < 2^31.
+ * Alignment: G, X 1024-byte aligned; main_grad 32-byte aligned.
+ * ws:       dgr_wgrad_workspace_bytes() bytes, zeroed once (status word).
+ * main_grad must not overlap G, X, d_offs or ws.
+ */
+size_t dgr_wgrad_workspace_bytes(int32_t E, int64_t N, int64_t K);
+dgr_status dgr_grouped_wgrad_accumulate(const void *G, const void *X, const int64_t *d_offs, int32_t E,
+                                        int64_t T_total, int64_t N, int64_t K, float *main_grad,
+                                        int32_t chunk_tokens, void *ws, size_t ws_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DGR_H */

@@ -1,0 +1,107 @@
+"""The C ABI: the library builds, loads and exports every entry point that
+include/*.h declares, and rejects bad arguments on the host before it touches
+the GPU (these calls never reach the device, so they run without one)."""
+import ctypes
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+import deterministic_gradient_reduction_gb300 as dgr
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        for m in re.finditer(r"^\s*[A-Za-z_][\w\s\*]*?\b(dgr_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def L():
+    dgr.build()
+    return dgr.lib()
+
+
+def test_header_declares_the_four_operations():
+    names = declared_functions()
+    for op in ("dgr_ordered_colsum", "dgr_ordered_rowdot_dprob", "dgr_det_index_add",
+               "dgr_grouped_wgrad_accumulate"):
+        assert op in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    out = subprocess.run(["nm", "-D", "--defined-only", dgr._LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if ln.strip()}
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    for n in declared_functions():
+        assert getattr(L, n) is not None
+
+
+def test_library_is_built_for_sm_103a_only():
+    out = subprocess.run(["cuobjdump", "--list-elf", dgr._LIB_PATH], capture_output=True, text=True)
+    if out.returncode != 0:
+        pytest.skip("cuobjdump unavailable")
+    archs = set(re.findall(r"sm_(\d+a?)", out.stdout))
+    assert archs == {"103a"}, archs
+
+
+def test_status_strings_and_version(L):
+    assert L.dgr_version() >= 100
+    for code, name in dgr.STATUS.items():
+        assert L.dgr_status_string(code).decode() == name
+    assert L.dgr_status_string(99).decode() == "DGR_ERR_UNKNOWN"
+
+
+def test_workspace_sizes(L):
+    # colsum: header + ready counters + [tiles x H] fp32 slots
+    assert dgr.colsum_workspace_bytes(8388608, 64) >= 65536 * 64 * 4
+    assert dgr.colsum_workspace_bytes(2048, 16) >= 16 * 16 * 4
+    assert dgr.colsum_workspace_bytes(0, 16) >= 256
+    assert dgr.colsum_workspace_bytes(100, 16, 3) == 0  # not a power of two
+    assert dgr.rowdot_workspace_bytes(65536, 4096) == 0
+    n = dgr.index_add_workspace_bytes(262144, 16384, 128)
+    assert n >= 4 * 262144 * 4 + (16384 + 2) * 4
+    assert dgr.index_add_workspace_bytes(10, 70000, 4) == 0  # R + 1 beyond the limit
+    assert dgr.wgrad_workspace_bytes(8, 4096, 2048) >= 256
+
+
+def _p(v):
+    return ctypes.c_void_p(v)
+
+
+def test_host_rejects_bad_arguments_before_any_launch(L):
+    fake = _p(0x10000)  # never dereferenced: every call below fails validation first
+    out = _p(0x20000)
+    # colsum: bad dtype, non power-of-two tile, negative size, H beyond the limit
+    assert L.dgr_ordered_colsum(fake, 7, 1, 4, 4, 16, 4, out, 0, 128, fake, 1 << 20, None) == 1
+    assert L.dgr_ordered_colsum(fake, 1, 1, 4, 4, 16, 4, out, 0, 100, fake, 1 << 20, None) == 1
+    assert L.dgr_ordered_colsum(fake, 1, -1, 4, 4, 16, 4, out, 0, 128, fake, 1 << 20, None) == 1
+    assert L.dgr_ordered_colsum(fake, 1, 1, 4, 5000, 5000, 5000, out, 0, 128, fake, 1 << 20, None) == 2
+    # workspace too small, misaligned workspace
+    assert L.dgr_ordered_colsum(fake, 1, 1, 4096, 16, 0, 16, out, 0, 128, fake, 16, None) == 3
+    assert L.dgr_ordered_colsum(fake, 1, 1, 4096, 16, 0, 16, out, 0, 128, _p(0x30008), 1 << 20, None) == 5
+    # out overlapping the input
+    assert L.dgr_ordered_colsum(_p(0x20000), 1, 1, 64, 16, 0, 16, _p(0x20010), 0, 128, _p(0x900000),
+                                1 << 20, None) == 4
+    # rowdot: only tile 128, ld smaller than N, overlap of dprob and dY
+    assert L.dgr_ordered_rowdot_dprob(fake, fake, 1, 4, 256, 256, 256, out, 0, 64, None, None, 0, None) == 1
+    assert L.dgr_ordered_rowdot_dprob(fake, fake, 1, 4, 256, 100, 256, out, 0, 128, None, None, 0, None) == 1
+    assert L.dgr_ordered_rowdot_dprob(_p(0x100000), _p(0x200000), 1, 4, 256, 256, 256, _p(0x100100), 0, 128,
+                                      None, None, 0, None) == 4
+    # index_add: seg_tile not a power of two, R too large, D not a multiple of 4
+    assert L.dgr_det_index_add(out, 10, 8, 8, fake, 8, fake, 4, 3, None, fake, 1 << 20, None) == 1
+    assert L.dgr_det_index_add(out, 70000, 8, 8, fake, 8, fake, 4, 128, None, fake, 1 << 20, None) == 2
+    assert L.dgr_det_index_add(_p(0x40000), 10, 6, 6, _p(0x80000), 6, fake, 4, 128, None, fake, 1 << 20,
+                               None) == 5
+    # index_add: workspace too small
+    assert L.dgr_det_index_add(_p(0x40000), 10, 8, 8, _p(0x80000), 8, _p(0xC0000), 4, 128, None, _p(0x100000),
+                               64, None) == 3
