@@ -1,0 +1,454 @@
+#!/usr/bin/env python3
+"""Benchmark of one deterministic-reduction step on GB300.
+
+A step is one pass of every operation on its seeded synthetic workload, with
+the inputs resident in HBM:
+  colsum_large    ordered column sum, bf16 [8388608, 64] (1 GiB)  -> fp32 [64]
+  colsum_small    ordered column sum, bf16 [2048, 16]             -> fp32 [16]
+  dprob           ordered dprob, bf16 [65536, 4096] x 2 (1 GiB)   -> fp32 [65536]
+  colsum_strided  ordered column sum, bf16 [4, 2048, 64] at token stride 128
+  index_add       deterministic index_add, fp32 [262144, 128] -> [16385, 128]
+  wgrad           grouped wgrad, E 8, T 32768, N 4096, K 2048, into fp32 main_grad
+The order interleaves the small operations with large streams, and every step
+moves several GB, far more than the 129 MB L2, so no operation finds its
+inputs in L2 from the previous step (no separate flush is needed).
+
+Printed (rank 0, one JSON line): the ordered-reduction throughput in GB/s
+(algorithmic bytes of the five reductions over their device time), the wgrad
+TFLOP/s, per-operation figures, the roofline of the dominant operation, the
+end-to-end figure through host buffers, SM clocks sampled during the timed
+region and the CPU oracle's own rate on the host cores.
+
+`--impl reference` times the CPU oracle instead (the only reference this
+project has): single-threaded C on the host cores, bounded samples per step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import dgr_inputs as gi  # noqa: E402
+
+METRIC = "ordered-reduction HBM GB/s (% of peak), bitwise replay; wgrad TFLOP/s"
+REDUCTIONS = ["colsum_large", "colsum_small", "dprob", "colsum_strided", "index_add"]
+
+# algorithmic bytes (or flops) per call: inputs read once, outputs written once
+ALGO = {
+    "colsum_large": 8388608 * 64 * 2 + 64 * 4,
+    "colsum_small": 2048 * 16 * 2 + 16 * 4,
+    "dprob": 2 * 65536 * 4096 * 2 + 65536 * 4,
+    "colsum_strided": 4 * 2048 * 64 * 2 + 64 * 4,
+    "index_add": 262144 * 128 * 4 + 262144 * 4 + 2 * 16385 * 128 * 4,
+    "wgrad_flop": 2 * 4096 * 2048 * 32768,
+    "wgrad": 32768 * 4096 * 2 + 32768 * 2048 * 2 + 2 * 8 * 4096 * 2048 * 4,
+}
+LAUNCHES = {"colsum_large": 1, "colsum_small": 1, "dprob": 1, "colsum_strided": 1, "index_add": 4, "wgrad": 1}
+
+WORKLOAD = ("deterministic reduction step: colsum bf16 8388608x64 + colsum bf16 2048x16 + dprob bf16 "
+            "65536x4096 + colsum bf16 4x2048x64 (token stride 128) + index_add fp32 262144x128 -> 16385 rows "
+            "+ grouped wgrad E8 T32768 N4096 K2048 into fp32 main_grad")
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm": d["hbm_gbs"], "bf16": d["bf16_tflops"], "bf16_sus": d.get("bf16_tflops_sustained"),
+                "src": "measured"}
+    return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sus": 1700.0, "src": "fallback"}
+
+
+def load_traffic() -> dict:
+    """DRAM bytes per launch from the committed ncu summaries (profiles/*.md):
+    a line `traffic: <op> <bytes>` per captured operation."""
+    out = {}
+    d = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(d):
+        return out
+    for f in sorted(os.listdir(d)):
+        if f.endswith(".md"):
+            for m in re.finditer(r"^traffic:\s*(\w+)\s+(\d+)\s*$", open(os.path.join(d, f)).read(), re.M):
+                out[m.group(1)] = int(m.group(2))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.proc = None
+        self.gpu = gpu_index
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self, begin: bool):
+        if begin:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        self.proc.wait()
+        inside = [s for t, s in self.samples if self.t0 is None or (self.t0 <= t <= (self.t1 or t) + 0.15)]
+        if not inside:
+            inside = [s for _, s in self.samples]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in inside:
+            f = [x.strip() for x in s.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def make_ops(dev, torch, dgr, with_wgrad):
+    """Build device inputs and one closure per operation (enqueue only)."""
+    ops, host, outs = {}, {}, {}
+
+    cl = gi.colsum_large()
+    cs = gi.colsum_small()
+    cst = gi.colsum_strided()
+    for name, ci in (("colsum_large", cl), ("colsum_small", cs), ("colsum_strided", cst)):
+        base = ci.base.to(dev)
+        x = base.as_strided((ci.B, ci.S, ci.H), (ci.stride_b, ci.stride_s, 1))
+        out = torch.zeros(ci.H, device=dev)
+        ws = dgr.workspace(dgr.colsum_workspace_bytes(ci.B * ci.S, ci.H), dev)
+        ops[name] = (lambda x=x, out=out, ws=ws: dgr.ordered_colsum(x, out, ws=ws))
+        host[name] = ([ci.base], [base])
+        outs[name] = out
+    dp = gi.dprob_full()
+    dY, Y = dp.dY.to(dev), dp.Y.to(dev)
+    dprob = torch.zeros(dp.M, device=dev)
+    ops["dprob"] = lambda: dgr.ordered_rowdot_dprob(dY, Y, dprob)
+    host["dprob"] = ([dp.dY, dp.Y], [dY, Y])
+    outs["dprob"] = dprob
+    ia = gi.index_add_full()
+    src, idx, iout = ia.src.to(dev), ia.idx.to(dev), ia.out.to(dev)
+    iws = dgr.workspace(dgr.index_add_workspace_bytes(262144, 16384, 128), dev)
+    ops["index_add"] = lambda: dgr.det_index_add(iout, src, idx, ws=iws)
+    host["index_add"] = ([ia.src, ia.idx, ia.out], [src, idx, iout])
+    outs["index_add"] = iout
+    if with_wgrad:
+        wi = gi.wgrad_full()
+        G, X, offs, mg = wi.G.to(dev), wi.X.to(dev), wi.offs.to(dev), wi.main_grad.to(dev)
+        wws = dgr.workspace(dgr.wgrad_workspace_bytes(8, 4096, 2048), dev)
+        ops["wgrad"] = lambda: dgr.grouped_wgrad_accumulate(G, X, offs, mg, ws=wws)
+        host["wgrad"] = ([wi.G, wi.X, wi.offs, wi.main_grad], [G, X, offs, mg])
+        outs["wgrad"] = mg
+    order = ["colsum_large", "colsum_small", "dprob", "colsum_strided", "index_add"]
+    if with_wgrad:
+        order.append("wgrad")
+    return order, ops, host, outs
+
+
+def wgrad_available(dgr) -> bool:
+    try:
+        import torch
+        wi = gi.wgrad_input(1, 16, 128, 256, seed=0)
+        dgr.grouped_wgrad_accumulate(wi.G.cuda(), wi.X.cuda(), wi.offs.cuda(), wi.main_grad.cuda())
+        torch.cuda.synchronize()
+        return True
+    except Exception as e:  # noqa: BLE001
+        if getattr(e, "code", None) == 2:  # DGR_ERR_UNSUPPORTED: not built yet
+            return False
+        raise
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import deterministic_gradient_reduction_gb300 as dgr
+
+    dgr.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    with_wgrad = wgrad_available(dgr)
+    order, ops, host, outs = make_ops(dev, torch, dgr, with_wgrad)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    # warm-up
+    for _ in range(args.warmup):
+        for name in order:
+            ops[name]()
+    torch.cuda.synchronize()
+
+    # timed: device events around every operation of every step
+    K = args.steps
+    ev = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+          for n in order}
+    step0, step1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0])
+                           if os.environ.get("CUDA_VISIBLE_DEVICES", "").isdigit() else local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    sampler.mark(True)
+    step0.record(stream)
+    for k in range(K):
+        for name in order:
+            a, b = ev[name][k]
+            a.record(stream)
+            ops[name]()
+            b.record(stream)
+    step1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark(False)
+    barrier()
+    clocks = sampler.stop()
+    total_ms = step0.elapsed_time(step1)
+    per_ms = {n: sum(a.elapsed_time(b) for a, b in ev[n]) / K for n in order}
+
+    # max over ranks
+    if world > 1:
+        t = torch.tensor([total_ms] + [per_ms[n] for n in order], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t[0])
+        per_ms = {n: float(t[i + 1]) for i, n in enumerate(order)}
+
+    # end to end through host buffers: pinned host inputs copied in, outputs read back, every step
+    e2e = run_e2e(args, torch, order, ops, host, outs, stream, world, dev)
+
+    if rank != 0:
+        return
+    peaks = load_peaks()
+    traffic = load_traffic()
+    red_ms = sum(per_ms[n] for n in REDUCTIONS)
+    red_bytes = sum(ALGO[n] for n in REDUCTIONS)
+    value = world * red_bytes / (red_ms * 1e-3) / 1e9
+    parts = {}
+    for n in order:
+        ms = per_ms[n]
+        if n == "wgrad":
+            tf = ALGO["wgrad_flop"] / (ms * 1e-3) / 1e12
+            parts[n] = {"us": round(ms * 1e3, 2), "tflops": round(tf, 1),
+                        "frac_bf16_sustained": round(tf / peaks["bf16_sus"], 4), "launches": LAUNCHES[n]}
+        else:
+            gbs = ALGO[n] / (ms * 1e-3) / 1e9
+            parts[n] = {"us": round(ms * 1e3, 2), "gbs": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm"], 4),
+                        "launches": LAUNCHES[n]}
+    dom = max(order, key=lambda n: per_ms[n])
+    if dom == "wgrad":
+        ach = ALGO["wgrad_flop"] / (per_ms[dom] * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": peaks["bf16_sus"], "unit": "TFLOP/s",
+                "frac": round(ach / peaks["bf16_sus"], 4), "traffic": traffic.get(dom), "kernel": dom,
+                "peak_source": f"{peaks['src']} bf16 sustained"}
+    else:
+        ach = ALGO[dom] / (per_ms[dom] * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm"], "unit": "GB/s",
+                "frac": round(ach / peaks["hbm"], 4), "traffic": traffic.get(dom), "kernel": dom,
+                "peak_source": f"{peaks['src']} hbm"}
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / K, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "l2": "no flush: every step streams > 3 GB, inputs larger than L2",
+                   "parallelism": f"replicas x{world}", "wgrad": "included" if with_wgrad else "not built"},
+        "reductions_frac_hbm": round(value / world / peaks["hbm"], 4),
+        "wgrad_tflops": parts.get("wgrad", {}).get("tflops"),
+        "parts": parts, "roofline": roof, "e2e": e2e, "clocks": clocks,
+        "gpu_launches": K * sum(LAUNCHES[n] for n in order),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
+    print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, torch, order, ops, host, outs, stream, world, dev):
+    pinned = {n: [t.pin_memory() for t in host[n][0]] for n in order}
+    res_host = {n: torch.empty(outs[n].shape, dtype=outs[n].dtype, pin_memory=True) for n in order}
+    h2d = sum(t.numel() * t.element_size() for n in order for t in pinned[n])
+    d2h = sum(t.numel() * t.element_size() for t in res_host.values())
+    K = max(1, args.e2e_steps)
+    ev = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+          for n in order}
+    torch.cuda.synchronize()
+    for k in range(K):
+        for n in order:
+            a, b = ev[n][k]
+            a.record(stream)
+            for hsrc, ddst in zip(pinned[n], host[n][1]):
+                ddst.copy_(hsrc, non_blocking=True)
+            ops[n]()
+            res_host[n].copy_(outs[n], non_blocking=True)
+            b.record(stream)
+    torch.cuda.synchronize()
+    per = {n: sum(a.elapsed_time(b) for a, b in ev[n]) / K for n in order}
+    if world > 1:
+        t = torch.tensor([per[n] for n in order], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        per = {n: float(t[i]) for i, n in enumerate(order)}
+    red_ms = sum(per[n] for n in REDUCTIONS)
+    val = world * sum(ALGO[n] for n in REDUCTIONS) / (red_ms * 1e-3) / 1e9
+    out = {"value": round(val, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "steps": K, "ms_per_step": round(sum(per.values()), 3)}
+    if "wgrad" in per:
+        out["wgrad_tflops"] = round(ALGO["wgrad_flop"] / (per["wgrad"] * 1e-3) / 1e12, 2)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline and reference arm)
+# ---------------------------------------------------------------------------
+
+class OracleWork:
+    """The oracle on contiguous slices of each reduction workload."""
+
+    def __init__(self):
+        import oracle
+        self.o = oracle
+        self.cl = gi.colsum_large()
+        self.cs = gi.colsum_small()
+        self.cst = gi.colsum_strided()
+        self.dp = gi.dprob_full()
+        self.ia = gi.index_add_full()
+        self.bits = {"cl": gi.bits(self.cl.base), "cs": gi.bits(self.cs.base), "cst": gi.bits(self.cst.base),
+                     "dy": gi.bits(self.dp.dY).reshape(-1), "y": gi.bits(self.dp.Y).reshape(-1)}
+
+    def run(self, frac: float) -> tuple[float, int]:
+        """Run every reduction on `frac` of its workload; returns (seconds, algorithmic bytes)."""
+        o, b = self.o, self.bits
+        t = time.perf_counter()
+        nbytes = 0
+        out = np.zeros(64, np.float32)
+        tok = max(128, int(8388608 * frac) // 128 * 128)
+        o.ordered_colsum(b["cl"], 1, tok, 64, tok * 64, 64, out)
+        nbytes += tok * 64 * 2 + 256
+        o.ordered_colsum(b["cs"], 1, 2048, 16, 2048 * 16, 16, np.zeros(16, np.float32))
+        nbytes += ALGO["colsum_small"]
+        rows = max(1, int(65536 * frac))
+        o.ordered_rowdot_dprob(b["dy"], b["y"], rows, 4096, 4096, 4096, np.zeros(rows, np.float32))
+        nbytes += rows * 4096 * 4 + rows * 4
+        o.ordered_colsum(b["cst"], 4, 2048, 64, 2048 * 128, 128, np.zeros(64, np.float32))
+        nbytes += ALGO["colsum_strided"]
+        n = max(2048, int(262144 * frac))
+        outi = np.zeros((16385, 128), np.float32)
+        o.det_index_add(outi, 16384, 128, 128, gi.f32(self.ia.src)[:n], 128, self.ia.idx.numpy()[:n], n)
+        nbytes += n * (128 * 4 + 4) + 2 * 16385 * 128 * 4
+        return time.perf_counter() - t, nbytes
+
+
+def cpu_baseline(budget_s: float = 15.0) -> dict:
+    w = OracleWork()
+    t_small, _ = w.run(1 / 256)
+    frac = min(1.0, max(1 / 256, budget_s / max(t_small * 256, 1e-3)))
+    t, nbytes = w.run(frac)
+    return {"value": round(nbytes / t / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"single-threaded C oracle on {frac:.3f} of each reduction workload "
+                      f"(colsum 1 GiB / dprob 1 GiB / index_add prefixes; small ones whole), {t:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = OracleWork()
+    t_small, _ = w.run(1 / 256)
+    per_step_budget = args.cpu_budget / max(1, args.steps + args.warmup)
+    frac = min(1.0, max(1 / 8192, per_step_budget / max(t_small * 256, 1e-3)))
+    for _ in range(args.warmup):
+        w.run(frac)
+    tot_t, tot_b = 0.0, 0
+    for _ in range(args.steps):
+        t, nb = w.run(frac)
+        tot_t += t
+        tot_b += nb
+    val = tot_b / tot_t / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(val, 3), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_t / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "l2": "n/a (CPU)", "parallelism": "single host thread",
+                       "wgrad": "not in the oracle rate"},
+            "cpu_baseline": {"value": round(val, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{frac:.5f} of each reduction workload per step"},
+            "e2e": {"value": round(val, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        if args.impl == "ours":
+            torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
