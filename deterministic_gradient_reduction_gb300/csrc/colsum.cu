@@ -360,3 +360,68 @@ extern "C" dgr_status dgr_ordered_colsum(const void *x, int32_t dtype, int64_t B
     return VE == 4 ? launch_rpt<DGR_DTYPE_F32, 4>(p, rpt, static_cast<int>(grid), s)
                    : launch_rpt<DGR_DTYPE_F32, 1>(p, rpt, static_cast<int>(grid), s);
 }
+
+// ---------------------------------------------------------------------------
+// Column sum without a caller workspace.
+//
+// For callers that cannot allocate device memory at the point where they need
+// the reduction: code running inside another allocator's critical section,
+// plugins handed only input and output pointers by a host framework that owns
+// all device memory, or hot paths where a cudaMalloc would synchronise the
+// device. Their scratch is this file-scope array instead (4 MiB, held on every
+// GPU that loads the library until the process exits). The host cannot use
+// the array's name as a device address (it is a host-side stand-in), so the
+// first call on each device looks the address up with cudaGetSymbolAddress
+// while that device is current and keeps it.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace dgr {
+namespace {
+
+constexpr size_t kStaticScratchBytes = DGR_COLSUM_NOALLOC_SCRATCH_BYTES;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_colsum_scratch[kStaticScratchBytes];
+
+std::once_flag g_scratch_once[kMaxDevices];
+void *g_scratch_ptr[kMaxDevices];
+cudaError_t g_scratch_err[kMaxDevices];
+
+dgr_status static_scratch(void **ptr) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DGR_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return DGR_ERR_UNSUPPORTED;
+    std::call_once(g_scratch_once[dev], [dev] {
+        void *p = nullptr;
+        g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_colsum_scratch);
+        g_scratch_ptr[dev] = p;
+    });
+    if (g_scratch_err[dev] != cudaSuccess || !g_scratch_ptr[dev]) return DGR_ERR_CUDA;
+    *ptr = g_scratch_ptr[dev];
+    return DGR_OK;
+}
+
+}  // namespace
+}  // namespace dgr
+
+extern "C" dgr_status dgr_ordered_colsum_noalloc(const void *x, int32_t dtype, int64_t B, int64_t S, int64_t H,
+                                                 int64_t stride_b, int64_t stride_s, float *out,
+                                                 int32_t accumulate, int32_t tile_rows, void *stream) {
+    if (B < 0 || S < 0 || H < 0 || H > 4096 || !is_pow2(tile_rows) || tile_rows > 4096 ||
+        (S > 0 && B > INT32_MAX / S))
+        return dgr_ordered_colsum(x, dtype, B, S, H, stride_b, stride_s, out, accumulate, tile_rows, nullptr, 0,
+                                  stream);  // the same argument errors as the workspace form
+    const Layout L = colsum_layout(B * S, H, tile_rows);
+    if (L.total > kStaticScratchBytes) return DGR_ERR_WORKSPACE_TOO_SMALL;
+    void *ws = nullptr;
+    dgr_status st = static_scratch(&ws);
+    if (st != DGR_OK) return st;
+    // The array keeps whatever the previous call left; the header (status word,
+    // folder ticket) and the ready counters must start at zero.
+    if (B * S > 0 && H > 0 &&
+        cudaMemsetAsync(ws, 0, L.slots_off, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return DGR_ERR_CUDA;
+    return dgr_ordered_colsum(x, dtype, B, S, H, stride_b, stride_s, out, accumulate, tile_rows, ws,
+                              kStaticScratchBytes, stream);
+}

@@ -100,6 +100,29 @@ dgr_status dgr_ordered_colsum(const void *x, int32_t dtype, int64_t B, int64_t S
                               int64_t stride_b, int64_t stride_s, float *out, int32_t accumulate,
                               int32_t tile_rows, void *ws, size_t ws_bytes, void *stream);
 
+/*
+ * The same column sum for callers that cannot allocate device memory where
+ * they call it (inside another allocator, in a plugin given only input and
+ * output pointers, or on a path where a cudaMalloc would stall the device).
+ * The pages have no counterpart: this form exists for those callers only.
+ *
+ * Arguments and results are those of dgr_ordered_colsum() without ws and
+ * ws_bytes. The scratch is a static device array of
+ * DGR_COLSUM_NOALLOC_SCRATCH_BYTES inside the library (present on every GPU
+ * that loads it, until the process exits); nothing is allocated. A call whose
+ * dgr_colsum_workspace_bytes(B*S, H, tile_rows) exceeds that size returns
+ * DGR_ERR_WORKSPACE_TOO_SMALL and launches nothing.
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture. Each call
+ * clears the array's counters on `stream` before its kernel. All calls share
+ * the one array: calls that can overlap on the GPU (different streams, or
+ * different host threads without ordering) race and give wrong results.
+ */
+#define DGR_COLSUM_NOALLOC_SCRATCH_BYTES (4u << 20)
+dgr_status dgr_ordered_colsum_noalloc(const void *x, int32_t dtype, int64_t B, int64_t S, int64_t H,
+                                      int64_t stride_b, int64_t stride_s, float *out, int32_t accumulate,
+                                      int32_t tile_rows, void *stream);
+
 /* ------------------------------------------------------------------------ */
 /* 2. Ordered per-row dprob                                                  */
 /* ------------------------------------------------------------------------ */
