@@ -10,7 +10,8 @@
 //     sub-windows so the tree is exactly the canonical one), one FP32 slot row
 //     per tile, then a release increment of the ready counter of its group of
 //     32 tiles;
-//   - folder CTAs (the first blockIdx values), one per block of FC columns:
+//   - folder CTAs (the first blockIdx values), one per block of FC columns
+//     (4 for H <= 256, at most 64 folders):
 //     they wait (bounded) for each batch of tiles to be ready, stage the slots
 //     through shared memory with many loader warps, and fold them in ascending
 //     tile order on one thread per column. The fold overlaps the stream, so a
@@ -24,7 +25,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kGroupTiles = 32;                 // tiles per ready counter
-constexpr int kFolderSmemBytes = 32 * 1024;     // double-buffered slot batches
+constexpr int kFolderSmemBytes = 32 * 1024;     // double-buffered slot batches (<= 1024 tiles each)
 constexpr int kMaxFolders = 64;
 
 struct ColsumParams {
@@ -179,13 +180,17 @@ __device__ void fold(const ColsumParams &p, int f, float *sm) {
     auto load = [&](int i) {
         const int j0 = i * p.batch;
         const int j1 = min(j0 + p.batch, p.n_tiles);
-        if (ltid == 0) {
-            for (int grp = j0 / kGroupTiles; grp <= (j1 - 1) / kGroupTiles; ++grp) {
+        if (ltid < 32) {  // one lane per group of the batch (a batch spans <= 32 groups)
+            const int grp = j0 / kGroupTiles + ltid;
+            bool ok = true;
+            if (grp <= (j1 - 1) / kGroupTiles) {
                 const int tiles_in_group = min(kGroupTiles, p.n_tiles - grp * kGroupTiles);
-                if (!wait_counter_geq(&p.counters[grp], tiles_in_group * p.n_pcb)) {
+                ok = wait_counter_geq(&p.counters[grp], tiles_in_group * p.n_pcb);
+            }
+            if (__any_sync(0xffffffffu, !ok)) {
+                if (ltid == 0) {
                     record_error(p.hdr, DGR_ERR_TIMEOUT, 1);
                     abort_flag = 1;
-                    break;
                 }
             }
         }
@@ -267,9 +272,10 @@ Layout colsum_layout(int64_t T, int64_t H, int32_t W) {
     Layout L{};
     L.n_tiles = static_cast<int32_t>((T + W - 1) / W);
     L.n_groups = (L.n_tiles + kGroupTiles - 1) / kGroupTiles;
-    const int64_t fcb8 = (H + 7) / 8;
-    L.FC = static_cast<int32_t>(8 * ((fcb8 + kMaxFolders - 1) / kMaxFolders));
-    if (L.FC < 8) L.FC = 8;
+    // FC columns per folder, a multiple of 4 (float4 staging): 4 for H <= 256
+    const int64_t fcb4 = (H + 3) / 4;
+    L.FC = static_cast<int32_t>(4 * ((fcb4 + kMaxFolders - 1) / kMaxFolders));
+    if (L.FC < 4) L.FC = 4;
     L.n_fcb = static_cast<int32_t>((H + L.FC - 1) / L.FC);
     L.counters_off = sizeof(WsHeader);
     L.slots_off = L.counters_off + align_up(static_cast<size_t>(L.n_groups) * 4);

@@ -58,7 +58,7 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint16_t h) {
 // 16-byte read-only load of data that no kernel writes during the launch.
 __device__ __forceinline__ uint4 ldg_nc_v4(const void *p) {
     uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
     return r;
 }

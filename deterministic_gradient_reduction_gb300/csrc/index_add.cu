@@ -18,8 +18,10 @@
 //                order) by the pairwise tree over tiles of 128 members and folds
 //                the tiles in order, then out[r] += sum with one rounding.
 //                Rows with more than 8 tiles are split: one warp per 32-member
-//                quarter of each tile writes a slot, and the last warp to
-//                arrive (an integer ticket) folds them in tile order.
+//                quarter of each tile writes a slot; the last quarter of a tile
+//                to arrive (an integer ticket) combines the quarters into the
+//                tile partial, and the last tile of the row folds the tile
+//                partials in order.
 // Integer atomics only count; no floating-point value depends on timing.
 #include "dgr_common.cuh"
 
@@ -48,7 +50,7 @@ struct IdxParams {
     float *out;
     int64_t ld_out;
     int32_t *bad_count;
-    int32_t *keys_a, *vals_a, *perm, *skey, *hist, *offs, *bucket_start, *seg_start, *tickets;
+    int32_t *keys_a, *vals_a, *perm, *skey, *hist, *offs, *bucket_start, *seg_start, *tickets, *tile_tickets;
     float *slots;
     WsHeader *hdr;
 };
@@ -347,7 +349,7 @@ __device__ __forceinline__ int64_t sub_slot(int32_t p0, int32_t t, int q) {
     return (static_cast<int64_t>(p0 >> 7) * 2 + (t == 0 ? 1 : 0)) * 4 + q;
 }
 
-__device__ void split_row_unit(const IdxParams &p, int32_t unit, int lane, float4 (*stk)[32]) {
+__device__ __noinline__ void split_row_unit(const IdxParams &p, int32_t unit, int lane, float4 (*stk)[32]) {
     const int32_t pb = unit >> 2;
     const int q = unit & 3;
     for (int m = 0; m < 4; ++m) {
@@ -382,33 +384,57 @@ __device__ void split_row_unit(const IdxParams &p, int32_t unit, int lane, float
             }
             __threadfence();
             __syncwarp();
+            // the last of the tile's four quarters combines them into the tile
+            // partial (the top two levels of its tree), kept in quarter slot 0
+            const int64_t tslot = static_cast<int64_t>(p0 >> 7) * 2 + (t == 0 ? 1 : 0);
+            int tq = 0;
+            if (lane == 0) tq = atomicAdd(&p.tile_tickets[tslot], 1);
+            tq = __shfl_sync(0xffffffffu, tq, 0);
+            if (tq != 3) continue;
+            __threadfence();
+            for (int c0 = 0; c0 < p.D; c0 += 128) {
+                const int col = c0 + lane * 4;
+                if (col >= p.D) continue;
+                float4 sq[4];
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq)
+                    if (qq * kSub < cnt_tile)
+                        sq[qq] = __ldcg(reinterpret_cast<const float4 *>(p.slots + sub_slot(p0, t, qq) * p.D + col));
+                float4 a = sq[0];
+                if (cnt_tile > 32) a = f4add(a, sq[1]);
+                if (cnt_tile > 64) {
+                    float4 c = sq[2];
+                    if (cnt_tile > 96) c = f4add(c, sq[3]);
+                    a = f4add(a, c);
+                }
+                *reinterpret_cast<float4 *>(p.slots + sub_slot(p0, t, 0) * p.D + col) = a;
+            }
+            __threadfence();
+            __syncwarp();
             int tk = 0;
-            if (lane == 0) tk = atomicAdd(&p.tickets[k], 1);
+            if (lane == 0) {
+                p.tile_tickets[tslot] = 0;
+                tk = atomicAdd(&p.tickets[k], 1);
+            }
             tk = __shfl_sync(0xffffffffu, tk, 0);
-            // every quarter of every tile arrives once, present or not
-            if (tk != n_tiles * 4 - 1) continue;
+            if (tk != n_tiles - 1) continue;
+            // the row's last tile folds the tile partials in ascending order,
+            // eight loads in flight at a time
             __threadfence();
             for (int c0 = 0; c0 < p.D; c0 += 128) {
                 const int col = c0 + lane * 4;
                 if (col >= p.D) continue;
                 float4 F = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int32_t tt = 0; tt < n_tiles; ++tt) {
-                    const int32_t pt = s0 + tt * kSegTile;
-                    const int ct = min(kSegTile, e0 - pt);
-                    float4 sq[4];
+                for (int32_t t0 = 0; t0 < n_tiles; t0 += 8) {
+                    float4 v[8];
 #pragma unroll
-                    for (int qq = 0; qq < 4; ++qq)
-                        if (qq * kSub < ct)
-                            sq[qq] = __ldcg(reinterpret_cast<const float4 *>(p.slots + sub_slot(pt, tt, qq) * p.D + col));
-                    // the top two levels of the tile's tree over its quarters
-                    float4 a = sq[0];
-                    if (ct > 32) a = f4add(a, sq[1]);
-                    if (ct > 64) {
-                        float4 c = sq[2];
-                        if (ct > 96) c = f4add(c, sq[3]);
-                        a = f4add(a, c);
-                    }
-                    F = (tt == 0) ? a : f4add(F, a);
+                    for (int u = 0; u < 8; ++u)
+                        if (t0 + u < n_tiles)
+                            v[u] = __ldcg(reinterpret_cast<const float4 *>(
+                                p.slots + sub_slot(s0 + (t0 + u) * kSegTile, t0 + u, 0) * p.D + col));
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        if (t0 + u < n_tiles) F = (t0 + u == 0) ? v[u] : f4add(F, v[u]);
                 }
                 add_out(p, k, col, F);
             }
@@ -504,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 3) segsum_kernel(const IdxParams p) 
 
 struct IdxLayout {
     int32_t nb, n_buckets, n_pblk;
-    size_t keys_a, vals_a, perm, skey, hist, offs, bucket_start, seg_start, tickets, slots, total;
+    size_t keys_a, vals_a, perm, skey, hist, offs, bucket_start, seg_start, tickets, tile_tickets, slots, total;
 };
 
 IdxLayout idx_layout(int64_t N, int64_t R, int64_t D) {
@@ -527,6 +553,7 @@ IdxLayout idx_layout(int64_t N, int64_t R, int64_t D) {
     L.bucket_start = take((kDigits + 1) * 4);
     L.seg_start = take((R + 2) * 4);
     L.tickets = take((R + 1) * 4);
+    L.tile_tickets = take(static_cast<size_t>(L.n_pblk) * 2 * 4);
     L.slots = take(static_cast<size_t>(L.n_pblk) * 8 * D * 4);
     L.total = o;
     return L;
@@ -597,6 +624,7 @@ extern "C" dgr_status dgr_det_index_add(float *out, int64_t R, int64_t D, int64_
     p.bucket_start = reinterpret_cast<int32_t *>(w + L.bucket_start);
     p.seg_start = reinterpret_cast<int32_t *>(w + L.seg_start);
     p.tickets = reinterpret_cast<int32_t *>(w + L.tickets);
+    p.tile_tickets = reinterpret_cast<int32_t *>(w + L.tile_tickets);
     p.slots = reinterpret_cast<float *>(w + L.slots);
     count_kernel<<<L.nb, kThreads, 0, s>>>(p);
     scatter_high_kernel<<<L.nb, kThreads, 0, s>>>(p);

@@ -16,9 +16,8 @@
 namespace dgr {
 namespace {
 
-constexpr int kWarps = 8;
+constexpr int kWarps = 4;
 constexpr int kTile = 128;
-constexpr int kUnroll = 4;  // 256-column steps in flight per lane
 
 struct RowdotParams {
     const char *dY;
@@ -93,6 +92,40 @@ __device__ __forceinline__ float lane_tile_partial(const float *a, const float *
     return v;
 }
 
+// The same when all 256 columns of the step are present: no presence flags.
+__device__ __forceinline__ float lane_tile_partial_full(const float *a, const float *b) {
+    float p[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) p[i] = __fmul_rn(a[i], b[i]);
+    p[0] = __fadd_rn(p[0], p[1]);
+    p[2] = __fadd_rn(p[2], p[3]);
+    p[4] = __fadd_rn(p[4], p[5]);
+    p[6] = __fadd_rn(p[6], p[7]);
+    p[0] = __fadd_rn(p[0], p[2]);
+    p[4] = __fadd_rn(p[4], p[6]);
+    float v = __fadd_rn(p[0], p[4]);
+#pragma unroll
+    for (int s = 1; s < 16; s *= 2) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, s));
+    return v;
+}
+
+template <int DT>
+__device__ __forceinline__ void unpack_raw(const uint4 *r, float *f) {
+    if (DT == DGR_DTYPE_BF16) {
+        const uint32_t w[4] = {r[0].x, r[0].y, r[0].z, r[0].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    } else {
+        f[0] = __uint_as_float(r[0].x); f[1] = __uint_as_float(r[0].y);
+        f[2] = __uint_as_float(r[0].z); f[3] = __uint_as_float(r[0].w);
+        f[4] = __uint_as_float(r[1].x); f[5] = __uint_as_float(r[1].y);
+        f[6] = __uint_as_float(r[1].z); f[7] = __uint_as_float(r[1].w);
+    }
+}
+
 template <int DT>
 __global__ void __launch_bounds__(kWarps * 32) rowdot_kernel(const RowdotParams p, int vec) {
     const int lane = threadIdx.x & 31;
@@ -101,25 +134,44 @@ __global__ void __launch_bounds__(kWarps * 32) rowdot_kernel(const RowdotParams 
     const int es = DT == DGR_DTYPE_BF16 ? 2 : 4;
     const char *rdy = p.dY + m * p.ld_dy * es;
     const char *ry = p.Y + m * p.ld_y * es;
+    // raw 16-byte words stay in flight (U steps per lane) and are widened at use
+    constexpr int V = DT == DGR_DTYPE_BF16 ? 1 : 2;  // uint4 per 8 elements
+    constexpr int U = DT == DGR_DTYPE_BF16 ? 8 : 4;  // 256-column steps in flight per lane
     float F = 0.0f;
     const int n_steps = (p.N + 255) / 256;  // each step covers two tiles
-    for (int i0 = 0; i0 < n_steps; i0 += kUnroll) {
-        float a[kUnroll][8], b[kUnroll][8];
+    for (int i0 = 0; i0 < n_steps; i0 += U) {
+        uint4 ra[U][V], rb[U][V];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int64_t c0 = static_cast<int64_t>(i0 + u) * 256 + lane * 8;
-            if (i0 + u < n_steps && c0 < p.N) {
-                load8<DT>(rdy, c0, p.N, vec != 0, a[u]);
-                load8<DT>(ry, c0, p.N, vec != 0, b[u]);
+            if (vec && i0 + u < n_steps && c0 + 8 <= p.N) {
+#pragma unroll
+                for (int q = 0; q < V; ++q) {
+                    ra[u][q] = ldg_nc_v4(rdy + c0 * es + 16 * q);
+                    rb[u][q] = ldg_nc_v4(ry + c0 * es + 16 * q);
+                }
             }
         }
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int i = i0 + u;
             if (i >= n_steps) break;
             const int64_t c0 = static_cast<int64_t>(i) * 256 + lane * 8;
-            const int nvalid = static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(8), p.N - c0)));
-            const float v = lane_tile_partial(a[u], b[u], nvalid, lane);
+            float a[8], b[8];
+            if (vec && c0 + 8 <= p.N) {
+                unpack_raw<DT>(ra[u], a);
+                unpack_raw<DT>(rb[u], b);
+            } else if (c0 < p.N) {
+                load8<DT>(rdy, c0, p.N, false, a);
+                load8<DT>(ry, c0, p.N, false, b);
+            }
+            float v;
+            if (static_cast<int64_t>(i) * 256 + 256 <= p.N) {
+                v = lane_tile_partial_full(a, b);
+            } else {
+                const int nvalid = static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(8), p.N - c0)));
+                v = lane_tile_partial(a, b, nvalid, lane);
+            }
             const float t0 = __shfl_sync(0xffffffffu, v, 0);
             const float t1 = __shfl_sync(0xffffffffu, v, 16);
             const int j0 = 2 * i, j1 = 2 * i + 1;
