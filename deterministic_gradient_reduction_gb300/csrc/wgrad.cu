@@ -1,5 +1,429 @@
 // Split-K grouped weight gradient accumulated into fp32 main_grad.
-#include "dgr_common.cuh"
+//
+// FlashInfer PR #8602 (fuse the fp32 weight-gradient accumulate into
+// main_grad) and follow-up #8924 ("Design and numerics"): out[e] gets
+// G_e^T X_e added; the deterministic route computes dW in a fixed order and
+// then RN32(out + dW); an empty group leaves out bitwise unchanged; the split
+// tail was the only order-varying launch. Here the split order is fixed:
+//   p_c = the chunk's G^T X on the tensor cores, chunks of 512 tokens from the
+//         expert's first token, a fresh accumulator per chunk, K16 steps in
+//         ascending token order;
+//   dW  = fold_c p_c (ascending, in registers of the epilogue warps);
+//   main_grad = RN(main_grad + dW), read-modify-write in the same kernel.
+//
+// Persistent kernel, one CTA per SM, 128 x 256 output tiles (n x k) walked
+// expert by expert. Warp 0 issues TMA loads (64-token stages, 128-byte
+// swizzle; G and X are MN-major as they lie in memory, so no transpose), warp
+// 1 issues tcgen05.mma into one of two TMEM accumulators (256 columns each),
+// warps 2-9 read the accumulator back, fold the chunks and finish the tile.
+// Rows of a stage past the expert's end are zeroed in shared memory before
+// the MMA reads them (TMA fills rows past the tensor's end with zeros).
+// Every wait is bounded; a timeout records DGR_ERR_TIMEOUT, aborts the CTA,
+// waits for its own TMA copies and frees its TMEM.
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "tc_common.cuh"
+#include "dgr_diag.h"
+
+namespace dgr {
+namespace {
+
+using namespace tc;
+
+constexpr int BM = 128;                 // n per tile (TMEM lanes)
+constexpr int BN = 256;                 // k per tile (TMEM columns per accumulator)
+constexpr int BK = 64;                  // tokens per pipeline stage
+constexpr int kStages = 4;
+constexpr int kChunk = 512;
+constexpr int kEpiWarps = 8;
+constexpr int kThreadsW = (2 + kEpiWarps) * 32;
+constexpr uint32_t kBoxBytes = 64 * 128;                  // one 64 x 64 bf16 TMA box
+constexpr uint32_t kStageA = 2 * kBoxBytes;               // 128 n x 64 tokens
+constexpr uint32_t kStageB = 4 * kBoxBytes;               // 256 k x 64 tokens
+constexpr uint32_t kStageBytes = kStageA + kStageB;
+constexpr uint32_t kLBO = kBoxBytes;                      // between 64-wide atoms along n / k
+constexpr uint32_t kSBO = 1024;                           // between 8-token row groups
+constexpr uint32_t kIdesc = idesc_bf16_mn(BM, BN);
+constexpr uint32_t kTmemCols = 2 * BN;
+
+struct Ctl {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint32_t tmem_base;
+    int abort;
+};
+constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + sizeof(Ctl);
+
+struct WgradParams {
+    const int64_t *offs;
+    int32_t E, N, K;
+    int32_t n_blk, k_blk, n_tiles;
+    float *main_grad;
+    WsHeader *hdr;
+};
+
+__device__ __forceinline__ void tile_coords(const WgradParams &p, int tau, int &e, int &nb, int &kb) {
+    const int per = p.n_blk * p.k_blk;
+    e = tau / per;
+    const int r = tau - e * per;
+    nb = r / p.k_blk;
+    kb = r - nb * p.k_blk;
+}
+
+__device__ __forceinline__ void expert_range(const WgradParams &p, int e, int32_t &t_beg, int32_t &te) {
+    const int64_t a = p.offs[e];
+    const int64_t b = p.offs[e + 1];
+    t_beg = static_cast<int32_t>(a);
+    te = static_cast<int32_t>(b > a ? b - a : 0);
+}
+
+__global__ void __launch_bounds__(kThreadsW, 1)
+    wgrad_kernel(const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmX,
+                 const WgradParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Ctl *ctl = reinterpret_cast<Ctl *>(smem + kStages * kStageBytes);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    volatile int *abort_flag = &ctl->abort;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&ctl->full[s], 1);
+            mbar_init(&ctl->empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&ctl->tfull[b], 1);
+            mbar_init(&ctl->tempty[b], kEpiWarps);
+        }
+        ctl->abort = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmG);
+        prefetch_tmap(&tmX);
+    }
+    if (warp == 1) {
+        tmem_alloc(&ctl->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem_base;
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            bool armed[kStages] = {};
+            uint32_t armed_phase[kStages] = {};
+            bool ok = true;
+            for (int tau = blockIdx.x; ok && tau < p.n_tiles; tau += gridDim.x) {
+                int e, nb, kb;
+                tile_coords(p, tau, e, nb, kb);
+                int32_t t_beg, te;
+                expert_range(p, e, t_beg, te);
+                for (int32_t c0 = 0; ok && c0 < te; c0 += kChunk) {
+                    const int32_t vc = min(kChunk, te - c0);
+                    for (int32_t s0 = 0; s0 < vc; s0 += BK) {
+                        if (!mbar_wait(&ctl->empty[stage], phase ^ 1, abort_flag, p.hdr, 10)) {
+                            ok = false;
+                            break;
+                        }
+                        uint8_t *sA = smem + stage * kStageBytes;
+                        uint8_t *sB = sA + kStageA;
+                        const int32_t t = t_beg + c0 + s0;
+                        mbar_arrive_expect_tx(&ctl->full[stage], kStageBytes);
+                        armed[stage] = true;
+                        armed_phase[stage] = phase;
+                        tma_load_2d(sA, &tmG, &ctl->full[stage], nb * BM, t);
+                        tma_load_2d(sA + kBoxBytes, &tmG, &ctl->full[stage], nb * BM + 64, t);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            tma_load_2d(sB + q * kBoxBytes, &tmX, &ctl->full[stage], kb * BN + 64 * q, t);
+                        if (++stage == kStages) {
+                            stage = 0;
+                            phase ^= 1;
+                        }
+                    }
+                }
+            }
+            if (!ok) {  // aborted: let our copies in flight land before the CTA exits
+                int dummy = 0;
+                for (int s = 0; s < kStages; ++s)
+                    if (armed[s]) mbar_wait(&ctl->full[s], armed_phase[s], &dummy, nullptr, 0);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        uint32_t stage = 0, phase = 0, g = 0;
+        bool ok = true;
+        for (int tau = blockIdx.x; ok && tau < p.n_tiles; tau += gridDim.x) {
+            int e, nb, kb;
+            tile_coords(p, tau, e, nb, kb);
+            int32_t t_beg, te;
+            expert_range(p, e, t_beg, te);
+            for (int32_t c0 = 0; ok && c0 < te; c0 += kChunk, ++g) {
+                const int32_t vc = min(kChunk, te - c0);
+                const uint32_t buf = g & 1, tph = (g >> 1) & 1;
+                if (!mbar_wait(&ctl->tempty[buf], tph ^ 1, abort_flag, p.hdr, 11)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + buf * BN;
+                for (int32_t s0 = 0; s0 < vc; s0 += BK) {
+                    if (!mbar_wait(&ctl->full[stage], phase, abort_flag, p.hdr, 12)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    uint8_t *sA = smem + stage * kStageBytes;
+                    uint8_t *sB = sA + kStageA;
+                    const int vst = min(BK, vc - s0);
+                    const int nk = (vst + 15) / 16;
+                    if (vst & 15) {
+                        // tokens [vst, 16*nk) of this stage belong to the next
+                        // expert (or lie past the tensor): zero them in A and B
+                        const int rows = 16 * nk - vst;
+                        for (int q = lane; q < 6 * rows * 8; q += 32) {
+                            const int box = q / (rows * 8);
+                            const int rr = (q / 8) % rows + vst;
+                            const int ch = q % 8;
+                            uint8_t *b = (box < 2 ? sA + box * kBoxBytes : sB + (box - 2) * kBoxBytes);
+                            *reinterpret_cast<uint4 *>(b + rr * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                    }
+                    if (lane == 0) {
+                        const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+                        for (int kk = 0; kk < nk; ++kk) {
+                            const uint64_t ad = smem_desc_sw128(a0 + kk * 2048, kLBO, kSBO);
+                            const uint64_t bd = smem_desc_sw128(b0 + kk * 2048, kLBO, kSBO);
+                            mma_bf16(d_tmem, ad, bd, kIdesc, (s0 > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        mma_commit(&ctl->empty[stage]);
+                    }
+                    __syncwarp();
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                if (lane == 0) mma_commit(&ctl->tfull[buf]);
+                __syncwarp();
+            }
+        }
+    } else {
+        // ---------------- epilogue: fold chunks, add into main_grad ----------------
+        const int q = warp & 3;                 // TMEM lane quarter this warp may access
+        const int h = (warp - 2) >> 2;          // column half of the tile
+        uint32_t g = 0;
+        bool ok = true;
+        float F[128];
+        for (int tau = blockIdx.x; ok && tau < p.n_tiles; tau += gridDim.x) {
+            int e, nb, kb;
+            tile_coords(p, tau, e, nb, kb);
+            int32_t t_beg, te;
+            expert_range(p, e, t_beg, te);
+            if (te == 0) continue;  // empty expert: main_grad untouched
+            for (int32_t c0 = 0; c0 < te; c0 += kChunk, ++g) {
+                const uint32_t buf = g & 1, tph = (g >> 1) & 1;
+                if (!mbar_wait(&ctl->tfull[buf], tph, abort_flag, p.hdr, 13)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t base = tmem + (static_cast<uint32_t>(32 * q) << 16) + buf * BN + 128 * h;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t r[32];
+                    tmem_ld32(base + 32 * j, r);
+                    tmem_wait_ld();
+                    if (c0 == 0) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) F[32 * j + i] = __uint_as_float(r[i]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) F[32 * j + i] = __fadd_rn(F[32 * j + i], __uint_as_float(r[i]));
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->tempty[buf]);
+            }
+            if (!ok) break;
+            const int n = nb * BM + 32 * q + lane;
+            float *mg = p.main_grad + (static_cast<int64_t>(e) * p.N + n) * p.K + kb * BN + 128 * h;
+#pragma unroll
+            for (int v0 = 0; v0 < 32; v0 += 8) {
+                float4 m[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) m[u] = reinterpret_cast<const float4 *>(mg)[v0 + u];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int f = 4 * (v0 + u);
+                    m[u].x = __fadd_rn(m[u].x, F[f]);
+                    m[u].y = __fadd_rn(m[u].y, F[f + 1]);
+                    m[u].z = __fadd_rn(m[u].z, F[f + 2]);
+                    m[u].w = __fadd_rn(m[u].w, F[f + 3]);
+                    reinterpret_cast<float4 *>(mg)[v0 + u] = m[u];
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// One K16 tensor-core step per CTA on caller data: D = [C +] A B, with A
+// [128 x 16] and B [16 x 256] bf16 placed in the same MN-major 128-byte
+// swizzle layout and descriptors as the wgrad kernel's stages. Used to check
+// the oracle's model of the step and the layout itself.
+// The probe holds a large allocation so that its descriptors can only ever
+// address shared memory the CTA owns.
+constexpr size_t kProbeSmem = 200 * 1024;
+
+__global__ void __launch_bounds__(128, 1)
+    tc_probe_kernel(const uint16_t *A, const uint16_t *B, const float *C, float *D, int accumulate, WsHeader *hdr) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + kStageA;
+    Ctl *ctl = reinterpret_cast<Ctl *>(smem + kStageBytes);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t prob = blockIdx.x;
+    A += prob * 128 * 16;
+    B += prob * 16 * 256;
+    C += prob * 128 * 256;
+    D += prob * 128 * 256;
+    for (int i = tid; i < static_cast<int>(kStageBytes / 16); i += 128)
+        reinterpret_cast<uint4 *>(smem)[i] = make_uint4(0, 0, 0, 0);
+    __syncthreads();
+    for (int i = tid; i < 128 * 16; i += 128) {
+        const int m = i / 16, k = i % 16;
+        *reinterpret_cast<uint16_t *>(sA + sw128_mn_offset(m, k, kLBO)) = A[i];
+    }
+    for (int i = tid; i < 16 * 256; i += 128) {
+        const int k = i / 256, n = i % 256;
+        *reinterpret_cast<uint16_t *>(sB + sw128_mn_offset(n, k, kLBO)) = B[i];
+    }
+    fence_proxy_async_smem();
+    if (tid == 0) {
+        mbar_init(&ctl->full[0], 1);
+        ctl->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&ctl->tmem_base, BN);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem_base;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+    const int row = 32 * warp + lane;
+#pragma unroll 1
+    for (int j = 0; j < BN / 32; ++j) {
+        uint32_t r[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(C[row * 256 + 32 * j + i]);
+        tmem_st32(lane_base + 32 * j, r);
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {
+        mma_bf16(tmem, smem_desc_sw128(smem_u32(sA), kLBO, kSBO), smem_desc_sw128(smem_u32(sB), kLBO, kSBO), kIdesc,
+                 accumulate ? 1u : 0u);
+        mma_commit(&ctl->full[0]);
+    }
+    __syncwarp();
+    const bool ok = mbar_wait(&ctl->full[0], 0, &ctl->abort, hdr, 20);
+    tc_fence_after();
+    if (ok) {
+#pragma unroll 1
+        for (int j = 0; j < BN / 32; ++j) {
+            uint32_t r[32];
+            tmem_ld32(lane_base + 32 * j, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) D[row * 256 + 32 * j + i] = __uint_as_float(r[i]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, BN);
+    }
+}
+
+// ---- host ---------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+dgr_status encode_fn(PFN_cuTensorMapEncodeTiled_v12000 *fn) {
+    std::call_once(g_encode_once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    if (!g_encode) return DGR_ERR_CUDA;
+    *fn = g_encode;
+    return DGR_OK;
+}
+
+// 2-D tensor map over a row-major bf16 [rows, cols] matrix, 64 x 64 boxes,
+// 128-byte swizzle, zero fill past the end.
+dgr_status make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    dgr_status st = encode_fn(&enc);
+    if (st != DGR_OK) return st;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
+    const cuuint32_t box[2] = {64, 64};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? DGR_OK : DGR_ERR_CUDA;
+}
+
+std::once_flag g_attr_once[64];
+cudaError_t g_attr_err[64];
+
+dgr_status set_smem_attrs() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DGR_ERR_CUDA;
+    std::call_once(g_attr_once[dev], [dev] {
+        cudaError_t e = cudaFuncSetAttribute(wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kSmemBytes));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(tc_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(kProbeSmem));
+        g_attr_err[dev] = e;
+    });
+    return g_attr_err[dev] == cudaSuccess ? DGR_OK : DGR_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace dgr
 
 using namespace dgr;
 
@@ -10,11 +434,62 @@ extern "C" size_t dgr_wgrad_workspace_bytes(int32_t E, int64_t N, int64_t K) {
     return sizeof(WsHeader);
 }
 
-extern "C" dgr_status dgr_grouped_wgrad_accumulate(const void *G, const void *X, const int64_t *d_offs,
-                                                   int32_t E, int64_t T_total, int64_t N, int64_t K,
-                                                   float *main_grad, int32_t chunk_tokens, void *ws,
-                                                   size_t ws_bytes, void *stream) {
-    (void)G; (void)X; (void)d_offs; (void)E; (void)T_total; (void)N; (void)K; (void)main_grad;
-    (void)chunk_tokens; (void)ws; (void)ws_bytes; (void)stream;
-    return DGR_ERR_UNSUPPORTED;
+extern "C" dgr_status dgr_grouped_wgrad_accumulate(const void *G, const void *X, const int64_t *d_offs, int32_t E,
+                                                   int64_t T_total, int64_t N, int64_t K, float *main_grad,
+                                                   int32_t chunk_tokens, void *ws, size_t ws_bytes, void *stream) {
+    if (E < 1 || T_total < 0 || N <= 0 || K <= 0 || chunk_tokens != kChunk) return DGR_ERR_INVALID_ARG;
+    if (N % BM != 0 || K % BN != 0 || T_total >= INT32_MAX || N > (1 << 20) || K > (1 << 20))
+        return DGR_ERR_UNSUPPORTED;
+    if (!main_grad || !d_offs || !ws || (T_total > 0 && (!G || !X))) return DGR_ERR_INVALID_ARG;
+    if (ws_bytes < sizeof(WsHeader)) return DGR_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned(G, 16) || !aligned(X, 16) || !aligned(main_grad, 32) || !aligned(d_offs, 8) ||
+        !aligned(ws, kAlign))
+        return DGR_ERR_MISALIGNED;
+    const size_t mg_bytes = static_cast<size_t>(E) * N * K * 4;
+    if (ranges_overlap(main_grad, mg_bytes, G, T_total * N * 2) ||
+        ranges_overlap(main_grad, mg_bytes, X, T_total * K * 2) ||
+        ranges_overlap(main_grad, mg_bytes, d_offs, (E + 1) * 8) || ranges_overlap(main_grad, mg_bytes, ws, ws_bytes))
+        return DGR_ERR_ALIAS;
+    dgr_status st = check_device();
+    if (st != DGR_OK) return st;
+    if (T_total == 0) return DGR_OK;
+    st = set_smem_attrs();
+    if (st != DGR_OK) return st;
+    CUtensorMap mG, mX;
+    if ((st = make_map(&mG, G, T_total, N)) != DGR_OK) return st;
+    if ((st = make_map(&mX, X, T_total, K)) != DGR_OK) return st;
+    WgradParams p{};
+    p.offs = d_offs;
+    p.E = E;
+    p.N = static_cast<int32_t>(N);
+    p.K = static_cast<int32_t>(K);
+    p.n_blk = static_cast<int32_t>(N / BM);
+    p.k_blk = static_cast<int32_t>(K / BN);
+    const int64_t n_tiles = static_cast<int64_t>(E) * p.n_blk * p.k_blk;
+    if (n_tiles > INT32_MAX) return DGR_ERR_UNSUPPORTED;
+    p.n_tiles = static_cast<int32_t>(n_tiles);
+    p.main_grad = main_grad;
+    p.hdr = static_cast<WsHeader *>(ws);
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DGR_ERR_CUDA;
+    const int grid = static_cast<int>(n_tiles < sms ? n_tiles : sms);
+    wgrad_kernel<<<grid, kThreadsW, kSmemBytes, static_cast<cudaStream_t>(stream)>>>(mG, mX, p);
+    return launch_status();
+}
+
+extern "C" dgr_status dgr_tc_probe_k16(const uint16_t *A, const uint16_t *B, const float *C, float *D, int32_t n_prob,
+                                       int32_t accumulate, void *ws, size_t ws_bytes, void *stream) {
+    if (n_prob < 0 || !A || !B || !C || !D || !ws) return DGR_ERR_INVALID_ARG;
+    if (ws_bytes < sizeof(WsHeader)) return DGR_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned(A, 2) || !aligned(B, 2) || !aligned(C, 4) || !aligned(D, 4) || !aligned(ws, kAlign))
+        return DGR_ERR_MISALIGNED;
+    dgr_status st = check_device();
+    if (st != DGR_OK) return st;
+    if (n_prob == 0) return DGR_OK;
+    st = set_smem_attrs();
+    if (st != DGR_OK) return st;
+    tc_probe_kernel<<<n_prob, 128, kProbeSmem, static_cast<cudaStream_t>(stream)>>>(
+        A, B, C, D, accumulate, static_cast<WsHeader *>(ws));
+    return launch_status();
 }

@@ -209,3 +209,72 @@ def wgrad_input(E: int, T: int, N: int, K: int, *, seed: int, dist: str = "norma
 
 def wgrad_full() -> WgradInput:
     return wgrad_input(8, 32768, 4096, 2048, seed=5)
+
+
+# --------------------------------------------------------------------------
+# one tensor-core K16 step (inputs for the hardware check of the step model)
+# --------------------------------------------------------------------------
+
+@dataclass
+class TcStepInput:
+    A: np.ndarray   # bf16 bits [n, 128, 16]
+    B: np.ndarray   # bf16 bits [n, 16, 256]
+    C: np.ndarray   # fp32 [n, 128, 256]
+    accumulate: int
+
+
+def _bf16_bits_np(x: np.ndarray) -> np.ndarray:
+    return bits(torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.bfloat16))
+
+
+def _wide(rng, shape, lo, hi):
+    s = rng.choice([-1.0, 1.0], shape)
+    return (s * (1 + rng.random(shape)) * np.exp2(rng.integers(lo, hi, shape))).astype(np.float32)
+
+
+def tc_step_input(kind: str, n: int, seed: int) -> TcStepInput:
+    """kind: 'normal' (N(0,1) operands and accumulator), 'normal_noacc' (no
+    accumulator input), 'wide' (magnitudes 2^-12..2^12, accumulator 2^-20..2^20),
+    'designed' (B = 1: rows of A are 16-term patterns - one large term among
+    tiny ones, cancelling pairs, equal magnitudes, spread powers of two - added
+    to accumulators from 2^-40 to 2^30)."""
+    rng = np.random.default_rng(seed)
+    acc = 0 if kind == "normal_noacc" else 1
+    if kind in ("normal", "normal_noacc"):
+        A = rng.standard_normal((n, 128, 16)).astype(np.float32)
+        B = rng.standard_normal((n, 16, 256)).astype(np.float32)
+        C = rng.standard_normal((n, 128, 256)).astype(np.float32)
+    elif kind == "wide":
+        A = _wide(rng, (n, 128, 16), -12, 12)
+        B = _wide(rng, (n, 16, 256), -12, 12)
+        C = _wide(rng, (n, 128, 256), -20, 20)
+    elif kind == "designed":
+        A = np.zeros((n, 128, 16), np.float32)
+        C = np.zeros((n, 128, 256), np.float32)
+        for p in range(n):
+            for m in range(128):
+                k = rng.integers(0, 6)
+                if k == 0:
+                    A[p, m] = _wide(rng, (16,), -30, -10)
+                    A[p, m, rng.integers(16)] = _wide(rng, (1,), 0, 4)[0]
+                elif k == 1:
+                    A[p, m] = _wide(rng, (16,), -26, -14)
+                    i, j = rng.choice(16, 2, replace=False)
+                    big = _wide(rng, (1,), 2, 10)[0]
+                    A[p, m, i], A[p, m, j] = big, -big
+                elif k == 2:
+                    A[p, m] = rng.choice([-1, 1], 16) * np.exp2(rng.integers(-30, 0))
+                elif k == 3:
+                    A[p, m] = rng.choice([-1, 1], 16) * np.exp2(rng.integers(-40, 5, 16))
+                elif k == 4:
+                    A[p, m, rng.integers(16)] = _wide(rng, (1,), -10, 10)[0]
+                else:
+                    A[p, m] = _wide(rng, (16,), -8, 8)
+                c = rng.integers(0, 4)
+                C[p, m] = (_wide(rng, (256,), -6, 6) if c == 0 else _wide(rng, (256,), 10, 30) if c == 1 else
+                           np.exp2(rng.integers(-30, 30, 256)) * rng.choice([-1, 1], 256) if c == 2 else
+                           _wide(rng, (256,), -40, -20)).astype(np.float32)
+        B = np.ones((n, 16, 256), np.float32)
+    else:
+        raise ValueError(kind)
+    return TcStepInput(_bf16_bits_np(A), _bf16_bits_np(B), C, acc)

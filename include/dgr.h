@@ -204,7 +204,7 @@ dgr_status dgr_det_index_add(float *out, int64_t R, int64_t D, int64_t ld_out, c
  * main_grad: [E, N, K] fp32, dense.
  * chunk_tokens: 512.
  * Limits:   N a multiple of 128, K a multiple of 256, E >= 1, T_total < 2^31.
- * Alignment: G, X 1024-byte aligned; main_grad 32-byte aligned.
+ * Alignment: G, X 16-byte aligned; main_grad 32-byte aligned.
  * ws:       dgr_wgrad_workspace_bytes() bytes, zeroed once (status word).
  * main_grad must not overlap G, X, d_offs or ws.
  */

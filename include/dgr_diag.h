@@ -1,0 +1,44 @@
+/*
+ * dgr_diag.h - diagnostics of the dgr library (GB300, sm_103a).
+ *
+ * Not part of the reduction path. These entries exist so that tests can
+ * check the assumptions the path rests on against the hardware itself.
+ */
+#ifndef DGR_DIAG_H
+#define DGR_DIAG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "dgr.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * One tensor-core K16 step (tcgen05.mma kind::f16, bf16 inputs, fp32
+ * accumulator, M = 128, N = 256) per problem: D = C + A B (accumulate != 0)
+ * or D = A B (accumulate = 0, the accumulator input disabled, as on the first
+ * step of a wgrad chunk). The operands are placed in shared memory with the
+ * same MN-major 128-byte-swizzle layout and descriptors as the grouped wgrad
+ * kernel's pipeline stages.
+ *
+ * The grouped wgrad of FlashInfer PR #8924 ("Design and numerics") fixes the
+ * split order but not the arithmetic inside one tensor-core step; the tests
+ * use this entry to check the oracle's model of that step bit for bit, in
+ * the manner of Fasi, Higham, Mikaitis and Pranesh, "Numerical behavior of
+ * NVIDIA tensor cores" (PeerJ CS 7:e330, 2021).
+ *
+ * A: [n_prob][128][16] bf16 bits (row m, column k), B: [n_prob][16][256] bf16
+ * bits (row k, column n), C, D: [n_prob][128][256] fp32; device pointers.
+ * ws: at least 256 bytes, zeroed (status word, see dgr_read_device_status()).
+ */
+dgr_status dgr_tc_probe_k16(const uint16_t *A, const uint16_t *B, const float *C, float *D, int32_t n_prob,
+                            int32_t accumulate, void *ws, size_t ws_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DGR_DIAG_H */

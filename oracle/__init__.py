@@ -43,11 +43,12 @@ def build(force: bool = False) -> str:
 class TcModel(ctypes.Structure):
     """Parameters of the tensor-core K16 step model (see dgr_oracle.c)."""
     _fields_ = [("group", ctypes.c_int32), ("frac_bits", ctypes.c_int32),
-                ("acc_in_sum", ctypes.c_int32), ("final_rn", ctypes.c_int32)]
+                ("acc_in_sum", ctypes.c_int32), ("final_rn", ctypes.c_int32),
+                ("ref_from_fields", ctypes.c_int32)]
 
     def __repr__(self) -> str:
-        return (f"TcModel(group={self.group}, frac_bits={self.frac_bits}, "
-                f"acc_in_sum={self.acc_in_sum}, final_rn={self.final_rn})")
+        return (f"TcModel(group={self.group}, frac_bits={self.frac_bits}, acc_in_sum={self.acc_in_sum}, "
+                f"final_rn={self.final_rn}, ref_from_fields={self.ref_from_fields})")
 
 
 _lib = None

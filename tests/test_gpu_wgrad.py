@@ -1,0 +1,102 @@
+"""GPU checks of the grouped wgrad accumulate (FlashInfer PRs #8602 / #8924).
+
+With ternary inputs every product, chunk partial, fold and the final add is an
+exact small integer, so the result must equal numpy's int64 G_e^T X_e plus
+main_grad bit for bit whatever the arithmetic inside a tensor-core step: this
+checks the shared-memory layout and descriptors, the pipeline, expert offsets
+(ragged, empty, not multiples of the 64-token stage or 16-token step), chunk
+tails and the final add. Empty experts must leave main_grad bitwise unchanged,
+and repeated calls must give identical bits.
+"""
+import numpy as np
+import pytest
+import torch
+
+import deterministic_gradient_reduction_gb300 as dgr
+import dgr_inputs as gi
+from util import assert_bits_equal
+
+pytestmark = pytest.mark.gpu
+
+
+def _exact(wi: gi.WgradInput) -> np.ndarray:
+    G = wi.G.to(torch.float64).numpy()
+    X = wi.X.to(torch.float64).numpy()
+    out = wi.main_grad.to(torch.float64).numpy().copy()
+    o = wi.offs.numpy()
+    for e in range(wi.E):
+        out[e] += G[o[e]:o[e + 1]].T @ X[o[e]:o[e + 1]]
+    return out
+
+
+def _gpu(wi: gi.WgradInput, dev=None, ws=None):
+    G, X, offs, mg = (wi.G.cuda(), wi.X.cuda(), wi.offs.cuda(), wi.main_grad.cuda()) if dev is None else dev
+    out = mg.clone()
+    dgr.grouped_wgrad_accumulate(G, X, offs, out, ws=ws)
+    return out
+
+
+@pytest.mark.parametrize("counts,N,K", [
+    ([512, 0, 1029, 300], 128, 256),        # ragged, one empty expert
+    ([1, 15, 17, 511, 513, 64, 1000], 256, 512),
+    ([4096, 4096], 384, 768),
+    ([0, 0, 777], 128, 256),
+])
+def test_ternary_exact(counts, N, K):
+    wi = gi.wgrad_input(len(counts), sum(counts), N, K, seed=900 + N, dist="ternary", counts=counts)
+    got = _gpu(wi).cpu().numpy()
+    assert_bits_equal(got, _exact(wi).astype(np.float32), f"wgrad ternary {counts}")
+    for e, c in enumerate(counts):
+        if c == 0:
+            assert_bits_equal(got[e], gi.f32(wi.main_grad)[e], f"empty expert {e}")
+
+
+def test_full_shape_ternary_and_replay():
+    # the benchmark's shape with ternary data: exact, and identical over replays
+    wi = gi.wgrad_input(8, 32768, 4096, 2048, seed=5, dist="ternary")
+    dev = (wi.G.cuda(), wi.X.cuda(), wi.offs.cuda(), wi.main_grad.cuda())
+    first = _gpu(wi, dev)
+    want = _exact(wi).astype(np.float32)
+    assert_bits_equal(first.cpu().numpy(), want, "full ternary")
+    for _ in range(3):
+        again = _gpu(wi, dev)
+        assert torch.equal(again.view(torch.int32), first.view(torch.int32))
+
+
+def _oracle_full(wi: gi.WgradInput) -> np.ndarray:
+    import oracle
+    T, N = wi.G.shape
+    K = wi.X.shape[1]
+    mg = gi.f32(wi.main_grad).copy()
+    oracle.grouped_wgrad_accumulate(gi.bits(wi.G), gi.bits(wi.X), wi.offs.numpy(), wi.E, N, K, mg)
+    return mg
+
+
+@pytest.mark.parametrize("counts,N,K", [([700, 0, 1029, 300], 128, 256), ([17, 513, 64], 256, 512)])
+def test_random_parity_full_output(counts, N, K):
+    wi = gi.wgrad_input(len(counts), sum(counts), N, K, seed=1000 + N, counts=counts)
+    got = _gpu(wi).cpu().numpy()
+    assert_bits_equal(got, _oracle_full(wi), f"wgrad random {counts}")
+
+
+def test_full_workload_sampled_parity_and_replay():
+    import oracle
+    wi = gi.wgrad_full()
+    dev = (wi.G.cuda(), wi.X.cuda(), wi.offs.cuda(), wi.main_grad.cuda())
+    first = _gpu(wi, dev)
+    for _ in range(2):
+        assert torch.equal(_gpu(wi, dev).view(torch.int32), first.view(torch.int32))
+    got = first.cpu().numpy()
+    rng = np.random.default_rng(11)
+    e = [rng.integers(0, 8, 4096)]
+    n = [rng.integers(0, 4096, 4096)]
+    k = [rng.integers(0, 2048, 4096)]
+    for ee in range(8):  # a 32 x 32 block at a tile corner of every expert
+        nn, kk = np.meshgrid(np.arange(96, 128), np.arange(224, 256), indexing="ij")
+        e.append(np.full(1024, ee))
+        n.append(nn.reshape(-1))
+        k.append(kk.reshape(-1))
+    e, n, k = (np.concatenate(v).astype(np.int64) for v in (e, n, k))
+    mg0 = gi.f32(wi.main_grad)[e, n, k]
+    want = oracle.wgrad_elements(gi.bits(wi.G), gi.bits(wi.X), wi.offs.numpy(), 4096, 2048, e, n, k, mg0)
+    assert_bits_equal(got[e, n, k], want, "wgrad full, sampled")
