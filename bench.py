@@ -151,14 +151,20 @@ class ClockSampler:
 # our arm
 # ---------------------------------------------------------------------------
 
-def make_ops(dev, torch, dgr, with_wgrad):
-    """Build device inputs and one closure per operation (enqueue only)."""
+def make_ops(dev, torch, dgr, with_wgrad, only=None, small=False):
+    """Build device inputs and one closure per operation (enqueue only).
+    `only` keeps one operation; `small` shrinks colsum_large, dprob and wgrad
+    (fewer tokens / rows, same widths) for profiler captures."""
     ops, host, outs = {}, {}, {}
+    want = (lambda n: only is None or n == only)
 
-    cl = gi.colsum_large()
-    cs = gi.colsum_small()
-    cst = gi.colsum_strided()
-    for name, ci in (("colsum_large", cl), ("colsum_small", cs), ("colsum_strided", cst)):
+    gens = {"colsum_large": (gi.colsum_large if not small else
+                             (lambda: gi.colsum_input(1, 2097152, 64, seed=4, scale=0.02))),
+            "colsum_small": gi.colsum_small, "colsum_strided": gi.colsum_strided}
+    for name, gen in gens.items():
+        if not want(name):
+            continue
+        ci = gen()
         base = ci.base.to(dev)
         x = base.as_strided((ci.B, ci.S, ci.H), (ci.stride_b, ci.stride_s, 1))
         out = torch.zeros(ci.H, device=dev)
@@ -166,28 +172,29 @@ def make_ops(dev, torch, dgr, with_wgrad):
         ops[name] = (lambda x=x, out=out, ws=ws: dgr.ordered_colsum(x, out, ws=ws))
         host[name] = ([ci.base], [base])
         outs[name] = out
-    dp = gi.dprob_full()
-    dY, Y = dp.dY.to(dev), dp.Y.to(dev)
-    dprob = torch.zeros(dp.M, device=dev)
-    ops["dprob"] = lambda: dgr.ordered_rowdot_dprob(dY, Y, dprob)
-    host["dprob"] = ([dp.dY, dp.Y], [dY, Y])
-    outs["dprob"] = dprob
-    ia = gi.index_add_full()
-    src, idx, iout = ia.src.to(dev), ia.idx.to(dev), ia.out.to(dev)
-    iws = dgr.workspace(dgr.index_add_workspace_bytes(262144, 16384, 128), dev)
-    ops["index_add"] = lambda: dgr.det_index_add(iout, src, idx, ws=iws)
-    host["index_add"] = ([ia.src, ia.idx, ia.out], [src, idx, iout])
-    outs["index_add"] = iout
-    if with_wgrad:
-        wi = gi.wgrad_full()
+    if want("dprob"):
+        dp = gi.dprob_full() if not small else gi.dprob_input(16384, 4096, seed=3)
+        dY, Y = dp.dY.to(dev), dp.Y.to(dev)
+        dprob = torch.zeros(dp.M, device=dev)
+        ops["dprob"] = lambda: dgr.ordered_rowdot_dprob(dY, Y, dprob)
+        host["dprob"] = ([dp.dY, dp.Y], [dY, Y])
+        outs["dprob"] = dprob
+    if want("index_add"):
+        ia = gi.index_add_full()
+        src, idx, iout = ia.src.to(dev), ia.idx.to(dev), ia.out.to(dev)
+        iws = dgr.workspace(dgr.index_add_workspace_bytes(262144, 16384, 128), dev)
+        ops["index_add"] = lambda: dgr.det_index_add(iout, src, idx, ws=iws)
+        host["index_add"] = ([ia.src, ia.idx, ia.out], [src, idx, iout])
+        outs["index_add"] = iout
+    if with_wgrad and want("wgrad"):
+        wi = gi.wgrad_full() if not small else gi.wgrad_input(8, 8192, 4096, 2048, seed=5)
         G, X, offs, mg = wi.G.to(dev), wi.X.to(dev), wi.offs.to(dev), wi.main_grad.to(dev)
         wws = dgr.workspace(dgr.wgrad_workspace_bytes(8, 4096, 2048), dev)
         ops["wgrad"] = lambda: dgr.grouped_wgrad_accumulate(G, X, offs, mg, ws=wws)
         host["wgrad"] = ([wi.G, wi.X, wi.offs, wi.main_grad], [G, X, offs, mg])
         outs["wgrad"] = mg
-    order = ["colsum_large", "colsum_small", "dprob", "colsum_strided", "index_add"]
-    if with_wgrad:
-        order.append("wgrad")
+    order = [n for n in ["colsum_large", "colsum_small", "dprob", "colsum_strided", "index_add", "wgrad"]
+             if n in ops]
     return order, ops, host, outs
 
 
@@ -212,7 +219,19 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     with_wgrad = wgrad_available(dgr)
-    order, ops, host, outs = make_ops(dev, torch, dgr, with_wgrad)
+    order, ops, host, outs = make_ops(dev, torch, dgr, with_wgrad, args.only, args.small)
+    if args.only or args.small:  # a profiling run: time it, print the per-operation figures only
+        for _ in range(args.warmup):
+            for name in order:
+                ops[name]()
+        torch.cuda.synchronize()
+        for _ in range(args.steps):
+            for name in order:
+                ops[name]()
+        torch.cuda.synchronize()
+        if rank == 0:
+            print(json.dumps({"profile_run": True, "only": args.only, "small": args.small, "ops": order}))
+        return
     stream = torch.cuda.current_stream()
 
     def barrier():
@@ -427,6 +446,10 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["colsum_large", "colsum_small", "dprob", "colsum_strided", "index_add",
+                                       "wgrad"], help="profiling: run one operation only (no JSON bench line)")
+    ap.add_argument("--small", action="store_true",
+                    help="profiling: colsum 2097152x64, dprob 16384x4096, wgrad T=8192 (same widths)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -5,20 +5,24 @@
 // dK is an index_add done as a stable sort plus a (prefix) sum, with padding
 // slots spread over dummy rows that the caller drops. Four launches:
 //   K1 count   - map idx to keys (idx outside [0, R) -> R; outside [-1, R) is
-//                counted), per-block histograms of the key's high byte; the
-//                last block to finish scans them (digit-major) into per-block
-//                scatter offsets and bucket starts.
+//                counted), per-block histograms of the key's high byte and each
+//                bucket's key range; the last block to finish scans the
+//                histograms (digit-major) into per-block scatter offsets and
+//                bucket starts, and marks buckets that hold a single key.
 //   K2 scatter - stable scatter by the high byte: inside a block, elements are
 //                ranked in original order with warp match/ballot and per-warp
-//                digit counters, so equal digits keep their input order.
+//                digit counters, so equal digits keep their input order. A
+//                single-key bucket (the dummy row) is already in final order
+//                and goes straight to the sorted arrays.
 //   K3 bucket  - one block per high-byte bucket: counting sort by the low byte
 //                (stable, same ranking), which also yields seg_start[] for the
-//                bucket's 256 keys; a bucket holding one key is copied as is.
+//                bucket's 256 keys, and lists the tiles of rows too long for
+//                one warp.
 //   K4 segsum  - one warp per destination row sums its members (in original
 //                order) by the pairwise tree over tiles of 128 members and folds
 //                the tiles in order, then out[r] += sum with one rounding.
 //                Rows with more than 8 tiles are split: one warp per 32-member
-//                quarter of each tile writes a slot; the last quarter of a tile
+//                quarter of each listed tile writes a slot; the last quarter of a tile
 //                to arrive (an integer ticket) combines the quarters into the
 //                tile partial, and the last tile of the row folds the tile
 //                partials in order.
@@ -30,8 +34,8 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kItems = 8;
-constexpr int kBlockElems = kThreads * kItems;  // 2048 elements per sort block
+constexpr int kItems = 32;
+constexpr int kBlockElems = kThreads * kItems;  // 8192 elements per sort block
 constexpr int kDigits = 256;
 constexpr int kSegTile = 128;
 constexpr int kWarpMaxTiles = 8;                // rows up to 1024 members: one warp
@@ -43,7 +47,7 @@ struct IdxParams {
     int32_t N, R, D;
     int32_t nb;             // sort blocks
     int32_t n_buckets;      // high-byte buckets covering keys 0..R
-    int32_t n_pblk;         // 128-position blocks (split-row warps = 4 * n_pblk)
+    int32_t n_pblk;         // 128-position blocks of the sorted order (slot indexing)
     int32_t seg_tile;
     const float *src;
     int64_t ld_src;
@@ -51,6 +55,8 @@ struct IdxParams {
     int64_t ld_out;
     int32_t *bad_count;
     int32_t *keys_a, *vals_a, *perm, *skey, *hist, *offs, *bucket_start, *seg_start, *tickets, *tile_tickets;
+    int32_t *bucket_negmin, *bucket_max, *bucket_key;
+    int2 *heavy;  // (row, tile) of every tile of a row with more than 8 tiles
     float *slots;
     WsHeader *hdr;
 };
@@ -72,27 +78,44 @@ __device__ __forceinline__ unsigned lanemask_lt() {
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads) count_kernel(const IdxParams p) {
     __shared__ int32_t h[kDigits];
+    __shared__ int32_t mn[kDigits];
+    __shared__ int32_t mx[kDigits];
     __shared__ int32_t base[kDigits + 1];
     __shared__ int32_t bad_block;
     __shared__ int is_last;
     const int tid = threadIdx.x;
     const int b = blockIdx.x;
     h[tid] = 0;
+    mn[tid] = INT32_MAX;
+    mx[tid] = -1;
     if (tid == 0) bad_block = 0;
+    if (b == 0 && tid == 0) p.hdr->pad[3] = 0;  // heavy-tile list of this call starts empty
     __syncthreads();
+    int32_t v[kItems];
+#pragma unroll
+    for (int r = 0; r < kItems; ++r) {
+        const int64_t e = static_cast<int64_t>(b) * kBlockElems + r * kThreads + tid;
+        v[r] = e < p.N ? p.idx[e] : INT32_MIN;
+    }
     int my_bad = 0;
-    for (int i = tid; i < kBlockElems; i += kThreads) {
-        const int64_t e = static_cast<int64_t>(b) * kBlockElems + i;
-        if (e < p.N) {
-            bool bad = false;
-            const int32_t k = map_key(p.idx[e], p.R, bad);
-            my_bad += bad ? 1 : 0;
-            atomicAdd(&h[k >> 8], 1);
-        }
+#pragma unroll
+    for (int r = 0; r < kItems; ++r) {
+        if (v[r] == INT32_MIN && static_cast<int64_t>(b) * kBlockElems + r * kThreads + tid >= p.N) continue;
+        bool bad = false;
+        const int32_t k = map_key(v[r], p.R, bad);
+        my_bad += bad ? 1 : 0;
+        atomicAdd(&h[k >> 8], 1);
+        atomicMin(&mn[k >> 8], k);
+        atomicMax(&mx[k >> 8], k);
     }
     if (my_bad) atomicAdd(&bad_block, my_bad);
     __syncthreads();
-    p.hist[static_cast<int64_t>(tid) * p.nb + b] = h[tid];
+    p.hist[static_cast<int64_t>(b) * kDigits + tid] = h[tid];
+    if (h[tid] > 0) {
+        // per-bucket key range over all blocks (integer max: order-free)
+        atomicMax(&p.bucket_negmin[tid], INT32_MAX - mn[tid]);
+        atomicMax(&p.bucket_max[tid], mx[tid]);
+    }
     if (tid == 0 && bad_block) atomicAdd(&p.hdr->pad[2], bad_block);
     __threadfence();
     __syncthreads();
@@ -100,9 +123,16 @@ __global__ void __launch_bounds__(kThreads) count_kernel(const IdxParams p) {
     __syncthreads();
     if (!is_last) return;
     __threadfence();
-    // digit-major exclusive scan: offs[d][b] = sum of digits < d + counts of d in blocks < b
+    // digit-major exclusive scan: offs[b][d] = sum of digits < d + counts of d in blocks < b
     int32_t total = 0;
-    for (int bb = 0; bb < p.nb; ++bb) total += __ldcg(&p.hist[static_cast<int64_t>(tid) * p.nb + bb]);
+    for (int b0 = 0; b0 < p.nb; b0 += 16) {
+        int32_t c[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+            c[u] = (b0 + u < p.nb) ? __ldcg(&p.hist[static_cast<int64_t>(b0 + u) * kDigits + tid]) : 0;
+#pragma unroll
+        for (int u = 0; u < 16; ++u) total += c[u];
+    }
     h[tid] = total;
     __syncthreads();
     if (tid == 0) {
@@ -115,12 +145,25 @@ __global__ void __launch_bounds__(kThreads) count_kernel(const IdxParams p) {
     }
     __syncthreads();
     int32_t run = base[tid];
-    for (int bb = 0; bb < p.nb; ++bb) {
-        const int64_t q = static_cast<int64_t>(tid) * p.nb + bb;
-        p.offs[q] = run;
-        run += __ldcg(&p.hist[q]);
+    for (int b0 = 0; b0 < p.nb; b0 += 16) {
+        int32_t c[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+            c[u] = (b0 + u < p.nb) ? __ldcg(&p.hist[static_cast<int64_t>(b0 + u) * kDigits + tid]) : 0;
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            if (b0 + u < p.nb) {
+                p.offs[static_cast<int64_t>(b0 + u) * kDigits + tid] = run;
+                run += c[u];
+            }
+        }
     }
     p.bucket_start[tid] = base[tid];
+    const int32_t kmax = __ldcg(&p.bucket_max[tid]);
+    const int32_t kmin = INT32_MAX - __ldcg(&p.bucket_negmin[tid]);
+    p.bucket_key[tid] = (total > 0 && kmin == kmax) ? kmax : -1;  // one key: its order is final after K2
+    p.bucket_negmin[tid] = 0;
+    p.bucket_max[tid] = 0;
     if (tid == 0) {
         p.bucket_start[kDigits] = base[kDigits];
         const int32_t bad = atomicAdd(&p.hdr->pad[2], 0);
@@ -130,8 +173,8 @@ __global__ void __launch_bounds__(kThreads) count_kernel(const IdxParams p) {
     }
 }
 
-// Stable in-block ranking: warp w owns elements [w*256, w*256 + 256) of the
-// block in 8 rounds of 32 (round-major, lane order = element order). Returns
+// Stable in-block ranking: warp w owns elements [w*kWarpElems, ...) of the
+// block in rounds of 32 (round-major, lane order = element order). Returns
 // each element's rank among equal digits inside its warp; cnt[w][d] ends as
 // the warp's digit counts.
 __device__ __forceinline__ void warp_rank(int digit, bool valid, int32_t (*cnt)[kDigits], int w, int32_t &rank) {
@@ -146,24 +189,31 @@ __device__ __forceinline__ void warp_rank(int digit, bool valid, int32_t (*cnt)[
 }
 
 // ---------------------------------------------------------------------------
-// K2: stable scatter by the high byte.
+// K2: stable scatter by the high byte. Elements of a one-key bucket go
+// straight to their final place (perm/skey); the others to keys_a/vals_a.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads) scatter_high_kernel(const IdxParams p) {
     __shared__ int32_t cnt[kWarps][kDigits];
     __shared__ int32_t pre[kWarps][kDigits];
+    __shared__ int32_t boff[kDigits];
+    __shared__ int32_t bkey[kDigits];
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     const int b = blockIdx.x;
     for (int q = tid; q < kWarps * kDigits; q += kThreads) (&cnt[0][0])[q] = 0;
+    boff[tid] = p.offs[static_cast<int64_t>(b) * kDigits + tid];
+    bkey[tid] = p.bucket_key[tid];
     __syncthreads();
-    int32_t key[kItems], rank[kItems];
+    const int64_t e0 = static_cast<int64_t>(b) * kBlockElems + w * (kItems * 32) + lane;
+    int32_t key[kItems];
 #pragma unroll
     for (int r = 0; r < kItems; ++r) {
-        const int64_t e = static_cast<int64_t>(b) * kBlockElems + w * (kItems * 32) + r * 32 + lane;
-        const bool valid = e < p.N;
+        const int64_t e = e0 + r * 32;
         bool bad = false;
-        key[r] = valid ? map_key(p.idx[e], p.R, bad) : -1;
-        warp_rank(valid ? (key[r] >> 8) : 0, valid, cnt, w, rank[r]);
+        key[r] = e < p.N ? map_key(p.idx[e], p.R, bad) : -1;
     }
+    int32_t rank[kItems];
+#pragma unroll
+    for (int r = 0; r < kItems; ++r) warp_rank(key[r] >> 8, key[r] >= 0, cnt, w, rank[r]);
     __syncthreads();
     {
         int32_t run = 0;
@@ -175,14 +225,26 @@ __global__ void __launch_bounds__(kThreads) scatter_high_kernel(const IdxParams 
     __syncthreads();
 #pragma unroll
     for (int r = 0; r < kItems; ++r) {
-        const int64_t e = static_cast<int64_t>(b) * kBlockElems + w * (kItems * 32) + r * 32 + lane;
-        if (e < p.N) {
-            const int d = key[r] >> 8;
-            const int32_t pos = p.offs[static_cast<int64_t>(d) * p.nb + b] + pre[w][d] + rank[r];
+        if (key[r] < 0) continue;
+        const int d = key[r] >> 8;
+        const int32_t pos = boff[d] + pre[w][d] + rank[r];
+        const int32_t e = static_cast<int32_t>(e0 + r * 32);
+        if (bkey[d] >= 0) {
+            p.perm[pos] = e;
+            p.skey[pos] = key[r];
+        } else {
             p.keys_a[pos] = key[r];
-            p.vals_a[pos] = static_cast<int32_t>(e);
+            p.vals_a[pos] = e;
         }
     }
+}
+
+// Heavy rows (more than kWarpMaxTiles tiles) get one list entry per tile.
+__device__ __forceinline__ void list_heavy_tiles(const IdxParams &p, int32_t key, int32_t n) {
+    if (n <= kWarpMaxTiles * kSegTile) return;
+    const int32_t n_tiles = (n + kSegTile - 1) / kSegTile;
+    const int32_t at = atomicAdd(&p.hdr->pad[3], n_tiles);
+    for (int32_t t = 0; t < n_tiles; ++t) p.heavy[at + t] = make_int2(key, t);
 }
 
 // ---------------------------------------------------------------------------
@@ -193,48 +255,56 @@ __global__ void __launch_bounds__(kThreads) bucket_kernel(const IdxParams p) {
     __shared__ int32_t base[kDigits];
     __shared__ int32_t cnt[kWarps][kDigits];
     __shared__ int32_t pre[kWarps][kDigits];
-    __shared__ int uniform;
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     const int d = blockIdx.x;
     const int32_t bs = p.bucket_start[d];
     const int32_t be = p.bucket_start[d + 1];
+    const int32_t k = d * 256 + tid;
+    const int32_t one_key = p.bucket_key[d];
+    if (one_key >= 0) {  // K2 already placed it; only the segment starts remain
+        if (k <= p.R) p.seg_start[k] = k <= one_key ? bs : be;
+        if (k == p.R) p.seg_start[p.R + 1] = p.N;
+        if (tid == 0 && p.seg_tile == kSegTile) list_heavy_tiles(p, one_key, be - bs);
+        return;
+    }
     h[tid] = 0;
-    if (tid == 0) uniform = 0;
     __syncthreads();
-    for (int32_t i = bs + tid; i < be; i += kThreads) atomicAdd(&h[p.keys_a[i] & 255], 1);
+    for (int32_t c0 = bs; c0 < be; c0 += kBlockElems) {
+        int32_t kk[kItems];
+#pragma unroll
+        for (int r = 0; r < kItems; ++r) {
+            const int32_t i = c0 + r * kThreads + tid;
+            kk[r] = i < be ? p.keys_a[i] : -1;
+        }
+#pragma unroll
+        for (int r = 0; r < kItems; ++r)
+            if (kk[r] >= 0) atomicAdd(&h[kk[r] & 255], 1);
+    }
     __syncthreads();
     if (tid == 0) {
         int32_t run = 0;
         for (int q = 0; q < kDigits; ++q) {
-            const int32_t c = h[q];
             base[q] = bs + run;
-            if (c == be - bs && c > 0) uniform = 1;
-            run += c;
+            run += h[q];
         }
     }
     __syncthreads();
-    const int32_t k = d * 256 + tid;
     if (k <= p.R) p.seg_start[k] = base[tid];
     if (k == p.R) p.seg_start[p.R + 1] = p.N;
-    if (uniform) {  // one key: the stable order is the input order
-        for (int32_t i = bs + tid; i < be; i += kThreads) {
-            p.perm[i] = p.vals_a[i];
-            p.skey[i] = p.keys_a[i];
-        }
-        return;
-    }
+    if (k <= p.R && p.seg_tile == kSegTile) list_heavy_tiles(p, k, h[tid]);
     for (int32_t c0 = bs; c0 < be; c0 += kBlockElems) {
         for (int q = tid; q < kWarps * kDigits; q += kThreads) (&cnt[0][0])[q] = 0;
         __syncthreads();
+        const int32_t e0 = c0 + w * (kItems * 32) + lane;
         int32_t key[kItems], val[kItems], rank[kItems];
 #pragma unroll
         for (int r = 0; r < kItems; ++r) {
-            const int32_t e = c0 + w * (kItems * 32) + r * 32 + lane;
-            const bool valid = e < be;
-            key[r] = valid ? p.keys_a[e] : 0;
-            val[r] = valid ? p.vals_a[e] : 0;
-            warp_rank(key[r] & 255, valid, cnt, w, rank[r]);
+            const int32_t e = e0 + r * 32;
+            key[r] = e < be ? p.keys_a[e] : -1;
+            val[r] = e < be ? p.vals_a[e] : 0;
         }
+#pragma unroll
+        for (int r = 0; r < kItems; ++r) warp_rank(key[r] & 255, key[r] >= 0, cnt, w, rank[r]);
         __syncthreads();
         {
             int32_t run = 0;
@@ -246,13 +316,11 @@ __global__ void __launch_bounds__(kThreads) bucket_kernel(const IdxParams p) {
         __syncthreads();
 #pragma unroll
         for (int r = 0; r < kItems; ++r) {
-            const int32_t e = c0 + w * (kItems * 32) + r * 32 + lane;
-            if (e < be) {
-                const int lo = key[r] & 255;
-                const int32_t pos = base[lo] + pre[w][lo] + rank[r];
-                p.perm[pos] = val[r];
-                p.skey[pos] = key[r];
-            }
+            if (key[r] < 0) continue;
+            const int lo = key[r] & 255;
+            const int32_t pos = base[lo] + pre[w][lo] + rank[r];
+            p.perm[pos] = val[r];
+            p.skey[pos] = key[r];
         }
         __syncthreads();
         {
@@ -349,98 +417,80 @@ __device__ __forceinline__ int64_t sub_slot(int32_t p0, int32_t t, int q) {
     return (static_cast<int64_t>(p0 >> 7) * 2 + (t == 0 ? 1 : 0)) * 4 + q;
 }
 
-__device__ __noinline__ void split_row_unit(const IdxParams &p, int32_t unit, int lane, float4 (*stk)[32]) {
-    const int32_t pb = unit >> 2;
+// One quarter (32 members) of one tile of a heavy row, from the list K3 built.
+// The last quarter of the tile to arrive (an integer ticket) combines the four
+// quarters into the tile partial by the top two levels of the tile's tree; the
+// last tile of the row to arrive folds the tile partials in ascending order.
+__device__ __noinline__ void heavy_unit(const IdxParams &p, int32_t unit, int lane, float4 (*stk)[32]) {
+    const int2 ent = p.heavy[unit >> 2];
     const int q = unit & 3;
-    for (int m = 0; m < 4; ++m) {
-        const int32_t pos = pb * 128 + m * 32 + lane;
-        bool start = false;
-        int32_t key = 0, s = 0, e = 0;
-        if (pos < p.N) {
-            key = p.skey[pos];
-            s = p.seg_start[key];
-            e = p.seg_start[key + 1];
-            start = (e - s > kWarpMaxTiles * kSegTile) && (((pos - s) & (kSegTile - 1)) == 0);
-        }
-        unsigned mask = __ballot_sync(0xffffffffu, start);
-        while (mask) {
-            const int src_lane = __ffs(mask) - 1;
-            mask &= mask - 1;
-            const int32_t p0 = __shfl_sync(0xffffffffu, pos, src_lane);
-            const int32_t k = __shfl_sync(0xffffffffu, key, src_lane);
-            const int32_t s0 = __shfl_sync(0xffffffffu, s, src_lane);
-            const int32_t e0 = __shfl_sync(0xffffffffu, e, src_lane);
-            const int32_t t = (p0 - s0) >> 7;
-            const int cnt_tile = min(kSegTile, e0 - p0);
-            const int cnt = min(kSub, cnt_tile - q * kSub);
-            const int32_t n_tiles = (e0 - s0 + kSegTile - 1) / kSegTile;
-            if (cnt > 0) {
-                for (int c0 = 0; c0 < p.D; c0 += 128) {
-                    const int col = c0 + lane * 4;
-                    const float4 v = window_sum(p, p0 + q * kSub, cnt, col < p.D ? col : -1, lane, stk);
-                    if (col < p.D)
-                        *reinterpret_cast<float4 *>(p.slots + sub_slot(p0, t, q) * p.D + col) = v;
-                }
-            }
-            __threadfence();
-            __syncwarp();
-            // the last of the tile's four quarters combines them into the tile
-            // partial (the top two levels of its tree), kept in quarter slot 0
-            const int64_t tslot = static_cast<int64_t>(p0 >> 7) * 2 + (t == 0 ? 1 : 0);
-            int tq = 0;
-            if (lane == 0) tq = atomicAdd(&p.tile_tickets[tslot], 1);
-            tq = __shfl_sync(0xffffffffu, tq, 0);
-            if (tq != 3) continue;
-            __threadfence();
-            for (int c0 = 0; c0 < p.D; c0 += 128) {
-                const int col = c0 + lane * 4;
-                if (col >= p.D) continue;
-                float4 sq[4];
-#pragma unroll
-                for (int qq = 0; qq < 4; ++qq)
-                    if (qq * kSub < cnt_tile)
-                        sq[qq] = __ldcg(reinterpret_cast<const float4 *>(p.slots + sub_slot(p0, t, qq) * p.D + col));
-                float4 a = sq[0];
-                if (cnt_tile > 32) a = f4add(a, sq[1]);
-                if (cnt_tile > 64) {
-                    float4 c = sq[2];
-                    if (cnt_tile > 96) c = f4add(c, sq[3]);
-                    a = f4add(a, c);
-                }
-                *reinterpret_cast<float4 *>(p.slots + sub_slot(p0, t, 0) * p.D + col) = a;
-            }
-            __threadfence();
-            __syncwarp();
-            int tk = 0;
-            if (lane == 0) {
-                p.tile_tickets[tslot] = 0;
-                tk = atomicAdd(&p.tickets[k], 1);
-            }
-            tk = __shfl_sync(0xffffffffu, tk, 0);
-            if (tk != n_tiles - 1) continue;
-            // the row's last tile folds the tile partials in ascending order,
-            // eight loads in flight at a time
-            __threadfence();
-            for (int c0 = 0; c0 < p.D; c0 += 128) {
-                const int col = c0 + lane * 4;
-                if (col >= p.D) continue;
-                float4 F = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int32_t t0 = 0; t0 < n_tiles; t0 += 8) {
-                    float4 v[8];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        if (t0 + u < n_tiles)
-                            v[u] = __ldcg(reinterpret_cast<const float4 *>(
-                                p.slots + sub_slot(s0 + (t0 + u) * kSegTile, t0 + u, 0) * p.D + col));
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        if (t0 + u < n_tiles) F = (t0 + u == 0) ? v[u] : f4add(F, v[u]);
-                }
-                add_out(p, k, col, F);
-            }
-            if (lane == 0) p.tickets[k] = 0;
+    const int32_t k = ent.x, t = ent.y;
+    const int32_t s0 = p.seg_start[k];
+    const int32_t e0 = p.seg_start[k + 1];
+    const int32_t p0 = s0 + t * kSegTile;
+    const int cnt_tile = min(kSegTile, e0 - p0);
+    const int cnt = min(kSub, cnt_tile - q * kSub);
+    const int32_t n_tiles = (e0 - s0 + kSegTile - 1) / kSegTile;
+    if (cnt > 0) {
+        for (int c0 = 0; c0 < p.D; c0 += 128) {
+            const int col = c0 + lane * 4;
+            const float4 v = window_sum(p, p0 + q * kSub, cnt, col < p.D ? col : -1, lane, stk);
+            if (col < p.D) *reinterpret_cast<float4 *>(p.slots + sub_slot(p0, t, q) * p.D + col) = v;
         }
     }
+    __threadfence();
+    __syncwarp();
+    const int64_t tslot = static_cast<int64_t>(p0 >> 7) * 2 + (t == 0 ? 1 : 0);
+    int tq = 0;
+    if (lane == 0) tq = atomicAdd(&p.tile_tickets[tslot], 1);
+    tq = __shfl_sync(0xffffffffu, tq, 0);
+    if (tq != 3) return;
+    __threadfence();
+    for (int c0 = 0; c0 < p.D; c0 += 128) {
+        const int col = c0 + lane * 4;
+        if (col >= p.D) continue;
+        float4 sq[4];
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq)
+            if (qq * kSub < cnt_tile)
+                sq[qq] = __ldcg(reinterpret_cast<const float4 *>(p.slots + sub_slot(p0, t, qq) * p.D + col));
+        float4 a = sq[0];
+        if (cnt_tile > 32) a = f4add(a, sq[1]);
+        if (cnt_tile > 64) {
+            float4 c = sq[2];
+            if (cnt_tile > 96) c = f4add(c, sq[3]);
+            a = f4add(a, c);
+        }
+        *reinterpret_cast<float4 *>(p.slots + sub_slot(p0, t, 0) * p.D + col) = a;
+    }
+    __threadfence();
+    __syncwarp();
+    int tk = 0;
+    if (lane == 0) {
+        p.tile_tickets[tslot] = 0;
+        tk = atomicAdd(&p.tickets[k], 1);
+    }
+    tk = __shfl_sync(0xffffffffu, tk, 0);
+    if (tk != n_tiles - 1) return;
+    __threadfence();
+    for (int c0 = 0; c0 < p.D; c0 += 128) {
+        const int col = c0 + lane * 4;
+        if (col >= p.D) continue;
+        float4 F = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int32_t b0 = 0; b0 < n_tiles; b0 += 8) {
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (b0 + u < n_tiles)
+                    v[u] = __ldcg(reinterpret_cast<const float4 *>(
+                        p.slots + sub_slot(s0 + (b0 + u) * kSegTile, b0 + u, 0) * p.D + col));
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (b0 + u < n_tiles) F = (b0 + u == 0) ? v[u] : f4add(F, v[u]);
+        }
+        add_out(p, k, col, F);
+    }
+    if (lane == 0) p.tickets[k] = 0;
 }
 
 __device__ void row_unit(const IdxParams &p, int32_t r, int lane, float4 (*stk)[32]) {
@@ -517,20 +567,19 @@ __global__ void __launch_bounds__(kThreads, 3) segsum_kernel(const IdxParams p) 
     const int lane = threadIdx.x & 31;
     float4 (*stk)[32] = stack[threadIdx.x >> 5];
     const int64_t wg = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-    const int64_t n_split = (p.seg_tile == kSegTile) ? static_cast<int64_t>(p.n_pblk) * 4 : 0;
-    if (wg < n_split) {
-        split_row_unit(p, static_cast<int32_t>(wg), lane, stk);
-        return;
-    }
-    const int64_t r = wg - n_split;
+    // the first 4 x (listed heavy tiles) warps also take one quarter of a heavy tile
+    const int64_t n_heavy = (p.seg_tile == kSegTile) ? static_cast<int64_t>(p.hdr->pad[3]) * 4 : 0;
+    if (wg < n_heavy) heavy_unit(p, static_cast<int32_t>(wg), lane, stk);
+    const int64_t r = wg;
     if (r > p.R) return;
     if (p.seg_tile == 2 || p.seg_tile == 4) row_unit_small(p, static_cast<int32_t>(r), lane);
     else row_unit(p, static_cast<int32_t>(r), lane, stk);
 }
 
 struct IdxLayout {
-    int32_t nb, n_buckets, n_pblk;
-    size_t keys_a, vals_a, perm, skey, hist, offs, bucket_start, seg_start, tickets, tile_tickets, slots, total;
+    int32_t nb, n_buckets, n_pblk, max_heavy;
+    size_t keys_a, vals_a, perm, skey, hist, offs, bucket_start, seg_start, tickets, tile_tickets, slots;
+    size_t bucket_negmin, bucket_max, bucket_key, heavy, total;
 };
 
 IdxLayout idx_layout(int64_t N, int64_t R, int64_t D) {
@@ -538,6 +587,8 @@ IdxLayout idx_layout(int64_t N, int64_t R, int64_t D) {
     L.nb = static_cast<int32_t>((N + kBlockElems - 1) / kBlockElems);
     L.n_buckets = static_cast<int32_t>((R + 1 + 255) / 256);
     L.n_pblk = static_cast<int32_t>((N + 127) / 128);
+    // tiles of rows with more than 8 tiles: at most N/128 plus one ragged tile per such row
+    L.max_heavy = static_cast<int32_t>(N / kSegTile + N / (kWarpMaxTiles * kSegTile + 1) + 1);
     size_t o = sizeof(WsHeader);
     auto take = [&](size_t bytes) {
         size_t at = o;
@@ -555,6 +606,10 @@ IdxLayout idx_layout(int64_t N, int64_t R, int64_t D) {
     L.tickets = take((R + 1) * 4);
     L.tile_tickets = take(static_cast<size_t>(L.n_pblk) * 2 * 4);
     L.slots = take(static_cast<size_t>(L.n_pblk) * 8 * D * 4);
+    L.bucket_negmin = take(kDigits * 4);
+    L.bucket_max = take(kDigits * 4);
+    L.bucket_key = take(kDigits * 4);
+    L.heavy = take(static_cast<size_t>(L.max_heavy) * 8);
     L.total = o;
     return L;
 }
@@ -626,12 +681,16 @@ extern "C" dgr_status dgr_det_index_add(float *out, int64_t R, int64_t D, int64_
     p.tickets = reinterpret_cast<int32_t *>(w + L.tickets);
     p.tile_tickets = reinterpret_cast<int32_t *>(w + L.tile_tickets);
     p.slots = reinterpret_cast<float *>(w + L.slots);
+    p.bucket_negmin = reinterpret_cast<int32_t *>(w + L.bucket_negmin);
+    p.bucket_max = reinterpret_cast<int32_t *>(w + L.bucket_max);
+    p.bucket_key = reinterpret_cast<int32_t *>(w + L.bucket_key);
+    p.heavy = reinterpret_cast<int2 *>(w + L.heavy);
     count_kernel<<<L.nb, kThreads, 0, s>>>(p);
     scatter_high_kernel<<<L.nb, kThreads, 0, s>>>(p);
     bucket_kernel<<<L.n_buckets, kThreads, 0, s>>>(p);
     if (D > 0) {
-        const int64_t n_split = seg_tile == kSegTile ? static_cast<int64_t>(L.n_pblk) * 4 : 0;
-        const int64_t warps = n_split + R + 1;
+        const int64_t heavy_warps = seg_tile == kSegTile ? static_cast<int64_t>(L.max_heavy) * 4 : 0;
+        const int64_t warps = (R + 1) > heavy_warps ? (R + 1) : heavy_warps;
         const int64_t grid = (warps + kWarps - 1) / kWarps;
         if (grid > INT32_MAX) return DGR_ERR_UNSUPPORTED;
         segsum_kernel<<<static_cast<unsigned>(grid), kThreads, 0, s>>>(p);

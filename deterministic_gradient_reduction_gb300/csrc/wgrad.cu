@@ -15,7 +15,9 @@
 // expert by expert. Warp 0 issues TMA loads (64-token stages, 128-byte
 // swizzle; G and X are MN-major as they lie in memory, so no transpose), warp
 // 1 issues tcgen05.mma into one of two TMEM accumulators (256 columns each),
-// warps 2-9 read the accumulator back, fold the chunks and finish the tile.
+// warps 4-11 read the accumulator back, fold the chunks and finish the tile
+// (the epilogue warpgroups hold the running fold, 128 fp32 per thread, so
+// they take most of the registers; warps 2-3 idle).
 // Rows of a stage past the expert's end are zeroed in shared memory before
 // the MMA reads them (TMA fills rows past the tensor's end with zeros).
 // Every wait is bounded; a timeout records DGR_ERR_TIMEOUT, aborts the CTA,
@@ -38,7 +40,13 @@ constexpr int BK = 64;                  // tokens per pipeline stage
 constexpr int kStages = 4;
 constexpr int kChunk = 512;
 constexpr int kEpiWarps = 8;
-constexpr int kThreadsW = (2 + kEpiWarps) * 32;
+constexpr int kThreadsW = (4 + kEpiWarps) * 32;  // warpgroup 0: TMA, MMA, 2 idle; warpgroups 1-2: epilogue
+// Register split: launched at 168 per thread (3 warps per SM sub-partition),
+// warpgroup 0 gives back to 56 and the epilogue warpgroups take 224:
+// 128 * 56 + 256 * 224 = 384 * 168.
+constexpr int kRegsLow = 56;
+constexpr int kRegsHigh = 224;
+static_assert(128 * kRegsLow + 256 * kRegsHigh <= 384 * 168, "register split exceeds the launch's registers");
 constexpr uint32_t kBoxBytes = 64 * 128;                  // one 64 x 64 bf16 TMA box
 constexpr uint32_t kStageA = 2 * kBoxBytes;               // 128 n x 64 tokens
 constexpr uint32_t kStageB = 4 * kBoxBytes;               // 256 k x 64 tokens
@@ -56,7 +64,11 @@ struct Ctl {
     uint32_t tmem_base;
     int abort;
 };
-constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + sizeof(Ctl);
+// per epilogue warp, a 32 x 33 fp32 tile to turn its rows (one per lane, as
+// TMEM gives them) into columns, so main_grad is read and written in whole
+// 128-byte lines
+constexpr uint32_t kXposeBytes = kEpiWarps * 32 * 33 * 4;
+constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + kXposeBytes + sizeof(Ctl);
 
 struct WgradParams {
     const int64_t *offs;
@@ -86,7 +98,8 @@ __global__ void __launch_bounds__(kThreadsW, 1)
                  const WgradParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Ctl *ctl = reinterpret_cast<Ctl *>(smem + kStages * kStageBytes);
+    float *xpose = reinterpret_cast<float *>(smem + kStages * kStageBytes);
+    Ctl *ctl = reinterpret_cast<Ctl *>(smem + kStages * kStageBytes + kXposeBytes);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     volatile int *abort_flag = &ctl->abort;
@@ -114,6 +127,8 @@ __global__ void __launch_bounds__(kThreadsW, 1)
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
 
+    if (warp < 4) setmaxnreg_dec<kRegsLow>();
+
     if (warp == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
@@ -128,6 +143,11 @@ __global__ void __launch_bounds__(kThreadsW, 1)
                 expert_range(p, e, t_beg, te);
                 for (int32_t c0 = 0; ok && c0 < te; c0 += kChunk) {
                     const int32_t vc = min(kChunk, te - c0);
+                    if (c0 + kChunk >= te) {
+                        // the epilogue will read this tile of main_grad soon: bring it into L2
+                        const float *mg = p.main_grad + (static_cast<int64_t>(e) * p.N + nb * BM) * p.K + kb * BN;
+                        for (int r = 0; r < BM; ++r) prefetch_l2_bulk(mg + static_cast<int64_t>(r) * p.K, BN * 4);
+                    }
                     for (int32_t s0 = 0; s0 < vc; s0 += BK) {
                         if (!mbar_wait(&ctl->empty[stage], phase ^ 1, abort_flag, p.hdr, 10)) {
                             ok = false;
@@ -219,10 +239,11 @@ __global__ void __launch_bounds__(kThreadsW, 1)
                 __syncwarp();
             }
         }
-    } else {
+    } else if (warp >= 4) {
         // ---------------- epilogue: fold chunks, add into main_grad ----------------
+        setmaxnreg_inc<kRegsHigh>();
         const int q = warp & 3;                 // TMEM lane quarter this warp may access
-        const int h = (warp - 2) >> 2;          // column half of the tile
+        const int h = (warp - 4) >> 2;          // column half of the tile
         uint32_t g = 0;
         bool ok = true;
         float F[128];
@@ -258,22 +279,28 @@ __global__ void __launch_bounds__(kThreadsW, 1)
                 if (lane == 0) mbar_arrive(&ctl->tempty[buf]);
             }
             if (!ok) break;
-            const int n = nb * BM + 32 * q + lane;
-            float *mg = p.main_grad + (static_cast<int64_t>(e) * p.N + n) * p.K + kb * BN + 128 * h;
+            // main_grad += dW through the warp's transpose tile: lane i holds row
+            // (32q + i) of the tile; each 32-column slice is written row-wise to
+            // shared memory and read back column-wise, so that lane i then owns
+            // column i of the slice and every load/store covers one 128-byte line
+            float *xt = xpose + (warp - 4) * 32 * 33;
+            const int64_t row0 = static_cast<int64_t>(e) * p.N + nb * BM + 32 * q;
+            float *mg = p.main_grad + row0 * p.K + kb * BN + 128 * h + lane;
 #pragma unroll
-            for (int v0 = 0; v0 < 32; v0 += 8) {
-                float4 m[8];
+            for (int j = 0; j < 4; ++j) {
 #pragma unroll
-                for (int u = 0; u < 8; ++u) m[u] = reinterpret_cast<const float4 *>(mg)[v0 + u];
+                for (int i = 0; i < 32; ++i) xt[lane * 33 + i] = F[32 * j + i];
+                __syncwarp();
+                float m[16];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int f = 4 * (v0 + u);
-                    m[u].x = __fadd_rn(m[u].x, F[f]);
-                    m[u].y = __fadd_rn(m[u].y, F[f + 1]);
-                    m[u].z = __fadd_rn(m[u].z, F[f + 2]);
-                    m[u].w = __fadd_rn(m[u].w, F[f + 3]);
-                    reinterpret_cast<float4 *>(mg)[v0 + u] = m[u];
+                for (int r0 = 0; r0 < 32; r0 += 16) {
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) m[r] = mg[static_cast<int64_t>(r0 + r) * p.K + 32 * j];
+#pragma unroll
+                    for (int r = 0; r < 16; ++r)
+                        mg[static_cast<int64_t>(r0 + r) * p.K + 32 * j] = __fadd_rn(m[r], xt[(r0 + r) * 33 + lane]);
                 }
+                __syncwarp();
             }
         }
     }
