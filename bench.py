@@ -284,7 +284,7 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return
     peaks = load_peaks()
-    traffic = load_traffic()
+    traffic = load_traffic()  # per-launch DRAM bytes of the kernels as they stand (profiles/)
     red_ms = sum(per_ms[n] for n in REDUCTIONS)
     red_bytes = sum(ALGO[n] for n in REDUCTIONS)
     value = world * red_bytes / (red_ms * 1e-3) / 1e9
@@ -298,7 +298,7 @@ def run_ours(args, rank, world, local_rank):
         else:
             gbs = ALGO[n] / (ms * 1e-3) / 1e9
             parts[n] = {"us": round(ms * 1e3, 2), "gbs": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm"], 4),
-                        "launches": LAUNCHES[n]}
+                        "launches": LAUNCHES[n], "dram_traffic": traffic.get(n)}
     dom = max(order, key=lambda n: per_ms[n])
     if dom == "wgrad":
         ach = ALGO["wgrad_flop"] / (per_ms[dom] * 1e-3) / 1e12

@@ -38,7 +38,7 @@ struct ColsumParams {
     int32_t n_tiles;
     int32_t flat;                // tokens are at t * stride_s
     // producer mapping
-    int32_t RG, CB, V, n_pcb;
+    int32_t RG, CB, V, n_pcb, TPC;
     // folder mapping
     int32_t FC, n_fcb, batch;
     float *out;
@@ -86,68 +86,99 @@ __device__ __forceinline__ int64_t token_offset(const ColsumParams &p, int32_t t
     return static_cast<int64_t>(b) * p.stride_b + static_cast<int64_t>(s) * p.stride_s;
 }
 
-// One producer unit: the tile partials of tile j for column vectors
-// [cv0, cv0 + CB). VE = elements per vector (8 bf16 or 4 fp32 for 16-byte
-// loads, 1 for the scalar path); RPT = rows a thread owns.
+// One producer unit: TPC consecutive tiles (a group of RG*CB threads each)
+// for column vectors [cv0, cv0 + CB). VE = elements per vector (8 bf16 or 4
+// fp32 for 16-byte loads, 1 for the scalar path); RPT = rows a thread owns.
+// A thread keeps its RPT rows in flight as raw 16-byte words and widens them
+// pair by pair into the first tree level.
 template <int DT, int VE, int RPT>
 __device__ void produce(const ColsumParams &p, int unit, float *sm) {
     using E = Elem<DT>;
-    const int j = unit / p.n_pcb;
-    const int pcb = unit - j * p.n_pcb;
+    const int tg = unit / p.n_pcb;                 // tile group
+    const int pcb = unit - tg * p.n_pcb;
     const int tid = threadIdx.x;
-    const int g = tid / p.CB;          // row group
-    const int v = tid - g * p.CB;      // column vector within the block
+    const int tpt = p.RG * p.CB;                   // threads per tile
+    const int ts = tid / tpt;                      // tile slot in this CTA
+    const int tt = tid - ts * tpt;
+    const int g = tt / p.CB;                       // row group
+    const int v = tt - g * p.CB;                   // column vector within the block
+    const int j = tg * p.TPC + ts;                 // tile
     const int cv0 = pcb * p.CB;
     const int cb_here = min(p.CB, p.V - cv0);
+    const bool active = ts < p.TPC && j < p.n_tiles && v < cb_here;
     const int64_t t0 = static_cast<int64_t>(j) * p.W;
-    const int count = static_cast<int>(min(static_cast<int64_t>(p.W), p.T - t0));
+    const int count = active ? static_cast<int>(min(static_cast<int64_t>(p.W), p.T - t0)) : 0;
     const int groups_present = (count + RPT - 1) / RPT;
-    const bool active = g < p.RG && v < cb_here;
     const int nrows = active ? max(0, min(RPT, count - g * RPT)) : 0;
+    float *tsm = sm + ts * tpt * VE;
 
-    float leaf[RPT][VE];
     if (nrows > 0) {
         const int c0 = (cv0 + v) * VE;
+        constexpr int RW = VE == 1 ? 1 : 4;        // 32-bit words per vector
+        uint32_t raw[RPT][RW];
 #pragma unroll
         for (int r = 0; r < RPT; ++r) {
             if (r < nrows) {
                 const int32_t t = static_cast<int32_t>(t0) + g * RPT + r;
                 const char *src = p.x + (token_offset(p, t) + c0) * E::kSize;
                 if constexpr (VE == 1) {
-                    leaf[r][0] = E::load1(src);
+                    raw[r][0] = __float_as_uint(E::load1(src));
                 } else {
-                    E::unpack(ldg_nc_v4(src), leaf[r]);
+                    const uint4 q = ldg_nc_v4(src);
+                    raw[r][0] = q.x; raw[r][1] = q.y; raw[r][2] = q.z; raw[r][3] = q.w;
                 }
             }
         }
-        // in-register levels of the tree: aligned windows of 2s rows
+        // level 1 while widening: rows (2i, 2i+1)
+        constexpr int NP = RPT > 1 ? RPT / 2 : 1;
+        float pr[NP][VE];
 #pragma unroll
-        for (int s = 1; s < RPT; s *= 2) {
+        for (int i = 0; i < NP; ++i) {
+            const int r = 2 * i;
+            if (r < nrows) {
+                float a[VE];
+                if constexpr (VE == 1) a[0] = __uint_as_float(raw[r][0]);
+                else E::unpack(make_uint4(raw[r][0], raw[r][1], raw[r][2], raw[r][3]), a);
+                if (RPT > 1 && r + 1 < nrows) {
+                    float b[VE];
+                    if constexpr (VE == 1) b[0] = __uint_as_float(raw[r + 1][0]);
+                    else E::unpack(make_uint4(raw[r + 1][0], raw[r + 1][1], raw[r + 1][2], raw[r + 1][3]), b);
 #pragma unroll
-            for (int r = 0; r + s < RPT; r += 2 * s) {
-                if (r + s < nrows) {
+                    for (int e = 0; e < VE; ++e) a[e] = __fadd_rn(a[e], b[e]);
+                }
 #pragma unroll
-                    for (int e = 0; e < VE; ++e) leaf[r][e] = __fadd_rn(leaf[r][e], leaf[r + s][e]);
+                for (int e = 0; e < VE; ++e) pr[i][e] = a[e];
+            }
+        }
+        // levels 2.. in registers: aligned windows of 2s pairs
+        const int npresent = (nrows + 1) / 2;
+#pragma unroll
+        for (int s = 1; s < NP; s *= 2) {
+#pragma unroll
+            for (int i = 0; i + s < NP; i += 2 * s) {
+                if (i + s < npresent) {
+#pragma unroll
+                    for (int e = 0; e < VE; ++e) pr[i][e] = __fadd_rn(pr[i][e], pr[i + s][e]);
                 }
             }
         }
-        float *dst = sm + (g * p.CB + v) * VE;
+        float *dst = tsm + (g * p.CB + v) * VE;
 #pragma unroll
-        for (int e = 0; e < VE; ++e) dst[e] = leaf[0][e];
+        for (int e = 0; e < VE; ++e) dst[e] = pr[0][e];
     }
     __syncthreads();
     // shared-memory levels: row group g absorbs g + s when both are present
     for (int s = 1; s < p.RG; s *= 2) {
         if (active && (g % (2 * s)) == 0 && g + s < groups_present) {
-            float *a = sm + (g * p.CB + v) * VE;
-            const float *b = sm + ((g + s) * p.CB + v) * VE;
+            float *a = tsm + (g * p.CB + v) * VE;
+            const float *b = tsm + ((g + s) * p.CB + v) * VE;
 #pragma unroll
             for (int e = 0; e < VE; ++e) a[e] = __fadd_rn(a[e], b[e]);
         }
         __syncthreads();
     }
     if (active && g == 0) {
-        const float *root = sm + v * VE;
+        const float *root = tsm + v * VE;
 #pragma unroll
         for (int e = 0; e < VE; ++e) {
             const int c = (cv0 + v) * VE + e;
@@ -159,7 +190,12 @@ __device__ void produce(const ColsumParams &p, int unit, float *sm) {
         __threadfence();
     }
     __syncthreads();
-    if (tid == 0) atomicAdd(&p.counters[j / kGroupTiles], 1);
+    if (tid == 0) {
+        // the CTA's tiles lie in one group of 32 (TPC divides 32)
+        const int first = tg * p.TPC;
+        const int n_here = min(p.TPC, p.n_tiles - first);
+        atomicAdd(&p.counters[first / kGroupTiles], n_here);
+    }
 }
 
 // One folder CTA: columns [f*FC, f*FC + FC), all tiles in ascending order.
@@ -340,11 +376,21 @@ extern "C" dgr_status dgr_ordered_colsum(const void *x, int32_t dtype, int64_t B
     const int VE = vec_ok ? vec : 1;
     p.V = static_cast<int32_t>((H + VE - 1) / VE);
     p.CB = p.V < 32 ? p.V : 32;
-    int rpt = 1;
-    while (rpt < 16 && rpt < tile_rows && (tile_rows / rpt) * p.CB > kThreads) rpt *= 2;
+    // each thread owns up to 16 rows; a tile takes RG * CB threads and a CTA
+    // packs TPC tiles (a power of two dividing the 32-tile counter group)
+    int rpt = tile_rows < 16 ? tile_rows : 16;
     if ((tile_rows / rpt) * p.CB > kThreads) p.CB = kThreads / (tile_rows / rpt);
     p.RG = tile_rows / rpt;
     p.n_pcb = (p.V + p.CB - 1) / p.CB;
+    int tpc = 1;
+    const int64_t units_min = 4LL * 152;  // keep enough CTAs to fill the GPU
+    while (tpc < 32 && 2 * tpc * p.RG * p.CB <= kThreads &&
+           (static_cast<int64_t>(L.n_tiles) + 2 * tpc - 1) / (2 * tpc) * p.n_pcb >= units_min)
+        tpc *= 2;
+    if (L.n_tiles <= 32) {  // tiny inputs: as few CTAs as the threads allow
+        while (tpc < 32 && 2 * tpc * p.RG * p.CB <= kThreads && tpc < L.n_tiles) tpc *= 2;
+    }
+    p.TPC = tpc;
     p.FC = L.FC;
     p.n_fcb = L.n_fcb;
     p.batch = kFolderSmemBytes / (2 * p.FC * 4);
@@ -354,10 +400,11 @@ extern "C" dgr_status dgr_ordered_colsum(const void *x, int32_t dtype, int64_t B
     p.hdr = reinterpret_cast<WsHeader *>(w);
     p.counters = reinterpret_cast<int32_t *>(w + L.counters_off);
     p.slots = reinterpret_cast<float *>(w + L.slots_off);
-    // producer scratch: RG * CB * VE floats must fit the launch's shared memory
-    if (static_cast<size_t>(p.RG) * p.CB * VE * 4 > static_cast<size_t>(kFolderSmemBytes))
+    // producer scratch: TPC * RG * CB * VE floats must fit the launch's shared memory
+    if (static_cast<size_t>(p.TPC) * p.RG * p.CB * VE * 4 > static_cast<size_t>(kFolderSmemBytes))
         return DGR_ERR_UNSUPPORTED;
-    const int64_t grid = static_cast<int64_t>(p.n_fcb) + static_cast<int64_t>(L.n_tiles) * p.n_pcb;
+    const int64_t n_groups_t = (L.n_tiles + p.TPC - 1) / p.TPC;
+    const int64_t grid = static_cast<int64_t>(p.n_fcb) + n_groups_t * p.n_pcb;
     if (grid > INT32_MAX) return DGR_ERR_UNSUPPORTED;
     if (dtype == DGR_DTYPE_BF16) {
         return VE == 8 ? launch_rpt<DGR_DTYPE_BF16, 8>(p, rpt, static_cast<int>(grid), s)
