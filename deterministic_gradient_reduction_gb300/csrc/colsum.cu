@@ -24,6 +24,8 @@ namespace dgr {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kWarpThreads = 512;                 // warp-producer kernel: one CTA per SM
+constexpr int kWarpSmemBytes = 116 * 1024;        // more than half an SM: one CTA per SM
 constexpr int kGroupTiles = 32;                 // tiles per ready counter
 constexpr int kFolderSmemBytes = 32 * 1024;     // double-buffered slot batches (<= 1024 tiles each)
 constexpr int kMaxFolders = 64;
@@ -39,11 +41,14 @@ struct ColsumParams {
     int32_t flat;                // tokens are at t * stride_s
     // producer mapping
     int32_t RG, CB, V, n_pcb, TPC;
+    // 1: warp producers (one warp per tile)
+    int32_t stream_mode;
     // folder mapping
     int32_t FC, n_fcb, batch;
     float *out;
     int32_t accumulate;
-    float *slots;                // [n_fcb][n_tiles][FC]
+    float *slots;                // [H][col_stride] (tile fastest)
+    int64_t col_stride;
     int32_t *counters;           // [n_groups]
     WsHeader *hdr;
 };
@@ -78,6 +83,13 @@ struct Elem<DGR_DTYPE_F32> {
         f[3] = __uint_as_float(v.w);
     }
 };
+
+// Slots are column-major inside each folder block: column c of tile j is at
+// c * col_stride + j (col_stride = n_tiles rounded up to 4), so a folder reads
+// four consecutive tiles of its column with one 16-byte load.
+__device__ __forceinline__ int64_t slot_index(const ColsumParams &p, int c, int j) {
+    return static_cast<int64_t>(c) * p.col_stride + j;
+}
 
 __device__ __forceinline__ int64_t token_offset(const ColsumParams &p, int32_t t) {
     if (p.flat) return static_cast<int64_t>(t) * p.stride_s;
@@ -183,8 +195,7 @@ __device__ void produce(const ColsumParams &p, int unit, float *sm) {
         for (int e = 0; e < VE; ++e) {
             const int c = (cv0 + v) * VE + e;
             if (c < p.H) {
-                const int f = c / p.FC;
-                p.slots[(static_cast<int64_t>(f) * p.n_tiles + j) * p.FC + (c - f * p.FC)] = root[e];
+                p.slots[slot_index(p, c, j)] = root[e];
             }
         }
         __threadfence();
@@ -198,16 +209,140 @@ __device__ void produce(const ColsumParams &p, int unit, float *sm) {
     }
 }
 
+// Warp producers (vector loads, V column vectors with V dividing 32): one warp
+// per tile. Lane = (row group, vector): RGW = 32 / V row groups of RPL = W /
+// RGW consecutive rows each. A lane sums its rows by the tree's first levels
+// in registers (batches of up to 16 raw 16-byte words in flight, a binary
+// counter over the batches), and the remaining levels are xor-shuffles
+// between row groups at lane distance V, 2V, ... - aligned windows, so the
+// tree is exactly the canonical one, with no shared memory and no block
+// barrier. Lanes of row group 0 then hold the tile partial.
+template <int DT, int VE, int RPL>
+__device__ __forceinline__ void produce_warp_tile(const ColsumParams &p, int64_t wunit) {
+    using E = Elem<DT>;
+    constexpr int BATCH = RPL < 8 ? RPL : 8;
+    constexpr int NB = RPL / BATCH;  // batches, a power of two <= 16
+    constexpr int LV = NB >= 16 ? 4 : NB >= 8 ? 3 : NB >= 4 ? 2 : NB >= 2 ? 1 : 0;
+    const int lane = threadIdx.x & 31;
+    if (wunit >= p.n_tiles) return;
+    const int j = static_cast<int>(wunit);
+    const int V = p.V;
+    const int g = lane / V;
+    const int v = lane - g * V;
+    const int64_t t0 = static_cast<int64_t>(j) * p.W;
+    const int count = static_cast<int>(min(static_cast<int64_t>(p.W), p.T - t0));
+    const int nrows = max(0, min(RPL, count - g * RPL));
+    const int c0 = v * VE;
+    float stack[LV + 1][VE];
+    float acc[VE];
+#pragma unroll
+    for (int bi = 0; bi < NB; ++bi) {
+        const int rb = bi * BATCH;  // first row of the batch within the lane's rows
+        uint4 raw[BATCH];
+#pragma unroll
+        for (int r = 0; r < BATCH; ++r) {
+            if (rb + r < nrows) {
+                const int32_t t = static_cast<int32_t>(t0) + g * RPL + rb + r;
+                raw[r] = ldg_nc_v4(p.x + (token_offset(p, t) + c0) * E::kSize);
+            }
+        }
+        // the batch's subtree (rows rb .. rb+BATCH-1), absent rows skipped;
+        // level 1 is taken while widening, pair by pair
+        const int nb_rows = max(0, min(BATCH, nrows - rb));
+        constexpr int NP = BATCH > 1 ? BATCH / 2 : 1;
+        float lv[NP][VE];
+#pragma unroll
+        for (int i = 0; i < NP; ++i) {
+            const int r = 2 * i;
+            if (r < nb_rows) {
+                E::unpack(raw[r], lv[i]);
+                if (BATCH > 1 && r + 1 < nb_rows) {
+                    float b2[VE];
+                    E::unpack(raw[r + 1], b2);
+#pragma unroll
+                    for (int e = 0; e < VE; ++e) lv[i][e] = __fadd_rn(lv[i][e], b2[e]);
+                }
+            }
+        }
+        const int np_present = (nb_rows + 1) / 2;
+#pragma unroll
+        for (int sft = 1; sft < NP; sft *= 2) {
+#pragma unroll
+            for (int i = 0; i + sft < NP; i += 2 * sft)
+                if (i + sft < np_present) {
+#pragma unroll
+                    for (int e = 0; e < VE; ++e) lv[i][e] = __fadd_rn(lv[i][e], lv[i + sft][e]);
+                }
+        }
+        // push batch bi (a compile-time index) onto the binary-counter stack
+        if (nb_rows > 0) {
+#pragma unroll
+            for (int e = 0; e < VE; ++e) acc[e] = lv[0][e];
+            int lvl = 0;
+#pragma unroll
+            for (int l = 0; l < LV; ++l) {
+                if (((bi >> l) & 1) == 0) break;
+#pragma unroll
+                for (int e = 0; e < VE; ++e) acc[e] = __fadd_rn(stack[l][e], acc[e]);
+                lvl = l + 1;
+            }
+#pragma unroll
+            for (int l = 0; l <= LV; ++l)
+                if (l == lvl) {
+#pragma unroll
+                    for (int e = 0; e < VE; ++e) stack[l][e] = acc[e];
+                }
+        }
+    }
+    // ragged end: complete blocks of the set bits of the present batch count,
+    // smallest first, each larger (earlier) block on the left
+    const int nbp = (nrows + BATCH - 1) / BATCH;
+    bool have = false;
+#pragma unroll
+    for (int l = 0; l <= LV; ++l) {
+        if ((nbp >> l) & 1) {
+#pragma unroll
+            for (int e = 0; e < VE; ++e) acc[e] = have ? __fadd_rn(stack[l][e], acc[e]) : stack[l][e];
+            have = true;
+        }
+    }
+    // cross-lane levels: row group g absorbs g + s (lane distance s * V)
+    bool present = nrows > 0;
+    for (int s = 1; s * V < 32; s *= 2) {
+        const bool left_is_me = (g & s) == 0;
+        const bool o_present = __shfl_xor_sync(0xffffffffu, present ? 1 : 0, s * V) != 0;
+        const bool left_present = left_is_me ? present : o_present;
+        const bool right_present = left_is_me ? o_present : present;
+#pragma unroll
+        for (int e = 0; e < VE; ++e) {
+            const float o = __shfl_xor_sync(0xffffffffu, acc[e], s * V);
+            if (left_present && right_present) acc[e] = __fadd_rn(acc[e], o);
+            else if (!left_is_me && left_present) acc[e] = o;
+        }
+        present = left_present;
+    }
+    if (g == 0) {
+#pragma unroll
+        for (int e = 0; e < VE; ++e) {
+            p.slots[slot_index(p, c0 + e, j)] = acc[e];
+        }
+        __threadfence();
+    }
+    __syncwarp();
+    if (lane == 0) atomicAdd(&p.counters[j / kGroupTiles], 1);
+}
+
 // One folder CTA: columns [f*FC, f*FC + FC), all tiles in ascending order.
+// Shared memory holds two batches, column-major: buf[cc * batch + k].
 __device__ void fold(const ColsumParams &p, int f, float *sm) {
     __shared__ int abort_flag;
     __shared__ int ticket;
     const int tid = threadIdx.x;
     const int chain_threads = ((p.FC + 31) / 32) * 32;
-    const int loader_threads = kThreads - chain_threads;
+    const int nthreads = blockDim.x;
+    const int loader_threads = nthreads - chain_threads;
     const int ltid = tid - chain_threads;  // loader index (>= 0 for loaders)
     const int n_batches = (p.n_tiles + p.batch - 1) / p.batch;
-    const float *src = p.slots + static_cast<int64_t>(f) * p.n_tiles * p.FC;
     const int col = f * p.FC + tid;
     if (tid == 0) abort_flag = 0;
     __syncthreads();
@@ -232,10 +367,15 @@ __device__ void fold(const ColsumParams &p, int f, float *sm) {
         }
         asm volatile("bar.sync 1, %0;" ::"r"(loader_threads) : "memory");
         if (abort_flag) return;
-        const int n4 = (j1 - j0) * p.FC / 4;
-        const float4 *s4 = reinterpret_cast<const float4 *>(src + static_cast<int64_t>(j0) * p.FC);
+        const int q4 = (j1 - j0 + 3) / 4;  // float4 per column (the column stride is padded to 4)
+        const int n4 = q4 * p.FC;
         float4 *d4 = reinterpret_cast<float4 *>(sm + (i & 1) * p.batch * p.FC);
-        for (int q = ltid; q < n4; q += loader_threads) d4[q] = __ldcg(s4 + q);
+        for (int q = ltid; q < n4; q += loader_threads) {
+            const int cc = q / q4;
+            const int k4 = q - cc * q4;
+            const float4 *s4 = reinterpret_cast<const float4 *>(p.slots + slot_index(p, f * p.FC + cc, j0));
+            d4[cc * (p.batch / 4) + k4] = __ldcg(s4 + k4);
+        }
     };
 
     if (ltid >= 0) load(0);
@@ -246,15 +386,50 @@ __device__ void fold(const ColsumParams &p, int f, float *sm) {
         if (ltid >= 0) {
             if (i + 1 < n_batches) load(i + 1);
         } else if (tid < p.FC && col < p.H) {
-            const float *b = sm + (i & 1) * p.batch * p.FC + tid;
+            const float4 *b4 = reinterpret_cast<const float4 *>(sm + (i & 1) * p.batch * p.FC + tid * p.batch);
             const int cnt = min(p.batch, p.n_tiles - i * p.batch);
             int k = 0;
-            if (i == 0) {
-                F = b[0];
-                k = 1;
+            if (i == 0) {  // the fold starts from tile 0's partial
+                const float4 q = b4[0];
+                F = q.x;
+                if (cnt > 1) F = __fadd_rn(F, q.y);
+                if (cnt > 2) F = __fadd_rn(F, q.z);
+                if (cnt > 3) F = __fadd_rn(F, q.w);
+                k = 4;
             }
-#pragma unroll 16
-            for (; k < cnt; ++k) F = __fadd_rn(F, b[k * p.FC]);
+            // blocks of 16 tiles: the next block's four 16-byte loads are issued
+            // before the current block's 16 dependent adds (the last block
+            // reloads itself instead of reading past the batch)
+            const int kfull = cnt > k ? k + ((cnt - k) / 16) * 16 : k;
+            if (k < kfull) {
+                float4 r0 = b4[(k >> 2)], r1 = b4[(k >> 2) + 1], r2 = b4[(k >> 2) + 2], r3 = b4[(k >> 2) + 3];
+                for (; k < kfull; k += 16) {
+                    const int nk = (k + 16 < kfull) ? k + 16 : k;
+                    const float4 s0 = b4[(nk >> 2)], s1 = b4[(nk >> 2) + 1], s2 = b4[(nk >> 2) + 2],
+                                 s3 = b4[(nk >> 2) + 3];
+                    F = __fadd_rn(F, r0.x); F = __fadd_rn(F, r0.y); F = __fadd_rn(F, r0.z); F = __fadd_rn(F, r0.w);
+                    F = __fadd_rn(F, r1.x); F = __fadd_rn(F, r1.y); F = __fadd_rn(F, r1.z); F = __fadd_rn(F, r1.w);
+                    F = __fadd_rn(F, r2.x); F = __fadd_rn(F, r2.y); F = __fadd_rn(F, r2.z); F = __fadd_rn(F, r2.w);
+                    F = __fadd_rn(F, r3.x); F = __fadd_rn(F, r3.y); F = __fadd_rn(F, r3.z); F = __fadd_rn(F, r3.w);
+                    r0 = s0;
+                    r1 = s1;
+                    r2 = s2;
+                    r3 = s3;
+                }
+            }
+            for (; k + 4 <= cnt; k += 4) {
+                const float4 q = b4[k >> 2];
+                F = __fadd_rn(F, q.x);
+                F = __fadd_rn(F, q.y);
+                F = __fadd_rn(F, q.z);
+                F = __fadd_rn(F, q.w);
+            }
+            if (k < cnt) {
+                const float4 q = b4[k >> 2];
+                F = __fadd_rn(F, q.x);
+                if (k + 1 < cnt) F = __fadd_rn(F, q.y);
+                if (k + 2 < cnt) F = __fadd_rn(F, q.z);
+            }
         }
         __syncthreads();
     }
@@ -271,14 +446,14 @@ __device__ void fold(const ColsumParams &p, int f, float *sm) {
     __syncthreads();
     if (ticket == p.n_fcb - 1) {
         const int n_groups = (p.n_tiles + kGroupTiles - 1) / kGroupTiles;
-        for (int q = tid; q < n_groups; q += kThreads) p.counters[q] = 0;
+        for (int q = tid; q < n_groups; q += nthreads) p.counters[q] = 0;
         if (tid == 0) p.hdr->pad[0] = 0;
     }
 }
 
 template <int DT, int VE, int RPT>
 __global__ void __launch_bounds__(kThreads) colsum_kernel(const ColsumParams p) {
-    extern __shared__ __align__(16) float smem[];
+    extern __shared__ __align__(128) float smem[];
     if (static_cast<int>(blockIdx.x) < p.n_fcb) {
         fold(p, blockIdx.x, smem);
     } else {
@@ -286,21 +461,69 @@ __global__ void __launch_bounds__(kThreads) colsum_kernel(const ColsumParams p) 
     }
 }
 
+// The same with warp producers. One 512-thread CTA per SM (the launch asks
+// for more than half an SM's shared memory), so a folder has its SM to
+// itself: its chain of dependent adds then issues at the add latency instead
+// of competing with producer warps for issue slots. Producer CTAs are
+// persistent; warp w of all producer warps takes tiles w, w + n, w + 2n, ...
+template <int DT, int VE, int RPL>
+__global__ void __launch_bounds__(kWarpThreads, 1) colsum_warp_kernel(const ColsumParams p) {
+    extern __shared__ __align__(128) float smem[];
+    if (static_cast<int>(blockIdx.x) < p.n_fcb) {
+        fold(p, blockIdx.x, smem);
+    } else {
+        const int64_t wpc = kWarpThreads / 32;
+        const int64_t n_warps = static_cast<int64_t>(gridDim.x - p.n_fcb) * wpc;
+        for (int64_t w = static_cast<int64_t>(blockIdx.x - p.n_fcb) * wpc + (threadIdx.x >> 5); w < p.n_tiles;
+             w += n_warps)
+            produce_warp_tile<DT, VE, RPL>(p, w);
+    }
+}
+
+template <int DT, int VE, int RPT>
+dgr_status launch_one(const ColsumParams &p, int grid, size_t smem, cudaStream_t st) {
+    colsum_kernel<DT, VE, RPT><<<grid, kThreads, smem, st>>>(p);
+    return launch_status();
+}
+
 template <int DT, int VE>
-dgr_status launch_rpt(const ColsumParams &p, int rpt, int grid, cudaStream_t st) {
+dgr_status launch_rpt(const ColsumParams &p, int rpt, int grid, size_t smem, cudaStream_t st) {
     switch (rpt) {
-        case 1: colsum_kernel<DT, VE, 1><<<grid, kThreads, kFolderSmemBytes, st>>>(p); break;
-        case 2: colsum_kernel<DT, VE, 2><<<grid, kThreads, kFolderSmemBytes, st>>>(p); break;
-        case 4: colsum_kernel<DT, VE, 4><<<grid, kThreads, kFolderSmemBytes, st>>>(p); break;
-        case 8: colsum_kernel<DT, VE, 8><<<grid, kThreads, kFolderSmemBytes, st>>>(p); break;
-        case 16: colsum_kernel<DT, VE, 16><<<grid, kThreads, kFolderSmemBytes, st>>>(p); break;
+        case 1: return launch_one<DT, VE, 1>(p, grid, smem, st);
+        case 2: return launch_one<DT, VE, 2>(p, grid, smem, st);
+        case 4: return launch_one<DT, VE, 4>(p, grid, smem, st);
+        case 8: return launch_one<DT, VE, 8>(p, grid, smem, st);
+        case 16: return launch_one<DT, VE, 16>(p, grid, smem, st);
         default: return DGR_ERR_INVALID_ARG;
     }
+}
+
+template <int DT, int VE, int RPL>
+dgr_status launch_warp_one(const ColsumParams &p, int grid, cudaStream_t st) {
+    if (cudaFuncSetAttribute(colsum_warp_kernel<DT, VE, RPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kWarpSmemBytes) != cudaSuccess)
+        return DGR_ERR_CUDA;
+    colsum_warp_kernel<DT, VE, RPL><<<grid, kWarpThreads, kWarpSmemBytes, st>>>(p);
     return launch_status();
+}
+
+template <int DT, int VE>
+dgr_status launch_warp(const ColsumParams &p, int rpl, int grid, cudaStream_t st) {
+    switch (rpl) {
+        case 2: return launch_warp_one<DT, VE, 2>(p, grid, st);
+        case 4: return launch_warp_one<DT, VE, 4>(p, grid, st);
+        case 8: return launch_warp_one<DT, VE, 8>(p, grid, st);
+        case 16: return launch_warp_one<DT, VE, 16>(p, grid, st);
+        case 32: return launch_warp_one<DT, VE, 32>(p, grid, st);
+        case 64: return launch_warp_one<DT, VE, 64>(p, grid, st);
+        case 128: return launch_warp_one<DT, VE, 128>(p, grid, st);
+        default: return DGR_ERR_INVALID_ARG;
+    }
 }
 
 struct Layout {
     int32_t n_tiles, n_groups, FC, n_fcb;
+    int64_t col_stride;
     size_t counters_off, slots_off, total;
 };
 
@@ -315,7 +538,8 @@ Layout colsum_layout(int64_t T, int64_t H, int32_t W) {
     L.n_fcb = static_cast<int32_t>((H + L.FC - 1) / L.FC);
     L.counters_off = sizeof(WsHeader);
     L.slots_off = L.counters_off + align_up(static_cast<size_t>(L.n_groups) * 4);
-    L.total = L.slots_off + align_up(static_cast<size_t>(L.n_fcb) * L.n_tiles * L.FC * 4);
+    L.col_stride = (static_cast<int64_t>(L.n_tiles) + 3) / 4 * 4;
+    L.total = L.slots_off + align_up(static_cast<size_t>(L.n_fcb) * L.FC * L.col_stride * 4);
     return L;
 }
 
@@ -391,27 +615,52 @@ extern "C" dgr_status dgr_ordered_colsum(const void *x, int32_t dtype, int64_t B
         while (tpc < 32 && 2 * tpc * p.RG * p.CB <= kThreads && tpc < L.n_tiles) tpc *= 2;
     }
     p.TPC = tpc;
+    // Warp producers when a power-of-two number of 16-byte column vectors
+    // (at most 32) tiles a warp and each lane gets 2 .. 128 rows.
+    size_t smem_bytes = kFolderSmemBytes;
+    p.stream_mode = 0;
+    int rpl = 0;
+    if (vec_ok && p.V <= 32 && (p.V & (p.V - 1)) == 0) {
+        rpl = static_cast<int>(static_cast<int64_t>(tile_rows) * p.V / 32);
+        if (rpl >= 2 && rpl <= 128) p.stream_mode = 1;
+    }
     p.FC = L.FC;
     p.n_fcb = L.n_fcb;
-    p.batch = kFolderSmemBytes / (2 * p.FC * 4);
+    p.batch = (kFolderSmemBytes / (2 * p.FC * 4)) & ~3;  // a multiple of 4: the chain reads 16-byte groups
     p.out = out;
     p.accumulate = accumulate ? 1 : 0;
     char *w = static_cast<char *>(ws);
     p.hdr = reinterpret_cast<WsHeader *>(w);
     p.counters = reinterpret_cast<int32_t *>(w + L.counters_off);
     p.slots = reinterpret_cast<float *>(w + L.slots_off);
+    p.col_stride = L.col_stride;
     // producer scratch: TPC * RG * CB * VE floats must fit the launch's shared memory
     if (static_cast<size_t>(p.TPC) * p.RG * p.CB * VE * 4 > static_cast<size_t>(kFolderSmemBytes))
         return DGR_ERR_UNSUPPORTED;
     const int64_t n_groups_t = (L.n_tiles + p.TPC - 1) / p.TPC;
-    const int64_t grid = static_cast<int64_t>(p.n_fcb) + n_groups_t * p.n_pcb;
-    if (grid > INT32_MAX) return DGR_ERR_UNSUPPORTED;
-    if (dtype == DGR_DTYPE_BF16) {
-        return VE == 8 ? launch_rpt<DGR_DTYPE_BF16, 8>(p, rpt, static_cast<int>(grid), s)
-                       : launch_rpt<DGR_DTYPE_BF16, 1>(p, rpt, static_cast<int>(grid), s);
+    int64_t n_prod_ctas = n_groups_t * p.n_pcb;
+    if (p.stream_mode) {  // persistent: one producer CTA per SM not taken by a folder
+        int dev = 0, sms = 0;
+        cudaGetDevice(&dev);
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DGR_ERR_CUDA;
+        const int64_t need = (L.n_tiles + kWarpThreads / 32 - 1) / (kWarpThreads / 32);
+        int64_t avail = static_cast<int64_t>(sms) - p.n_fcb;
+        if (avail < 1) avail = 1;
+        n_prod_ctas = need < avail ? need : avail;
     }
-    return VE == 4 ? launch_rpt<DGR_DTYPE_F32, 4>(p, rpt, static_cast<int>(grid), s)
-                   : launch_rpt<DGR_DTYPE_F32, 1>(p, rpt, static_cast<int>(grid), s);
+    const int64_t grid = static_cast<int64_t>(p.n_fcb) + n_prod_ctas;
+    if (grid > INT32_MAX) return DGR_ERR_UNSUPPORTED;
+    if (p.stream_mode) {
+        p.n_pcb = 1;
+        if (dtype == DGR_DTYPE_BF16) return launch_warp<DGR_DTYPE_BF16, 8>(p, rpl, static_cast<int>(grid), s);
+        return launch_warp<DGR_DTYPE_F32, 4>(p, rpl, static_cast<int>(grid), s);
+    }
+    if (dtype == DGR_DTYPE_BF16) {
+        return VE == 8 ? launch_rpt<DGR_DTYPE_BF16, 8>(p, rpt, static_cast<int>(grid), smem_bytes, s)
+                       : launch_rpt<DGR_DTYPE_BF16, 1>(p, rpt, static_cast<int>(grid), smem_bytes, s);
+    }
+    return VE == 4 ? launch_rpt<DGR_DTYPE_F32, 4>(p, rpt, static_cast<int>(grid), smem_bytes, s)
+                   : launch_rpt<DGR_DTYPE_F32, 1>(p, rpt, static_cast<int>(grid), smem_bytes, s);
 }
 
 // ---------------------------------------------------------------------------

@@ -54,6 +54,12 @@ CASES = [
     (1, 1, 8, None, torch.bfloat16, 128),
     (1, 70000, 520, None, torch.bfloat16, 128),  # several column blocks and folders
     (1, 3000, 4096, None, torch.bfloat16, 128),  # the H limit
+    # contiguous rows and many tiles: the bulk-copy producers
+    (1, 100000, 64, None, torch.bfloat16, 128),  # ragged last tile
+    (3, 40000, 16, None, torch.bfloat16, 128),
+    (1, 50000, 32, None, torch.float32, 128),
+    (1, 60000, 64, None, torch.bfloat16, 64),
+    (1, 20001, 8, None, torch.bfloat16, 16),
 ]
 
 
