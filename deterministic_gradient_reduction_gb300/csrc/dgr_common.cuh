@@ -63,6 +63,45 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void *p) {
     return r;
 }
 
+// Predicated loads: the destination keeps its value when pred is false. The
+// predicate lives inside the asm with the destination as an in-out operand,
+// so nothing has to merge the old and the new value (a merge would wait for
+// the load to land and serialise loads meant to be in flight together).
+__device__ __forceinline__ void ldg_nc_v4f_if(float4 &v, const void *ptr, bool pred) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+        "@q ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];\n\t}"
+        : "+f"(v.x), "+f"(v.y), "+f"(v.z), "+f"(v.w)
+        : "l"(ptr), "r"(static_cast<int>(pred)));
+}
+
+// Same, L2 only (.cg): data written earlier in this launch by other blocks.
+__device__ __forceinline__ void ldcg_v4f_if(float4 &v, const void *ptr, bool pred) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+        "@q ld.global.cg.v4.f32 {%0,%1,%2,%3}, [%4];\n\t}"
+        : "+f"(v.x), "+f"(v.y), "+f"(v.z), "+f"(v.w)
+        : "l"(ptr), "r"(static_cast<int>(pred)));
+}
+
+// Same, plain weak load (data this thread may also write).
+__device__ __forceinline__ void ld_v4f_if(float4 &v, const void *ptr, bool pred) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+        "@q ld.global.v4.f32 {%0,%1,%2,%3}, [%4];\n\t}"
+        : "+f"(v.x), "+f"(v.y), "+f"(v.z), "+f"(v.w)
+        : "l"(ptr), "r"(static_cast<int>(pred)));
+}
+
+// 32-bit read-only load under a predicate.
+__device__ __forceinline__ void ldg_nc_b32_if(int32_t &v, const int32_t *ptr, bool pred) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
+        "@q ld.global.nc.b32 %0, [%1];\n\t}"
+        : "+r"(v)
+        : "l"(ptr), "r"(static_cast<int>(pred)));
+}
+
 // Host side -------------------------------------------------------------------
 
 inline bool ranges_overlap(const void *a, size_t na, const void *b, size_t nb) {

@@ -38,9 +38,11 @@ constexpr int kItems = 32;
 constexpr int kBlockElems = kThreads * kItems;  // 8192 elements per sort block
 constexpr int kDigits = 256;
 constexpr int kSegTile = 128;
-constexpr int kWarpMaxTiles = 8;                // rows up to 1024 members: one warp
-constexpr int kSub = 32;                         // split-row work unit (a quarter tile)
-constexpr int kStackLevels = 5;                  // group stack depth for 16 groups of 8
+constexpr int kSplitMin = kSegTile;             // rows longer than one tile are split into quarters
+constexpr int kWarpFoldTiles = 32;               // split rows up to 32 tiles: folded by one warp
+constexpr int kMaxFoldBlocks = 16;               // longer rows: folded by up to 16 fold blocks
+constexpr int32_t kSplitBit = 1 << 30;           // sorted key flag: the key's row is split
+constexpr int32_t kKeyMask = kSplitBit - 1;
 
 struct IdxParams {
     const int32_t *idx;
@@ -54,9 +56,9 @@ struct IdxParams {
     float *out;
     int64_t ld_out;
     int32_t *bad_count;
-    int32_t *keys_a, *vals_a, *perm, *skey, *hist, *offs, *bucket_start, *seg_start, *tickets, *tile_tickets;
+    int32_t *keys_a, *vals_a, *perm, *skey, *hist, *offs, *bucket_start, *seg_start, *tickets;
     int32_t *bucket_negmin, *bucket_max, *bucket_key;
-    int2 *heavy;  // (row, tile) of every tile of a row with more than 8 tiles
+    int32_t *heavy_rows;  // split rows longer than kWarpFoldTiles tiles (fold-block work)
     float *slots;
     WsHeader *hdr;
 };
@@ -89,7 +91,7 @@ __global__ void __launch_bounds__(kThreads) count_kernel(const IdxParams p) {
     mn[tid] = INT32_MAX;
     mx[tid] = -1;
     if (tid == 0) bad_block = 0;
-    if (b == 0 && tid == 0) p.hdr->pad[3] = 0;  // heavy-tile list of this call starts empty
+    if (b == 0 && tid == 0) p.hdr->pad[3] = 0;  // fold-row list of this call starts empty
     __syncthreads();
     int32_t v[kItems];
 #pragma unroll
@@ -201,7 +203,12 @@ __global__ void __launch_bounds__(kThreads) scatter_high_kernel(const IdxParams 
     const int b = blockIdx.x;
     for (int q = tid; q < kWarps * kDigits; q += kThreads) (&cnt[0][0])[q] = 0;
     boff[tid] = p.offs[static_cast<int64_t>(b) * kDigits + tid];
-    bkey[tid] = p.bucket_key[tid];
+    {
+        int32_t bk = p.bucket_key[tid];
+        if (bk >= 0 && p.seg_tile == kSegTile && p.bucket_start[tid + 1] - p.bucket_start[tid] > kSplitMin)
+            bk |= kSplitBit;
+        bkey[tid] = bk;
+    }
     __syncthreads();
     const int64_t e0 = static_cast<int64_t>(b) * kBlockElems + w * (kItems * 32) + lane;
     int32_t key[kItems];
@@ -231,7 +238,7 @@ __global__ void __launch_bounds__(kThreads) scatter_high_kernel(const IdxParams 
         const int32_t e = static_cast<int32_t>(e0 + r * 32);
         if (bkey[d] >= 0) {
             p.perm[pos] = e;
-            p.skey[pos] = key[r];
+            p.skey[pos] = bkey[d];
         } else {
             p.keys_a[pos] = key[r];
             p.vals_a[pos] = e;
@@ -239,12 +246,11 @@ __global__ void __launch_bounds__(kThreads) scatter_high_kernel(const IdxParams 
     }
 }
 
-// Heavy rows (more than kWarpMaxTiles tiles) get one list entry per tile.
-__device__ __forceinline__ void list_heavy_tiles(const IdxParams &p, int32_t key, int32_t n) {
-    if (n <= kWarpMaxTiles * kSegTile) return;
-    const int32_t n_tiles = (n + kSegTile - 1) / kSegTile;
-    const int32_t at = atomicAdd(&p.hdr->pad[3], n_tiles);
-    for (int32_t t = 0; t < n_tiles; ++t) p.heavy[at + t] = make_int2(key, t);
+// Split rows longer than kWarpFoldTiles tiles go on the fold blocks' list
+// (its order is immaterial: each row is folded by one block, the same way).
+__device__ __forceinline__ void list_fold_row(const IdxParams &p, int32_t key, int32_t n) {
+    if (n <= kWarpFoldTiles * kSegTile) return;
+    p.heavy_rows[atomicAdd(&p.hdr->pad[3], 1)] = key;
 }
 
 // ---------------------------------------------------------------------------
@@ -264,7 +270,7 @@ __global__ void __launch_bounds__(kThreads) bucket_kernel(const IdxParams p) {
     if (one_key >= 0) {  // K2 already placed it; only the segment starts remain
         if (k <= p.R) p.seg_start[k] = k <= one_key ? bs : be;
         if (k == p.R) p.seg_start[p.R + 1] = p.N;
-        if (tid == 0 && p.seg_tile == kSegTile) list_heavy_tiles(p, one_key, be - bs);
+        if (tid == 0 && p.seg_tile == kSegTile) list_fold_row(p, one_key, be - bs);
         return;
     }
     h[tid] = 0;
@@ -291,7 +297,7 @@ __global__ void __launch_bounds__(kThreads) bucket_kernel(const IdxParams p) {
     __syncthreads();
     if (k <= p.R) p.seg_start[k] = base[tid];
     if (k == p.R) p.seg_start[p.R + 1] = p.N;
-    if (k <= p.R && p.seg_tile == kSegTile) list_heavy_tiles(p, k, h[tid]);
+    if (k <= p.R && p.seg_tile == kSegTile) list_fold_row(p, k, h[tid]);
     for (int32_t c0 = bs; c0 < be; c0 += kBlockElems) {
         for (int q = tid; q < kWarps * kDigits; q += kThreads) (&cnt[0][0])[q] = 0;
         __syncthreads();
@@ -320,7 +326,7 @@ __global__ void __launch_bounds__(kThreads) bucket_kernel(const IdxParams p) {
             const int lo = key[r] & 255;
             const int32_t pos = base[lo] + pre[w][lo] + rank[r];
             p.perm[pos] = val[r];
-            p.skey[pos] = key[r];
+            p.skey[pos] = (p.seg_tile == kSegTile && h[lo] > kSplitMin) ? (key[r] | kSplitBit) : key[r];
         }
         __syncthreads();
         {
@@ -340,139 +346,23 @@ __device__ __forceinline__ float4 f4add(float4 a, float4 b) {
     return make_float4(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y), __fadd_rn(a.z, b.z), __fadd_rn(a.w, b.w));
 }
 
-__device__ __forceinline__ float4 ld_src4(const IdxParams &p, int32_t row, int col) {
-    const uint4 u = ldg_nc_v4(p.src + static_cast<int64_t>(row) * p.ld_src + col);
-    return make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w));
-}
-
-// Pairwise tree over the members [q0, q0 + cnt) of a window of 8..128
-// members (cnt <= 128), in sorted-position order (= original order within a
-// row). The window's width does not matter: leaves past cnt are absent, and
-// an absent right half passes its left half up unchanged. Each lane sums its 4 columns starting at `col` (col < 0: the
-// lane only joins the shuffles). Groups of 8 members are summed in registers;
-// a binary-counter stack over groups (in this warp's shared-memory rows `stk`)
-// gives the higher levels; absent members (past cnt) are skipped, which is the
-// canonical tail rule.
-__device__ __forceinline__ float4 window_sum(const IdxParams &p, int32_t q0, int cnt, int col, int lane,
-                                          float4 (*stk)[32]) {
-    constexpr int kM = kSegTile / 32;
-    int32_t pidx[kM];
-#pragma unroll
-    for (int m = 0; m < kM; ++m) {
-        const int j = m * 32 + lane;
-        pidx[m] = (j < cnt) ? p.perm[q0 + j] : 0;
-    }
-    const int n_groups = (cnt + 7) / 8;
-#pragma unroll 1
-    for (int gi = 0; gi < n_groups; ++gi) {
-        int32_t mine = pidx[0];
-#pragma unroll
-        for (int m = 1; m < kM; ++m)
-            if ((gi >> 2) == m) mine = pidx[m];
-        float4 v[8];
-        const int nu = min(8, cnt - gi * 8);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int32_t row = __shfl_sync(0xffffffffu, mine, (gi & 3) * 8 + u);
-            if (u < nu && col >= 0) v[u] = ld_src4(p, row, col);
-        }
-#pragma unroll
-        for (int s = 1; s < 8; s *= 2) {
-#pragma unroll
-            for (int r = 0; r + s < 8; r += 2 * s)
-                if (r + s < nu) v[r] = f4add(v[r], v[r + s]);
-        }
-        // push group gi: carry through the levels where gi has a one bit
-        float4 cur = v[0];
-        int l = 0;
-        while ((gi >> l) & 1) {
-            cur = f4add(stk[l][lane], cur);
-            ++l;
-        }
-        stk[l][lane] = cur;
-    }
-    // ragged end: combine the complete blocks of the set bits of n_groups,
-    // smallest first, each larger (earlier) block on the left
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    bool have = false;
-    for (int l = 0; (n_groups >> l) != 0; ++l) {
-        if ((n_groups >> l) & 1) {
-            acc = have ? f4add(stk[l][lane], acc) : stk[l][lane];
-            have = true;
-        }
-    }
-    return acc;
-}
-
 __device__ __forceinline__ void add_out(const IdxParams &p, int32_t r, int col, float4 F) {
     float4 *o = reinterpret_cast<float4 *>(p.out + static_cast<int64_t>(r) * p.ld_out + col);
     const float4 a = *o;
     *o = f4add(a, F);
 }
 
-// Sub-slot of quarter q of the tile starting at sorted position p0 (tile index t):
-// within a 128-position block at most two split-row tiles start, the last tile
-// of one row and the first of the next, so the parity bit keeps them apart.
-__device__ __forceinline__ int64_t sub_slot(int32_t p0, int32_t t, int q) {
-    return (static_cast<int64_t>(p0 >> 7) * 2 + (t == 0 ? 1 : 0)) * 4 + q;
+// Slot of the partial of the split-row tile starting at sorted position p0:
+// within a 128-position block at most two split-row tiles start, the last
+// tile of one row and the first tile (tfirst) of the next, so the parity bit
+// keeps them apart.
+__device__ __forceinline__ float4 *tile_slot(const IdxParams &p, int64_t p0, bool tfirst, int col) {
+    return reinterpret_cast<float4 *>(p.slots + ((p0 >> 7) * 2 + (tfirst ? 1 : 0)) * p.D + col);
 }
 
-// One quarter (32 members) of one tile of a heavy row, from the list K3 built.
-// The last quarter of the tile to arrive (an integer ticket) combines the four
-// quarters into the tile partial by the top two levels of the tile's tree; the
-// last tile of the row to arrive folds the tile partials in ascending order.
-__device__ __noinline__ void heavy_unit(const IdxParams &p, int32_t unit, int lane, float4 (*stk)[32]) {
-    const int2 ent = p.heavy[unit >> 2];
-    const int q = unit & 3;
-    const int32_t k = ent.x, t = ent.y;
-    const int32_t s0 = p.seg_start[k];
-    const int32_t e0 = p.seg_start[k + 1];
-    const int32_t p0 = s0 + t * kSegTile;
-    const int cnt_tile = min(kSegTile, e0 - p0);
-    const int cnt = min(kSub, cnt_tile - q * kSub);
-    const int32_t n_tiles = (e0 - s0 + kSegTile - 1) / kSegTile;
-    if (cnt > 0) {
-        for (int c0 = 0; c0 < p.D; c0 += 128) {
-            const int col = c0 + lane * 4;
-            const float4 v = window_sum(p, p0 + q * kSub, cnt, col < p.D ? col : -1, lane, stk);
-            if (col < p.D) *reinterpret_cast<float4 *>(p.slots + sub_slot(p0, t, q) * p.D + col) = v;
-        }
-    }
-    __threadfence();
-    __syncwarp();
-    const int64_t tslot = static_cast<int64_t>(p0 >> 7) * 2 + (t == 0 ? 1 : 0);
-    int tq = 0;
-    if (lane == 0) tq = atomicAdd(&p.tile_tickets[tslot], 1);
-    tq = __shfl_sync(0xffffffffu, tq, 0);
-    if (tq != 3) return;
-    __threadfence();
-    for (int c0 = 0; c0 < p.D; c0 += 128) {
-        const int col = c0 + lane * 4;
-        if (col >= p.D) continue;
-        float4 sq[4];
-#pragma unroll
-        for (int qq = 0; qq < 4; ++qq)
-            if (qq * kSub < cnt_tile)
-                sq[qq] = __ldcg(reinterpret_cast<const float4 *>(p.slots + sub_slot(p0, t, qq) * p.D + col));
-        float4 a = sq[0];
-        if (cnt_tile > 32) a = f4add(a, sq[1]);
-        if (cnt_tile > 64) {
-            float4 c = sq[2];
-            if (cnt_tile > 96) c = f4add(c, sq[3]);
-            a = f4add(a, c);
-        }
-        *reinterpret_cast<float4 *>(p.slots + sub_slot(p0, t, 0) * p.D + col) = a;
-    }
-    __threadfence();
-    __syncwarp();
-    int tk = 0;
-    if (lane == 0) {
-        p.tile_tickets[tslot] = 0;
-        tk = atomicAdd(&p.tickets[k], 1);
-    }
-    tk = __shfl_sync(0xffffffffu, tk, 0);
-    if (tk != n_tiles - 1) return;
-    __threadfence();
+// Ordered fold of the tile partials of a split row of at most kWarpFoldTiles
+// tiles by one warp, then out[k] += F.
+__device__ void warp_fold(const IdxParams &p, int32_t k, int64_t s0, int32_t n_tiles, int lane) {
     for (int c0 = 0; c0 < p.D; c0 += 128) {
         const int col = c0 + lane * 4;
         if (col >= p.D) continue;
@@ -480,105 +370,482 @@ __device__ __noinline__ void heavy_unit(const IdxParams &p, int32_t unit, int la
         for (int32_t b0 = 0; b0 < n_tiles; b0 += 8) {
             float4 v[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                if (b0 + u < n_tiles)
-                    v[u] = __ldcg(reinterpret_cast<const float4 *>(
-                        p.slots + sub_slot(s0 + (b0 + u) * kSegTile, b0 + u, 0) * p.D + col));
+            for (int u = 0; u < 8; ++u) {
+                v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                ldcg_v4f_if(v[u], tile_slot(p, s0 + static_cast<int64_t>(b0 + u) * kSegTile, b0 + u == 0, col),
+                            b0 + u < n_tiles);
+            }
 #pragma unroll
             for (int u = 0; u < 8; ++u)
                 if (b0 + u < n_tiles) F = (b0 + u == 0) ? v[u] : f4add(F, v[u]);
         }
         add_out(p, k, col, F);
     }
+}
+
+// A split-row tile is done for one column block: its partial goes to its slot
+// and the row counts it (an integer ticket). The last of the row's
+// tiles x column blocks to arrive folds a row of at most kWarpFoldTiles tiles;
+// a longer row is folded by a fold block.
+__device__ __noinline__ void tile_done(const IdxParams &p, int32_t k, int32_t p0, bool tfirst, float4 P, int col,
+                                       bool act, int lane) {
+    if (act) *tile_slot(p, p0, tfirst, col) = P;
+    __threadfence();
+    __syncwarp();
+    int32_t s0 = 0, e0 = 0, tk = 0;
+    if (lane == 0) {
+        s0 = p.seg_start[k];
+        e0 = p.seg_start[k + 1];
+        tk = atomicAdd(&p.tickets[k], 1);
+    }
+    s0 = __shfl_sync(0xffffffffu, s0, 0);
+    e0 = __shfl_sync(0xffffffffu, e0, 0);
+    tk = __shfl_sync(0xffffffffu, tk, 0);
+    const int32_t n_tiles = (e0 - s0 + kSegTile - 1) / kSegTile;
+    const int32_t n_cb = (p.D + 127) / 128;
+    if (n_tiles > kWarpFoldTiles || tk != n_tiles * n_cb - 1) return;
+    __threadfence();
+    warp_fold(p, k, s0, n_tiles, lane);
     if (lane == 0) p.tickets[k] = 0;
 }
 
-__device__ void row_unit(const IdxParams &p, int32_t r, int lane, float4 (*stk)[32]) {
-    const int32_t s = p.seg_start[r];
-    const int32_t e = p.seg_start[r + 1];
-    const int32_t n = e - s;
-    if (n <= 0) return;
-    if (p.seg_tile == 1) {  // purely sequential fold in original order
-        for (int c0 = 0; c0 < p.D; c0 += 128) {
-            const int col = c0 + lane * 4;
-            float4 F = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int32_t q0 = 0; q0 < n; q0 += 32) {
-                const int32_t mine = (q0 + lane < n) ? p.perm[s + q0 + lane] : 0;
-                const int cnt = min(32, n - q0);
-#pragma unroll 4
-                for (int u = 0; u < cnt; ++u) {
-                    const int32_t row = __shfl_sync(0xffffffffu, mine, u);
-                    if (col < p.D) {
-                        const float4 v = ld_src4(p, row, col);
-                        F = (q0 + u == 0) ? v : f4add(F, v);
+// Work of 32 consecutive keys, one per lane, cut into groups of gs members
+// (gs = 8, or the tile width when it is smaller) aligned to the row start.
+// An unsplit row is the warp's whole; of a split row the warp takes the tiles
+// whose first member lies in its share [P0, P1).
+struct KeyRows {
+    int32_t st, L, G, inc;  // first member taken, members taken, groups, inclusive prefix of G
+    int32_t ga0, sp;        // group index (within the row) of the first group taken; split row
+    int32_t kc, T;          // first key, total groups (uniform)
+};
+
+__device__ __forceinline__ void load_seg(const IdxParams &p, int32_t kc, int32_t k_end, int lane, int32_t &st,
+                                         int32_t &en) {
+    const int32_t k = kc + lane;
+    st = en = 0;
+    ldg_nc_b32_if(st, &p.seg_start[k], lane < k_end - kc);
+    ldg_nc_b32_if(en, &p.seg_start[k + 1], lane < k_end - kc);
+}
+
+__device__ __forceinline__ KeyRows key_rows(int32_t kc, int32_t k_end, int32_t st, int32_t en, int gs, bool split_on,
+                                            int32_t P0, int32_t P1, int lane) {
+    KeyRows R;
+    R.kc = kc;
+    const bool in = lane < k_end - kc;
+    const int32_t L = en - st;
+    R.sp = (split_on && L > kSplitMin) ? 1 : 0;
+    R.st = st;
+    R.L = L;
+    R.ga0 = 0;
+    if (R.sp) {
+        const int32_t n_t = (L + kSegTile - 1) / kSegTile;
+        const int32_t t_lo = st >= P0 ? 0 : (P0 - st + kSegTile - 1) / kSegTile;
+        const int32_t t_hi = min(n_t, static_cast<int32_t>((static_cast<int64_t>(P1) - st + kSegTile - 1) / kSegTile));
+        if (t_hi <= t_lo) {
+            R.L = 0;
+        } else {
+            const int64_t a = static_cast<int64_t>(st) + static_cast<int64_t>(t_lo) * kSegTile;
+            const int64_t b = min(static_cast<int64_t>(en), static_cast<int64_t>(st) + static_cast<int64_t>(t_hi) * kSegTile);
+            R.st = static_cast<int32_t>(a);
+            R.L = static_cast<int32_t>(b - a);
+            R.ga0 = t_lo * (kSegTile / 8);
+        }
+    }
+    R.G = (in && R.L > 0) ? (R.L + gs - 1) / gs : 0;
+    int32_t inc = R.G;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int32_t t = __shfl_up_sync(0xffffffffu, inc, d);
+        if (lane >= d) inc += t;
+    }
+    R.inc = inc;
+    R.T = __shfl_sync(0xffffffffu, inc, 31);
+    return R;
+}
+
+// A group's descriptor in one word: members (bits 0-3), first group (bit 4:
+// of its row, or of its tile in a split row), last group (bit 5: of its row,
+// or of its tile in a split row), index in its tile (bits 6-9), split row
+// (bit 10), group of the row's first tile (bit 11), row key (bits 12-28).
+__device__ __forceinline__ int32_t pack_group(int32_t key, int nv, bool first, bool last, int gi, bool sp, bool tfirst) {
+    return nv | (first << 4) | (last << 5) | (gi << 6) | (sp << 10) | (tfirst << 11) | (key << 12);
+}
+__device__ __forceinline__ int gd_nv(int32_t d) { return d & 15; }
+__device__ __forceinline__ bool gd_first(int32_t d) { return (d >> 4) & 1; }
+__device__ __forceinline__ bool gd_last(int32_t d) { return (d >> 5) & 1; }
+__device__ __forceinline__ int gd_gi(int32_t d) { return (d >> 6) & 15; }
+__device__ __forceinline__ bool gd_split(int32_t d) { return (d >> 10) & 1; }
+__device__ __forceinline__ bool gd_tfirst(int32_t d) { return (d >> 11) & 1; }
+__device__ __forceinline__ int32_t gd_key(int32_t d) { return d >> 12; }
+
+// Four consecutive groups: lane l holds member (l & 7) of group q0 + (l >> 3).
+struct Quad {
+    int32_t pq;    // that member's perm entry
+    int32_t desc;  // the group's descriptor
+    int32_t aux;   // first sorted position of the group's tile
+    int32_t n;     // groups in the quad (uniform)
+};
+
+__device__ __forceinline__ Quad make_quad(const IdxParams &p, const KeyRows &R, int32_t q0, int gs, int gpt, int lane) {
+    const unsigned full = 0xffffffffu;
+    const int32_t q = q0 + (lane >> 3);
+    const int u = lane & 7;
+    int r = 0;  // rows whose groups end at or before q: q's row
+#pragma unroll
+    for (int s = 16; s; s >>= 1)
+        if (__shfl_sync(full, R.inc, r + s - 1) <= q) r += s;
+    const int32_t Gr = __shfl_sync(full, R.G, r), incr = __shfl_sync(full, R.inc, r);
+    const int32_t str = __shfl_sync(full, R.st, r), Lr = __shfl_sync(full, R.L, r);
+    const int32_t ga0 = __shfl_sync(full, R.ga0, r);
+    const bool sp = __shfl_sync(full, R.sp, r) != 0;
+    const bool in = q < R.T;
+    const int32_t g = q - (incr - Gr);
+    const int nv = in ? min(gs, Lr - g * gs) : 0;
+    const int32_t ga = ga0 + g;
+    const int gi = ga & (gpt - 1);
+    const int32_t mpos = str + g * gs;
+    Quad Q;
+    Q.desc = pack_group(R.kc + r, nv, sp ? gi == 0 : g == 0, g == Gr - 1 || (sp && gi == gpt - 1), gi, sp, ga < gpt);
+    Q.aux = mpos - gi * gs;
+    Q.pq = 0;
+    ldg_nc_b32_if(Q.pq, &p.perm[mpos + u], in && u < nv);
+    Q.n = min(4, R.T - q0);
+    return Q;
+}
+
+// Cursor over the groups of keys [kc, k_end): the current 32 keys' work, the
+// next 32 keys' segment starts (prefetched), the next quad to build.
+struct GroupCursor {
+    KeyRows R;
+    int32_t nst, nen, q0, k_end, P0, P1;
+};
+
+__device__ __forceinline__ bool next_quad(const IdxParams &p, GroupCursor &c, Quad &Q, int gs, int gpt, bool split_on,
+                                          int lane) {
+    while (c.q0 >= c.R.T) {
+        if (c.k_end - c.R.kc <= 32) return false;
+        const int32_t kc = c.R.kc + 32;
+        c.R = key_rows(kc, c.k_end, c.nst, c.nen, gs, split_on, c.P0, c.P1, lane);
+        if (c.k_end - kc > 32) load_seg(p, kc + 32, c.k_end, lane, c.nst, c.nen);
+        c.q0 = 0;
+    }
+    Q = make_quad(p, c.R, c.q0, gs, gpt, lane);
+    c.q0 += 4;
+    return true;
+}
+
+// A tile's group stack in registers: level l holds the sum of a complete
+// block of 2^l groups waiting for its right sibling (at most 16 groups of 8
+// in a tile of 128, so five levels).
+struct GStack {
+    float4 s0, s1, s2, s3, s4;
+};
+
+// Group gi of its tile joins the blocks it closes (the pairwise tree, bottom-up).
+__device__ __forceinline__ void gpush(GStack &S, int gi, float4 v) {
+    if (!(gi & 1)) {
+        S.s0 = v;
+        return;
+    }
+    v = f4add(S.s0, v);
+    if (!(gi & 2)) {
+        S.s1 = v;
+        return;
+    }
+    v = f4add(S.s1, v);
+    if (!(gi & 4)) {
+        S.s2 = v;
+        return;
+    }
+    v = f4add(S.s2, v);
+    if (!(gi & 8)) {
+        S.s3 = v;
+        return;
+    }
+    S.s4 = f4add(S.s3, v);
+}
+
+// Partial of a tile holding c groups: the complete blocks of the set bits of
+// c, smallest first, each larger (earlier) block on the left - the canonical
+// tree with the absent leaves past the end passing their sibling up.
+__device__ __forceinline__ float4 gpartial(const GStack &S, int c) {
+    float4 acc = S.s0;
+    bool have = (c & 1) != 0;
+    if (c & 2) {
+        acc = have ? f4add(S.s1, acc) : S.s1;
+        have = true;
+    }
+    if (c & 4) {
+        acc = have ? f4add(S.s2, acc) : S.s2;
+        have = true;
+    }
+    if (c & 8) {
+        acc = have ? f4add(S.s3, acc) : S.s3;
+        have = true;
+    }
+    if (c & 16) acc = have ? f4add(S.s4, acc) : S.s4;
+    return acc;
+}
+
+// 16-byte asynchronous copy global -> shared (L2 only), under a predicate.
+__device__ __forceinline__ void cp_async16_if(void *smem, const void *gmem, bool pred) {
+    const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
+        "@q cp.async.cg.shared.global [%0], [%1], 16;\n\t}" ::"r"(s),
+        "l"(gmem), "r"(static_cast<int>(pred))
+        : "memory");
+}
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) { cp_async16_if(smem, gmem, true); }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// A warp's ring of kStages slots; a slot holds one group: its 8 source rows
+// and, on an unsplit row's first group, the row's out[key] (row 8), 16 bytes
+// per lane each; the group's descriptor and tile start sit beside the ring.
+constexpr int kStages = 3;
+constexpr int kSlotRows = 9;
+constexpr int kSlotF4 = kSlotRows * 32;
+constexpr int kSegThreads = 512;
+constexpr int kSegWarps = kSegThreads / 32;
+constexpr int kSegSmemBytes = kSegWarps * (kStages * kSlotF4 * 16 + kStages * 2 * 4);
+
+// Copies of group j of quad Q into a slot. Each lane copies (and later reads)
+// only its own 16-byte column slice; the descriptor words (dslot) are written
+// by lane 0 and read by all lanes after a warp barrier.
+__device__ __forceinline__ void issue_group(const IdxParams &p, float4 *slot, int32_t *dslot, const Quad &Q, int j,
+                                            int col, bool act, int lane) {
+    const unsigned full = 0xffffffffu;
+    const int32_t gd = __shfl_sync(full, Q.desc, j * 8);
+    const int32_t aux = __shfl_sync(full, Q.aux, j * 8);
+    __syncwarp();
+    if (lane == 0) {
+        dslot[0] = gd;
+        dslot[1] = aux;
+    }
+    const int nv = gd_nv(gd);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int32_t row = __shfl_sync(full, Q.pq, j * 8 + u);
+        cp_async16_if(slot + u * 32 + lane, p.src + static_cast<int64_t>(row) * p.ld_src + col, u < nv && act);
+    }
+    cp_async16_if(slot + 8 * 32 + lane, p.out + static_cast<int64_t>(gd_key(gd)) * p.ld_out + col,
+                  gd_first(gd) && !gd_split(gd) && act);
+}
+
+struct RowAcc {
+    float4 F, o;
+    int32_t tix;
+};
+
+// Group sum by the tile tree's lowest levels in registers (absent members past
+// nv pass their sibling up), then the group joins its tile's group stack; a
+// tile's last group yields the tile partial. An unsplit row folds its tile
+// partials into F in order and its last group writes out[key] + F; a split
+// row's tile partial goes to the tile's slot.
+__device__ __forceinline__ void consume_group(const IdxParams &p, const float4 *slot, const int32_t *dslot, RowAcc &ra,
+                                              GStack &S, int gs, int gpt, int col, bool act, int lane) {
+    __syncwarp();
+    const int32_t gd = dslot[0];
+    const int nv = gd_nv(gd);
+    float4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = slot[u * 32 + lane];
+#pragma unroll
+    for (int st = 1; st < 8; st *= 2) {
+        if (st < gs) {
+#pragma unroll
+            for (int r = 0; r + st < 8; r += 2 * st)
+                if (r + st < nv) v[r] = f4add(v[r], v[r + st]);
+        }
+    }
+    const bool sp = gd_split(gd);
+    if (gd_first(gd) && !sp) {
+        ra.o = slot[8 * 32 + lane];
+        ra.tix = 0;
+    }
+    const int gi = gd_gi(gd);
+    gpush(S, gi, v[0]);
+    const bool last = gd_last(gd);
+    if (last || gi == gpt - 1) {
+        const float4 P = gpartial(S, gi + 1);
+        if (sp) {
+            tile_done(p, gd_key(gd), dslot[1], gd_tfirst(gd), P, col, act, lane);
+            return;
+        }
+        ra.F = (ra.tix == 0) ? P : f4add(ra.F, P);
+        ++ra.tix;
+    }
+    if (last && act)
+        *reinterpret_cast<float4 *>(p.out + static_cast<int64_t>(gd_key(gd)) * p.ld_out + col) = f4add(ra.o, ra.F);
+}
+
+// Warp's share of the sorted order: positions [P0, P1). The warp sums every
+// unsplit row that starts there and every split-row tile that starts there:
+// keys [k_first, k_end), walked as one stream of groups. Perm entries come one
+// quad (4 groups) ahead; source rows land in the warp's shared-memory ring
+// kStages - 1 groups ahead of the sums.
+__device__ void walk(const IdxParams &p, int32_t P0, int32_t P1, int lane, float4 *ring, int32_t *dring) {
+    int32_t k_first, k_end;
+    {
+        const int32_t s0 = p.skey[P0];
+        const int32_t k0 = s0 & kKeyMask;
+        const int32_t kb = P0 > 0 ? (p.skey[P0 - 1] & kKeyMask) : -1;
+        k_first = (k0 != kb || (s0 & kSplitBit)) ? k0 : k0 + 1;
+        if (P1 < p.N) {
+            const int32_t k1 = p.skey[P1] & kKeyMask;
+            k_end = k1 != (p.skey[P1 - 1] & kKeyMask) ? k1 : k1 + 1;
+        } else {
+            k_end = p.R + 1;
+        }
+    }
+    if (k_first >= k_end) return;
+    const int gs = min(8, p.seg_tile);
+    const int gpt = p.seg_tile / gs;
+    const bool split_on = p.seg_tile == kSegTile;
+    for (int c0 = 0; c0 < p.D; c0 += 128) {
+        const int col = c0 + lane * 4;
+        const bool act = col < p.D;
+        GroupCursor cur;
+        cur.k_end = k_end;
+        cur.P0 = P0;
+        cur.P1 = P1;
+        {
+            int32_t st, en;
+            load_seg(p, k_first, k_end, lane, st, en);
+            cur.nst = cur.nen = 0;
+            if (k_end - k_first > 32) load_seg(p, k_first + 32, k_end, lane, cur.nst, cur.nen);
+            cur.R = key_rows(k_first, k_end, st, en, gs, split_on, P0, P1, lane);
+            cur.q0 = 0;
+        }
+        Quad Qc, Qn;
+        bool have = next_quad(p, cur, Qc, gs, gpt, split_on, lane);
+        if (!have) continue;
+        bool hn = next_quad(p, cur, Qn, gs, gpt, split_on, lane);
+        int ji = 0;
+        int issued = 0, consumed = 0;
+        RowAcc ra;
+        ra.F = ra.o = make_float4(0.f, 0.f, 0.f, 0.f);
+        ra.tix = 0;
+        GStack S;
+        S.s0 = S.s1 = S.s2 = S.s3 = S.s4 = ra.F;
+        auto issue_next = [&]() {
+            if (have) {
+                const int slot = issued % kStages;
+                issue_group(p, ring + slot * kSlotF4, dring + slot * 2, Qc, ji, col, act, lane);
+                ++issued;
+                if (++ji == Qc.n) {
+                    ji = 0;
+                    if (!hn) {
+                        have = false;
+                    } else {
+                        Qc = Qn;
+                        hn = next_quad(p, cur, Qn, gs, gpt, split_on, lane);
                     }
                 }
             }
-            if (col < p.D) add_out(p, r, col, F);
+            cp_async_commit();
+        };
+#pragma unroll
+        for (int i = 0; i < kStages - 1; ++i) issue_next();
+        while (consumed < issued) {
+            issue_next();
+            cp_async_wait<kStages - 1>();
+            const int slot = consumed % kStages;
+            consume_group(p, ring + slot * kSlotF4, dring + slot * 2, ra, S, gs, gpt, col, act, lane);
+            ++consumed;
         }
+        cp_async_wait<0>();
+    }
+}
+
+// Fold block: the ordered fold of the tile partials of split rows longer than
+// kWarpFoldTiles tiles. The block waits (bounded) until every tile (in every
+// column block) of the row is counted, stages the partials in shared memory
+// with cp.async, kFoldTiles tiles per buffer in two buffers, and warp 0 folds
+// them in ascending order.
+constexpr int kFoldTiles = 192;
+
+__device__ void fold_rows(const IdxParams &p, int first, int stride, int n_rows, float4 *stage) {
+    __shared__ int timed_out;
+    const int tid = threadIdx.x, lane = tid & 31;
+    for (int i = first; i < n_rows; i += stride) {
+        const int32_t k = p.heavy_rows[i];
+        const int64_t s0 = p.seg_start[k], e0 = p.seg_start[k + 1];
+        const int32_t T = static_cast<int32_t>((e0 - s0 + kSegTile - 1) / kSegTile);
+        if (tid == 0) {
+            timed_out = wait_counter_geq(&p.tickets[k], T * ((p.D + 127) / 128)) ? 0 : 1;
+            if (timed_out) record_error(p.hdr, DGR_ERR_TIMEOUT, 2);
+        }
+        __syncthreads();
+        const bool skip = timed_out != 0;
+        __syncthreads();
+        if (skip) continue;
+        for (int c0 = 0; c0 < p.D; c0 += 128) {
+            const int w4 = min(32, (p.D - c0) / 4);  // float4 per tile row in this column block
+            auto issue = [&](int buf, int32_t t0) {
+                for (int e = tid; e < kFoldTiles * 32; e += kSegThreads) {
+                    const int32_t t = t0 + e / 32;
+                    const int c = e % 32;
+                    if (t < T && c < w4)
+                        cp_async16(stage + (buf * kFoldTiles + e / 32) * 32 + c,
+                                   tile_slot(p, s0 + static_cast<int64_t>(t) * kSegTile, t == 0, c0 + c * 4));
+                }
+                cp_async_commit();
+            };
+            issue(0, 0);
+            issue(1, kFoldTiles);
+            float4 F = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int32_t t0 = 0, j = 0; t0 < T; t0 += kFoldTiles, ++j) {
+                cp_async_wait<1>();
+                __syncthreads();
+                if (tid < 32 && lane < w4) {
+                    const float4 *sb = stage + (j & 1) * kFoldTiles * 32;
+                    const int nt = min(kFoldTiles, T - t0);
+                    for (int u = 0; u < nt; ++u) F = (t0 + u == 0) ? sb[u * 32 + lane] : f4add(F, sb[u * 32 + lane]);
+                }
+                __syncthreads();
+                issue(j & 1, t0 + 2 * kFoldTiles);
+            }
+            cp_async_wait<0>();
+            if (tid < 32 && lane < w4) add_out(p, k, c0 + lane * 4, F);
+            __syncthreads();
+        }
+        if (tid == 0) p.tickets[k] = 0;
+    }
+}
+
+// Persistent: one block of 16 warps per SM. The first blocks (up to
+// kMaxFoldBlocks, one per long split row) fold; every other warp takes an
+// equal share of the sorted order.
+__global__ void __launch_bounds__(kSegThreads, 1) segsum_kernel(const IdxParams p) {
+    extern __shared__ __align__(16) float4 seg_smem[];
+    const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
+    const int n_fold_rows = p.seg_tile == kSegTile ? p.hdr->pad[3] : 0;
+    const int n_fold = min(n_fold_rows, min(kMaxFoldBlocks, static_cast<int>(gridDim.x) - 1));
+    if (static_cast<int>(blockIdx.x) < n_fold) {
+        fold_rows(p, blockIdx.x, n_fold, n_fold_rows, seg_smem);
         return;
     }
-    const int W = p.seg_tile;
-    const int32_t n_tiles = (n + W - 1) / W;
-    if (W == kSegTile && n_tiles > kWarpMaxTiles) return;  // split-row units handle it
-    for (int c0 = 0; c0 < p.D; c0 += 128) {
-        const int col = c0 + lane * 4;
-        const int lcol = col < p.D ? col : -1;
-        float4 F = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int32_t t = 0; t < n_tiles; ++t) {
-            const int cnt = min(W, n - t * W);
-            const float4 P = window_sum(p, s + t * W, cnt, lcol, lane, stk);
-            F = (t == 0) ? P : f4add(F, P);
-        }
-        if (col < p.D) add_out(p, r, col, F);
-    }
+    const int64_t W = static_cast<int64_t>(gridDim.x - n_fold) * kSegWarps;
+    const int64_t w = static_cast<int64_t>(blockIdx.x - n_fold) * kSegWarps + wi;
+    int64_t span = (static_cast<int64_t>(p.N) + W - 1) / W;
+    if (span < 32) span = 32;
+    const int64_t P0 = w * span;
+    if (P0 >= p.N) return;
+    const int32_t P1 = static_cast<int32_t>(min(P0 + span, static_cast<int64_t>(p.N)));
+    float4 *ring = seg_smem + wi * (kStages * kSlotF4);
+    int32_t *dring = reinterpret_cast<int32_t *>(seg_smem + kSegWarps * kStages * kSlotF4) + wi * (kStages * 2);
+    walk(p, static_cast<int32_t>(P0), P1, lane, ring, dring);
 }
 
-// Small widths (2, 4): a tree over 2 or 4 members, per lane, no stack.
-__device__ void row_unit_small(const IdxParams &p, int32_t r, int lane) {
-    const int32_t s = p.seg_start[r];
-    const int32_t e = p.seg_start[r + 1];
-    const int32_t n = e - s;
-    if (n <= 0) return;
-    const int W = p.seg_tile;
-    for (int c0 = 0; c0 < p.D; c0 += 128) {
-        const int col = c0 + lane * 4;
-        float4 F = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int32_t t0 = 0; t0 < n; t0 += W) {
-            const int cnt = min(W, n - t0);
-            float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0, v2 = v0, v3 = v0;
-            if (col < p.D) {
-                v0 = ld_src4(p, p.perm[s + t0], col);
-                if (cnt > 1) v1 = ld_src4(p, p.perm[s + t0 + 1], col);
-                if (cnt > 2) v2 = ld_src4(p, p.perm[s + t0 + 2], col);
-                if (cnt > 3) v3 = ld_src4(p, p.perm[s + t0 + 3], col);
-                if (cnt > 1) v0 = f4add(v0, v1);
-                if (cnt > 3) v2 = f4add(v2, v3);
-                if (cnt > 2) v0 = f4add(v0, v2);
-                F = (t0 == 0) ? v0 : f4add(F, v0);
-            }
-        }
-        if (col < p.D) add_out(p, r, col, F);
-    }
-}
-
-__global__ void __launch_bounds__(kThreads, 3) segsum_kernel(const IdxParams p) {
-    __shared__ float4 stack[kWarps][kStackLevels][32];
-    const int lane = threadIdx.x & 31;
-    float4 (*stk)[32] = stack[threadIdx.x >> 5];
-    const int64_t wg = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-    // the first 4 x (listed heavy tiles) warps also take one quarter of a heavy tile
-    const int64_t n_heavy = (p.seg_tile == kSegTile) ? static_cast<int64_t>(p.hdr->pad[3]) * 4 : 0;
-    if (wg < n_heavy) heavy_unit(p, static_cast<int32_t>(wg), lane, stk);
-    const int64_t r = wg;
-    if (r > p.R) return;
-    if (p.seg_tile == 2 || p.seg_tile == 4) row_unit_small(p, static_cast<int32_t>(r), lane);
-    else row_unit(p, static_cast<int32_t>(r), lane, stk);
-}
-
+static_assert(2 * kFoldTiles * 32 * 16 <= kSegSmemBytes, "fold stage fits the segsum shared memory");
 struct IdxLayout {
-    int32_t nb, n_buckets, n_pblk, max_heavy;
-    size_t keys_a, vals_a, perm, skey, hist, offs, bucket_start, seg_start, tickets, tile_tickets, slots;
+    int32_t nb, n_buckets, n_pblk, max_fold_rows;
+    size_t keys_a, vals_a, perm, skey, hist, offs, bucket_start, seg_start, tickets, slots;
     size_t bucket_negmin, bucket_max, bucket_key, heavy, total;
 };
 
@@ -587,8 +854,7 @@ IdxLayout idx_layout(int64_t N, int64_t R, int64_t D) {
     L.nb = static_cast<int32_t>((N + kBlockElems - 1) / kBlockElems);
     L.n_buckets = static_cast<int32_t>((R + 1 + 255) / 256);
     L.n_pblk = static_cast<int32_t>((N + 127) / 128);
-    // tiles of rows with more than 8 tiles: at most N/128 plus one ragged tile per such row
-    L.max_heavy = static_cast<int32_t>(N / kSegTile + N / (kWarpMaxTiles * kSegTile + 1) + 1);
+    L.max_fold_rows = static_cast<int32_t>(N / (kWarpFoldTiles * kSegTile + 1) + 1);
     size_t o = sizeof(WsHeader);
     auto take = [&](size_t bytes) {
         size_t at = o;
@@ -604,12 +870,11 @@ IdxLayout idx_layout(int64_t N, int64_t R, int64_t D) {
     L.bucket_start = take((kDigits + 1) * 4);
     L.seg_start = take((R + 2) * 4);
     L.tickets = take((R + 1) * 4);
-    L.tile_tickets = take(static_cast<size_t>(L.n_pblk) * 2 * 4);
-    L.slots = take(static_cast<size_t>(L.n_pblk) * 8 * D * 4);
+    L.slots = take(static_cast<size_t>(L.n_pblk) * 2 * D * 4);
     L.bucket_negmin = take(kDigits * 4);
     L.bucket_max = take(kDigits * 4);
     L.bucket_key = take(kDigits * 4);
-    L.heavy = take(static_cast<size_t>(L.max_heavy) * 8);
+    L.heavy = take(static_cast<size_t>(L.max_fold_rows) * 4);
     L.total = o;
     return L;
 }
@@ -679,21 +944,22 @@ extern "C" dgr_status dgr_det_index_add(float *out, int64_t R, int64_t D, int64_
     p.bucket_start = reinterpret_cast<int32_t *>(w + L.bucket_start);
     p.seg_start = reinterpret_cast<int32_t *>(w + L.seg_start);
     p.tickets = reinterpret_cast<int32_t *>(w + L.tickets);
-    p.tile_tickets = reinterpret_cast<int32_t *>(w + L.tile_tickets);
     p.slots = reinterpret_cast<float *>(w + L.slots);
     p.bucket_negmin = reinterpret_cast<int32_t *>(w + L.bucket_negmin);
     p.bucket_max = reinterpret_cast<int32_t *>(w + L.bucket_max);
     p.bucket_key = reinterpret_cast<int32_t *>(w + L.bucket_key);
-    p.heavy = reinterpret_cast<int2 *>(w + L.heavy);
+    p.heavy_rows = reinterpret_cast<int32_t *>(w + L.heavy);
     count_kernel<<<L.nb, kThreads, 0, s>>>(p);
     scatter_high_kernel<<<L.nb, kThreads, 0, s>>>(p);
     bucket_kernel<<<L.n_buckets, kThreads, 0, s>>>(p);
-    if (D > 0) {
-        const int64_t heavy_warps = seg_tile == kSegTile ? static_cast<int64_t>(L.max_heavy) * 4 : 0;
-        const int64_t warps = (R + 1) > heavy_warps ? (R + 1) : heavy_warps;
-        const int64_t grid = (warps + kWarps - 1) / kWarps;
-        if (grid > INT32_MAX) return DGR_ERR_UNSUPPORTED;
-        segsum_kernel<<<static_cast<unsigned>(grid), kThreads, 0, s>>>(p);
+    if (D > 0) {  // persistent: one block per SM, each warp one share of the sorted order
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaFuncSetAttribute(segsum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSegSmemBytes) !=
+                cudaSuccess)
+            return DGR_ERR_CUDA;
+        segsum_kernel<<<static_cast<unsigned>(sms), kSegThreads, kSegSmemBytes, s>>>(p);
     }
     return launch_status();
 }

@@ -49,6 +49,10 @@ CASES = [
     (4000, 4, 0, 128, "zeros"),          # only the dummy row
     (1, 4, 3, 128, "random"),
     (70000, 128, 60000, 128, "zeros"),   # many high-byte buckets
+    (9000, 64, 40, 128, "random"),       # rows of ~200: split, folded by one warp
+    (100000, 32, 20, 128, "random"),     # rows of ~4500: split, 21 rows over 16 fold blocks
+    (60000, 256, 30, 128, "random"),     # split rows over two column blocks
+    (50000, 128, 1, 128, "zeros"),       # one long row and the dummy row
 ]
 
 
