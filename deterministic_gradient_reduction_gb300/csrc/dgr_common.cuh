@@ -93,6 +93,15 @@ __device__ __forceinline__ void ld_v4f_if(float4 &v, const void *ptr, bool pred)
         : "l"(ptr), "r"(static_cast<int>(pred)));
 }
 
+// 16-byte read-only integer load under a predicate.
+__device__ __forceinline__ void ldg_nc_v4u_if(uint4 &v, const void *ptr, bool pred) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+        "@q ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];\n\t}"
+        : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w)
+        : "l"(ptr), "r"(static_cast<int>(pred)));
+}
+
 // 32-bit read-only load under a predicate.
 __device__ __forceinline__ void ldg_nc_b32_if(int32_t &v, const int32_t *ptr, bool pred) {
     asm volatile(

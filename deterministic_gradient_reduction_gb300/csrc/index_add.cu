@@ -3,64 +3,68 @@
 //
 // Megatron-LM PR #7441 (DSv4 --deterministic-mode), Source 3: the atomic-free
 // dK is an index_add done as a stable sort plus a (prefix) sum, with padding
-// slots spread over dummy rows that the caller drops. Four launches:
-//   K1 count   - map idx to keys (idx outside [0, R) -> R; outside [-1, R) is
-//                counted), per-block histograms of the key's high byte and each
-//                bucket's key range; the last block to finish scans the
-//                histograms (digit-major) into per-block scatter offsets and
-//                bucket starts, and marks buckets that hold a single key.
-//   K2 scatter - stable scatter by the high byte: inside a block, elements are
-//                ranked in original order with warp match/ballot and per-warp
-//                digit counters, so equal digits keep their input order. A
-//                single-key bucket (the dummy row) is already in final order
-//                and goes straight to the sorted arrays.
-//   K3 bucket  - one block per high-byte bucket: counting sort by the low byte
-//                (stable, same ranking), which also yields seg_start[] for the
-//                bucket's 256 keys, and lists the tiles of rows too long for
-//                one warp.
-//   K4 segsum  - one warp per destination row sums its members (in original
-//                order) by the pairwise tree over tiles of 128 members and folds
-//                the tiles in order, then out[r] += sum with one rounding.
-//                Rows with more than 8 tiles are split: one warp per 32-member
-//                quarter of each listed tile writes a slot; the last quarter of a tile
-//                to arrive (an integer ticket) combines the quarters into the
-//                tile partial, and the last tile of the row folds the tile
-//                partials in order.
-// Integer atomics only count; no floating-point value depends on timing.
+// slots spread over dummy rows that the caller drops. Five launches:
+//   hist     - map idx to keys (idx outside [0, R) -> R; outside [-1, R) is
+//              counted); each 2048-element tile stores its low-byte digit
+//              counts and adds its low- and high-byte histograms to the
+//              global ones (integer atomics).
+//   pass 0/1 - stable LSD radix passes by the low, then the high byte. Each
+//              tile ranks its elements in original order with warp
+//              match/ballot and per-warp digit counters; a digit's offset is
+//              its global base plus the earlier tiles' counts of it, summed
+//              32 tiles at a time back to the nearest tile that has already
+//              published its inclusive count. Every count is there before the
+//              pass starts (pass 0 adds, per element, to the digit counts of
+//              the pass-1 tile it lands in), so nothing waits. Pass 1 writes
+//              the sorted keys and the permutation.
+//   segstart - segment starts from the key changes of the sorted keys, and
+//              the list of rows longer than 32 tiles.
+// Every scratch word a launch leaves non-zero is cleared by a later launch of
+// the same call, so a workspace zeroed once serves every call.
+//   segsum   - persistent warps, each an equal share of the sorted order: the
+//              rows starting in the share as one stream of 8-member groups,
+//              summed by the pairwise tree over tiles of 128 members and
+//              folded tile by tile, then out[r] += sum with one rounding. A
+//              row longer than one tile is split by tile; the tile partials
+//              go to slots and are folded in order by the warp completing the
+//              last tile (an integer ticket) or, for rows longer than 32
+//              tiles, by a fold block.
+// Integer atomics only count or hand out tile numbers; no floating-point
+// value depends on timing.
 #include "dgr_common.cuh"
 
 namespace dgr {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kItems = 32;
-constexpr int kBlockElems = kThreads * kItems;  // 8192 elements per sort block
+constexpr int kSortThreads = 256;
+constexpr int kSortWarps = kSortThreads / 32;
+constexpr int kSortItems = 8;
+constexpr int kSortTile = kSortThreads * kSortItems;  // 2048 elements per sort tile
 constexpr int kDigits = 256;
 constexpr int kSegTile = 128;
-constexpr int kSplitMin = kSegTile;             // rows longer than one tile are split into quarters
-constexpr int kWarpFoldTiles = 32;               // split rows up to 32 tiles: folded by one warp
-constexpr int kMaxFoldBlocks = 16;               // longer rows: folded by up to 16 fold blocks
-constexpr int32_t kSplitBit = 1 << 30;           // sorted key flag: the key's row is split
-constexpr int32_t kKeyMask = kSplitBit - 1;
+constexpr int kSplitMin = kSegTile;    // rows longer than one tile are split by tile
+constexpr int kWarpFoldTiles = 32;     // split rows up to 32 tiles: folded by one warp
+constexpr int kMaxFoldBlocks = 16;     // longer rows: folded by up to 16 fold blocks
+constexpr int kSegStartThreads = 256;
 
 struct IdxParams {
     const int32_t *idx;
     int32_t N, R, D;
-    int32_t nb;             // sort blocks
-    int32_t n_buckets;      // high-byte buckets covering keys 0..R
-    int32_t n_pblk;         // 128-position blocks of the sorted order (slot indexing)
+    int32_t nb;      // sort tiles
+    int32_t n_pblk;  // 128-position blocks of the sorted order (slot indexing)
     int32_t seg_tile;
     const float *src;
     int64_t ld_src;
     float *out;
     int64_t ld_out;
     int32_t *bad_count;
-    int32_t *keys_a, *vals_a, *perm, *skey, *hist, *offs, *bucket_start, *seg_start, *tickets;
-    int32_t *bucket_negmin, *bucket_max, *bucket_key;
-    int32_t *heavy_rows;  // split rows longer than kWarpFoldTiles tiles (fold-block work)
+    int32_t *keys_a, *vals_a, *perm, *skey, *seg_start, *tickets;
+    int32_t *hist;               // [2][256] global digit histograms (low byte, high byte)
+    int32_t *cnt;                // [2][nb][256] per-tile digit counts of the two passes
+    int32_t *incl;               // [2][nb][256] published inclusive counts (bit 31: published)
+    int32_t *heavy_rows;         // split rows longer than kWarpFoldTiles tiles (fold-block work)
     float *slots;
-    WsHeader *hdr;
+    WsHeader *hdr;  // pad[2]: bad-index total, pad[3]: fold-row count
 };
 
 __device__ __forceinline__ int32_t map_key(int32_t v, int32_t R, bool &bad) {
@@ -76,109 +80,47 @@ __device__ __forceinline__ unsigned lanemask_lt() {
 }
 
 // ---------------------------------------------------------------------------
-// K1: high-byte histograms per block; the last block scans them.
+// hist: global digit histograms of the two passes, and the bad-index count.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) count_kernel(const IdxParams p) {
-    __shared__ int32_t h[kDigits];
-    __shared__ int32_t mn[kDigits];
-    __shared__ int32_t mx[kDigits];
-    __shared__ int32_t base[kDigits + 1];
+__global__ void __launch_bounds__(kSortThreads) hist_kernel(const IdxParams p) {
+    __shared__ int32_t h[2][kDigits];
     __shared__ int32_t bad_block;
-    __shared__ int is_last;
     const int tid = threadIdx.x;
-    const int b = blockIdx.x;
-    h[tid] = 0;
-    mn[tid] = INT32_MAX;
-    mx[tid] = -1;
+    h[0][tid] = 0;
+    h[1][tid] = 0;
     if (tid == 0) bad_block = 0;
-    if (b == 0 && tid == 0) p.hdr->pad[3] = 0;  // fold-row list of this call starts empty
+    if (blockIdx.x == 0 && tid == 0) p.hdr->pad[3] = 0;  // fold-row list of this call starts empty
     __syncthreads();
-    int32_t v[kItems];
+    int32_t v[kSortItems];
 #pragma unroll
-    for (int r = 0; r < kItems; ++r) {
-        const int64_t e = static_cast<int64_t>(b) * kBlockElems + r * kThreads + tid;
-        v[r] = e < p.N ? p.idx[e] : INT32_MIN;
+    for (int r = 0; r < kSortItems; ++r) {
+        const int64_t e = static_cast<int64_t>(blockIdx.x) * kSortTile + r * kSortThreads + tid;
+        v[r] = 0;
+        ldg_nc_b32_if(v[r], p.idx + e, e < p.N);
     }
     int my_bad = 0;
 #pragma unroll
-    for (int r = 0; r < kItems; ++r) {
-        if (v[r] == INT32_MIN && static_cast<int64_t>(b) * kBlockElems + r * kThreads + tid >= p.N) continue;
+    for (int r = 0; r < kSortItems; ++r) {
+        const int64_t e = static_cast<int64_t>(blockIdx.x) * kSortTile + r * kSortThreads + tid;
+        if (e >= p.N) continue;
         bool bad = false;
         const int32_t k = map_key(v[r], p.R, bad);
         my_bad += bad ? 1 : 0;
-        atomicAdd(&h[k >> 8], 1);
-        atomicMin(&mn[k >> 8], k);
-        atomicMax(&mx[k >> 8], k);
+        atomicAdd(&h[0][k & 255], 1);
+        atomicAdd(&h[1][k >> 8], 1);
     }
     if (my_bad) atomicAdd(&bad_block, my_bad);
     __syncthreads();
-    p.hist[static_cast<int64_t>(b) * kDigits + tid] = h[tid];
-    if (h[tid] > 0) {
-        // per-bucket key range over all blocks (integer max: order-free)
-        atomicMax(&p.bucket_negmin[tid], INT32_MAX - mn[tid]);
-        atomicMax(&p.bucket_max[tid], mx[tid]);
-    }
+    p.cnt[static_cast<int64_t>(blockIdx.x) * kDigits + tid] = h[0][tid];
+    if (h[0][tid]) atomicAdd(&p.hist[tid], h[0][tid]);
+    if (h[1][tid]) atomicAdd(&p.hist[kDigits + tid], h[1][tid]);
     if (tid == 0 && bad_block) atomicAdd(&p.hdr->pad[2], bad_block);
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) is_last = atomicAdd(&p.hdr->pad[1], 1) == p.nb - 1;
-    __syncthreads();
-    if (!is_last) return;
-    __threadfence();
-    // digit-major exclusive scan: offs[b][d] = sum of digits < d + counts of d in blocks < b
-    int32_t total = 0;
-    for (int b0 = 0; b0 < p.nb; b0 += 16) {
-        int32_t c[16];
-#pragma unroll
-        for (int u = 0; u < 16; ++u)
-            c[u] = (b0 + u < p.nb) ? __ldcg(&p.hist[static_cast<int64_t>(b0 + u) * kDigits + tid]) : 0;
-#pragma unroll
-        for (int u = 0; u < 16; ++u) total += c[u];
-    }
-    h[tid] = total;
-    __syncthreads();
-    if (tid == 0) {
-        int32_t run = 0;
-        for (int d = 0; d < kDigits; ++d) {
-            base[d] = run;
-            run += h[d];
-        }
-        base[kDigits] = run;
-    }
-    __syncthreads();
-    int32_t run = base[tid];
-    for (int b0 = 0; b0 < p.nb; b0 += 16) {
-        int32_t c[16];
-#pragma unroll
-        for (int u = 0; u < 16; ++u)
-            c[u] = (b0 + u < p.nb) ? __ldcg(&p.hist[static_cast<int64_t>(b0 + u) * kDigits + tid]) : 0;
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            if (b0 + u < p.nb) {
-                p.offs[static_cast<int64_t>(b0 + u) * kDigits + tid] = run;
-                run += c[u];
-            }
-        }
-    }
-    p.bucket_start[tid] = base[tid];
-    const int32_t kmax = __ldcg(&p.bucket_max[tid]);
-    const int32_t kmin = INT32_MAX - __ldcg(&p.bucket_negmin[tid]);
-    p.bucket_key[tid] = (total > 0 && kmin == kmax) ? kmax : -1;  // one key: its order is final after K2
-    p.bucket_negmin[tid] = 0;
-    p.bucket_max[tid] = 0;
-    if (tid == 0) {
-        p.bucket_start[kDigits] = base[kDigits];
-        const int32_t bad = atomicAdd(&p.hdr->pad[2], 0);
-        if (p.bad_count) *p.bad_count = bad;
-        p.hdr->pad[2] = 0;
-        p.hdr->pad[1] = 0;
-    }
 }
 
-// Stable in-block ranking: warp w owns elements [w*kWarpElems, ...) of the
-// block in rounds of 32 (round-major, lane order = element order). Returns
-// each element's rank among equal digits inside its warp; cnt[w][d] ends as
-// the warp's digit counts.
+// Stable in-warp ranking: warp w owns its elements in rounds of 32
+// (round-major, lane order = element order). Returns each element's rank
+// among equal digits inside its warp; cnt[w][d] ends as the warp's digit
+// counts.
 __device__ __forceinline__ void warp_rank(int digit, bool valid, int32_t (*cnt)[kDigits], int w, int32_t &rank) {
     const int d = valid ? digit : kDigits;  // invalid lanes match each other only
     const unsigned peers = __match_any_sync(0xffffffffu, d);
@@ -191,155 +133,275 @@ __device__ __forceinline__ void warp_rank(int digit, bool valid, int32_t (*cnt)[
 }
 
 // ---------------------------------------------------------------------------
-// K2: stable scatter by the high byte. Elements of a one-key bucket go
-// straight to their final place (perm/skey); the others to keys_a/vals_a.
+// pass 0/1: stable radix pass by the low (0) or high (1) byte of the key.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) scatter_high_kernel(const IdxParams p) {
-    __shared__ int32_t cnt[kWarps][kDigits];
-    __shared__ int32_t pre[kWarps][kDigits];
-    __shared__ int32_t boff[kDigits];
-    __shared__ int32_t bkey[kDigits];
-    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-    const int b = blockIdx.x;
-    for (int q = tid; q < kWarps * kDigits; q += kThreads) (&cnt[0][0])[q] = 0;
-    boff[tid] = p.offs[static_cast<int64_t>(b) * kDigits + tid];
-    {
-        int32_t bk = p.bucket_key[tid];
-        if (bk >= 0 && p.seg_tile == kSegTile && p.bucket_start[tid + 1] - p.bucket_start[tid] > kSplitMin)
-            bk |= kSplitBit;
-        bkey[tid] = bk;
-    }
-    __syncthreads();
-    const int64_t e0 = static_cast<int64_t>(b) * kBlockElems + w * (kItems * 32) + lane;
-    int32_t key[kItems];
+template <int PASS>
+__device__ __forceinline__ int pass_digit(int32_t key) {
+    return PASS == 0 ? (key & 255) : (key >> 8);
+}
+
+constexpr int kLookWindow = 32;
+constexpr int32_t kPublished = static_cast<int32_t>(0x80000000u);
+
+// Relaxed 32-bit load under a predicate; v keeps its value otherwise.
+__device__ __forceinline__ void ld_relaxed_b32_if(int32_t &v, const int32_t *a, bool pred) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
+        "@q ld.relaxed.gpu.global.b32 %0, [%1];\n\t}"
+        : "+r"(v)
+        : "l"(a), "r"(static_cast<int>(pred))
+        : "memory");
+}
+
+// Count of digit d in the tiles before tile b: the earlier tiles' counts,
+// nearest first, kLookWindow at a time, until a tile whose inclusive count is
+// already published (it then replaces the rest); then tile b publishes its
+// own inclusive count. The counts come from earlier launches, so nothing
+// waits; an inclusive word holds all it publishes, so relaxed accesses
+// suffice. The first window is loaded early (look_load) and consumed late
+// (look_finish), with the tile's ranking in between.
+struct LookWin {
+    int32_t c[kLookWindow], f[kLookWindow];
+};
+
+__device__ __forceinline__ void look_load(LookWin &L, const int32_t *cnt, const int32_t *incl, int32_t j_hi, int d) {
 #pragma unroll
-    for (int r = 0; r < kItems; ++r) {
-        const int64_t e = e0 + r * 32;
-        bool bad = false;
-        key[r] = e < p.N ? map_key(p.idx[e], p.R, bad) : -1;
-    }
-    int32_t rank[kItems];
-#pragma unroll
-    for (int r = 0; r < kItems; ++r) warp_rank(key[r] >> 8, key[r] >= 0, cnt, w, rank[r]);
-    __syncthreads();
-    {
-        int32_t run = 0;
-        for (int ww = 0; ww < kWarps; ++ww) {
-            pre[ww][tid] = run;
-            run += cnt[ww][tid];
-        }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int r = 0; r < kItems; ++r) {
-        if (key[r] < 0) continue;
-        const int d = key[r] >> 8;
-        const int32_t pos = boff[d] + pre[w][d] + rank[r];
-        const int32_t e = static_cast<int32_t>(e0 + r * 32);
-        if (bkey[d] >= 0) {
-            p.perm[pos] = e;
-            p.skey[pos] = bkey[d];
-        } else {
-            p.keys_a[pos] = key[r];
-            p.vals_a[pos] = e;
-        }
+    for (int u = 0; u < kLookWindow; ++u) {
+        const int64_t at = static_cast<int64_t>(j_hi - u) * kDigits + d;
+        L.c[u] = 0;
+        L.f[u] = 0;
+        ld_relaxed_b32_if(L.f[u], incl + at, j_hi - u >= 0);
+        ldg_nc_b32_if(L.c[u], cnt + at, j_hi - u >= 0);
     }
 }
 
-// Split rows longer than kWarpFoldTiles tiles go on the fold blocks' list
-// (its order is immaterial: each row is folded by one block, the same way).
-__device__ __forceinline__ void list_fold_row(const IdxParams &p, int32_t key, int32_t n) {
-    if (n <= kWarpFoldTiles * kSegTile) return;
-    p.heavy_rows[atomicAdd(&p.hdr->pad[3], 1)] = key;
-}
-
-// ---------------------------------------------------------------------------
-// K3: per bucket, stable counting sort by the low byte, and segment starts.
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) bucket_kernel(const IdxParams p) {
-    __shared__ int32_t h[kDigits];
-    __shared__ int32_t base[kDigits];
-    __shared__ int32_t cnt[kWarps][kDigits];
-    __shared__ int32_t pre[kWarps][kDigits];
-    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-    const int d = blockIdx.x;
-    const int32_t bs = p.bucket_start[d];
-    const int32_t be = p.bucket_start[d + 1];
-    const int32_t k = d * 256 + tid;
-    const int32_t one_key = p.bucket_key[d];
-    if (one_key >= 0) {  // K2 already placed it; only the segment starts remain
-        if (k <= p.R) p.seg_start[k] = k <= one_key ? bs : be;
-        if (k == p.R) p.seg_start[p.R + 1] = p.N;
-        if (tid == 0 && p.seg_tile == kSegTile) list_fold_row(p, one_key, be - bs);
-        return;
-    }
-    h[tid] = 0;
-    __syncthreads();
-    for (int32_t c0 = bs; c0 < be; c0 += kBlockElems) {
-        int32_t kk[kItems];
+__device__ __forceinline__ int32_t look_finish(LookWin &L, const int32_t *cnt, int32_t *incl, int32_t b, int d,
+                                               int32_t count) {
+    int32_t excl = 0;
+    for (int32_t j_hi = b - 1; j_hi >= 0; j_hi -= kLookWindow) {
+        if (j_hi != b - 1) look_load(L, cnt, incl, j_hi, d);
+        bool done = false;
 #pragma unroll
-        for (int r = 0; r < kItems; ++r) {
-            const int32_t i = c0 + r * kThreads + tid;
-            kk[r] = i < be ? p.keys_a[i] : -1;
-        }
-#pragma unroll
-        for (int r = 0; r < kItems; ++r)
-            if (kk[r] >= 0) atomicAdd(&h[kk[r] & 255], 1);
-    }
-    __syncthreads();
-    if (tid == 0) {
-        int32_t run = 0;
-        for (int q = 0; q < kDigits; ++q) {
-            base[q] = bs + run;
-            run += h[q];
-        }
-    }
-    __syncthreads();
-    if (k <= p.R) p.seg_start[k] = base[tid];
-    if (k == p.R) p.seg_start[p.R + 1] = p.N;
-    if (k <= p.R && p.seg_tile == kSegTile) list_fold_row(p, k, h[tid]);
-    for (int32_t c0 = bs; c0 < be; c0 += kBlockElems) {
-        for (int q = tid; q < kWarps * kDigits; q += kThreads) (&cnt[0][0])[q] = 0;
-        __syncthreads();
-        const int32_t e0 = c0 + w * (kItems * 32) + lane;
-        int32_t key[kItems], val[kItems], rank[kItems];
-#pragma unroll
-        for (int r = 0; r < kItems; ++r) {
-            const int32_t e = e0 + r * 32;
-            key[r] = e < be ? p.keys_a[e] : -1;
-            val[r] = e < be ? p.vals_a[e] : 0;
-        }
-#pragma unroll
-        for (int r = 0; r < kItems; ++r) warp_rank(key[r] & 255, key[r] >= 0, cnt, w, rank[r]);
-        __syncthreads();
-        {
-            int32_t run = 0;
-            for (int ww = 0; ww < kWarps; ++ww) {
-                pre[ww][tid] = run;
-                run += cnt[ww][tid];
+        for (int u = 0; u < kLookWindow; ++u) {
+            if (done) continue;
+            if (L.f[u] & kPublished) {
+                excl += L.f[u] & ~kPublished;
+                done = true;
+            } else {
+                excl += L.c[u];
             }
         }
-        __syncthreads();
+        if (done) break;
+    }
+    asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(incl + static_cast<int64_t>(b) * kDigits + d),
+                 "r"(kPublished | (excl + count))
+                 : "memory");
+    return excl;
+}
+
+// Sum over tiles [0, b) of the digit counts, by 8 warps: warp v takes tiles
+// v, v + 8, ..., lane l digits 8l .. 8l + 7 (two 16-byte loads a tile), 8
+// tiles a lane in flight; the 8 partial sums go to red[v][].
+__device__ __forceinline__ void direct_prefix(const int32_t *cnt, int32_t b, int v, int lane, int32_t (*red)[kDigits]) {
+    int32_t acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int32_t j0 = v; j0 < b; j0 += 8 * kSortWarps) {
+        uint4 x[16];
 #pragma unroll
-        for (int r = 0; r < kItems; ++r) {
+        for (int u = 0; u < 8; ++u) {
+            const int32_t j = j0 + u * kSortWarps;
+            x[2 * u] = x[2 * u + 1] = make_uint4(0u, 0u, 0u, 0u);
+            ldg_nc_v4u_if(x[2 * u], cnt + static_cast<int64_t>(j) * kDigits + lane * 8, j < b);
+            ldg_nc_v4u_if(x[2 * u + 1], cnt + static_cast<int64_t>(j) * kDigits + lane * 8 + 4, j < b);
+        }
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            acc[(u & 1) * 4 + 0] += static_cast<int32_t>(x[u].x);
+            acc[(u & 1) * 4 + 1] += static_cast<int32_t>(x[u].y);
+            acc[(u & 1) * 4 + 2] += static_cast<int32_t>(x[u].z);
+            acc[(u & 1) * 4 + 3] += static_cast<int32_t>(x[u].w);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) red[v][lane * 8 + i] = acc[i];
+}
+
+constexpr int kPassThreads = 2 * kSortThreads;  // 8 ranking warps, 8 prefix warps
+constexpr int32_t kDirectTiles = 512;           // tiles below this sum the earlier counts directly
+
+template <int PASS>
+__global__ void __launch_bounds__(kPassThreads) pass_kernel(const IdxParams p) {
+    __shared__ int32_t cnt[kSortWarps][kDigits];
+    __shared__ int32_t red[kSortWarps][kDigits];
+    __shared__ int32_t gbase[kDigits];  // global position of this tile's first element of each digit
+    __shared__ int32_t lbase[kDigits];  // local position of the same
+    __shared__ int32_t excl_s[kDigits];
+    __shared__ int32_t wsum[kSortWarps];
+    __shared__ int32_t lsum[kSortWarps];
+    __shared__ int32_t sk[kSortTile], sv[kSortTile];
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+    const int32_t b = blockIdx.x;
+    const int64_t tiles = static_cast<int64_t>(p.nb) * kDigits;
+    const int32_t *cnt_g = p.cnt + PASS * tiles;
+    int32_t *incl_g = p.incl + PASS * tiles;
+    for (int q = tid; q < kSortWarps * kDigits; q += kPassThreads) (&cnt[0][0])[q] = 0;
+    __syncthreads();
+    int32_t key[kSortItems], val[kSortItems], rank[kSortItems];
+    int32_t gx = 0, my_count = 0;
+    if (w < kSortWarps) {
+        // ranking warps: warp w owns elements [b*2048 + w*256, +256) in 8 rounds of 32
+        const int64_t e0 = static_cast<int64_t>(b) * kSortTile + w * (kSortItems * 32) + lane;
+#pragma unroll
+        for (int r = 0; r < kSortItems; ++r) {
+            const int64_t e = e0 + r * 32;
+            key[r] = 0;
+            val[r] = static_cast<int32_t>(e);
+            if (PASS == 0) {
+                ldg_nc_b32_if(key[r], p.idx + e, e < p.N);
+            } else {
+                ldg_nc_b32_if(key[r], p.keys_a + e, e < p.N);
+                ldg_nc_b32_if(val[r], p.vals_a + e, e < p.N);
+            }
+        }
+        const int32_t hc = __ldcg(&p.hist[PASS * kDigits + tid]);
+        my_count = __ldcg(&cnt_g[static_cast<int64_t>(b) * kDigits + tid]);
+#pragma unroll
+        for (int r = 0; r < kSortItems; ++r) {
+            const int64_t e = e0 + r * 32;
+            if (e >= p.N) {
+                key[r] = -1;
+            } else if (PASS == 0) {
+                bool bad = false;
+                key[r] = map_key(key[r], p.R, bad);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < kSortItems; ++r)
+            warp_rank(key[r] >= 0 ? pass_digit<PASS>(key[r]) : 0, key[r] >= 0, cnt, w, rank[r]);
+        // exclusive scans over digits of the global histogram (global digit
+        // bases) and of this tile's counts (local digit bases)
+        int32_t gi = hc, li = my_count;
+#pragma unroll
+        for (int s = 1; s < 32; s <<= 1) {
+            const int32_t tg = __shfl_up_sync(0xffffffffu, gi, s);
+            const int32_t tl = __shfl_up_sync(0xffffffffu, li, s);
+            if (lane >= s) {
+                gi += tg;
+                li += tl;
+            }
+        }
+        if (lane == 31) {
+            wsum[w] = gi;
+            lsum[w] = li;
+        }
+        gx = gi - hc;
+        lbase[tid] = li - my_count;
+    } else if (b < kDirectTiles) {
+        direct_prefix(cnt_g, b, w - kSortWarps, lane, red);
+    }
+    __syncthreads();
+    if (w < kSortWarps) {
+        int32_t lx = lbase[tid];
+        for (int ww = 0; ww < w; ++ww) {
+            gx += wsum[ww];
+            lx += lsum[ww];
+        }
+        lbase[tid] = lx;
+        int32_t run = 0;
+#pragma unroll
+        for (int ww = 0; ww < kSortWarps; ++ww) {
+            const int32_t c = cnt[ww][tid];
+            cnt[ww][tid] = run;
+            run += c;
+        }
+    } else {
+        const int d = tid - kSortThreads;
+        const int32_t mine = __ldcg(&cnt_g[static_cast<int64_t>(b) * kDigits + d]);
+        int32_t excl = 0;
+        if (b < kDirectTiles) {
+#pragma unroll
+            for (int v = 0; v < kSortWarps; ++v) excl += red[v][d];
+            asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(incl_g + static_cast<int64_t>(b) * kDigits + d),
+                         "r"(kPublished | (excl + mine))
+                         : "memory");
+        } else {
+            LookWin L;
+            look_load(L, cnt_g, incl_g, b - 1, d);
+            excl = look_finish(L, cnt_g, incl_g, b, d, mine);
+        }
+        excl_s[d] = excl;
+    }
+    __syncthreads();
+    if (w < kSortWarps) {
+        gbase[tid] = gx + excl_s[tid];
+        // the tile in digit order in shared memory
+#pragma unroll
+        for (int r = 0; r < kSortItems; ++r) {
             if (key[r] < 0) continue;
-            const int lo = key[r] & 255;
-            const int32_t pos = base[lo] + pre[w][lo] + rank[r];
-            p.perm[pos] = val[r];
-            p.skey[pos] = (p.seg_tile == kSegTile && h[lo] > kSplitMin) ? (key[r] | kSplitBit) : key[r];
+            const int d = pass_digit<PASS>(key[r]);
+            const int32_t lp = lbase[d] + cnt[w][d] + rank[r];
+            sk[lp] = key[r];
+            sv[lp] = val[r];
         }
-        __syncthreads();
-        {
-            int32_t add = 0;
-            for (int ww = 0; ww < kWarps; ++ww) add += cnt[ww][tid];
-            base[tid] += add;
+    }
+    __syncthreads();
+    // each digit's run written out contiguously
+    const int n_here = static_cast<int>(
+        min(static_cast<int64_t>(kSortTile), static_cast<int64_t>(p.N) - static_cast<int64_t>(b) * kSortTile));
+#pragma unroll
+    for (int r = 0; r < kSortTile / kPassThreads; ++r) {
+        const int i = r * kPassThreads + tid;
+        if (i >= n_here) continue;
+        const int32_t k = sk[i];
+        const int d = pass_digit<PASS>(k);
+        const int32_t pos = gbase[d] + (i - lbase[d]);
+        if (PASS == 0) {
+            p.keys_a[pos] = k;
+            p.vals_a[pos] = sv[i];
+            atomicAdd(&p.cnt[tiles + static_cast<int64_t>(pos / kSortTile) * kDigits + (k >> 8)], 1);
+        } else {
+            p.perm[pos] = sv[i];
+            p.skey[pos] = k;
         }
-        __syncthreads();
+    }
+    // pass 0's inclusive words are read no more: clear them for the next call
+    if (PASS == 1 && tid < kDigits) p.incl[static_cast<int64_t>(b) * kDigits + tid] = 0;
+}
+
+// ---------------------------------------------------------------------------
+// segstart: seg_start[] from the key changes of the sorted keys; rows longer
+// than kWarpFoldTiles tiles go on the fold blocks' list (its order is
+// immaterial: each row is folded by one block, the same way). Also clears
+// what the sort passes leave behind for the next call.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kSegStartThreads) segstart_kernel(const IdxParams p) {
+    const int64_t gid = static_cast<int64_t>(blockIdx.x) * kSegStartThreads + threadIdx.x;
+    const int64_t n_threads = static_cast<int64_t>(gridDim.x) * kSegStartThreads;
+    for (int64_t i = gid; i < static_cast<int64_t>(p.nb) * kDigits; i += n_threads) {
+        p.cnt[static_cast<int64_t>(p.nb) * kDigits + i] = 0;   // pass 1's tile counts (added up by pass 0)
+        p.incl[static_cast<int64_t>(p.nb) * kDigits + i] = 0;  // pass 1's inclusive words
+    }
+    if (gid < 2 * kDigits) p.hist[gid] = 0;
+    if (gid < p.N) {
+        const int32_t k = p.skey[gid];
+        const int32_t kp = gid > 0 ? p.skey[gid - 1] : -1;
+        if (k != kp) {
+            for (int32_t j = kp + 1; j <= k; ++j) p.seg_start[j] = static_cast<int32_t>(gid);
+            const int64_t far = gid + static_cast<int64_t>(kWarpFoldTiles) * kSegTile;
+            if (p.seg_tile == kSegTile && far < p.N && p.skey[far] == k)
+                p.heavy_rows[atomicAdd(&p.hdr->pad[3], 1)] = k;
+        }
+        if (gid == p.N - 1)
+            for (int32_t j = k + 1; j <= p.R + 1; ++j) p.seg_start[j] = p.N;
+    }
+    if (gid == 0) {
+        const int32_t bad = atomicAdd(&p.hdr->pad[2], 0);
+        if (p.bad_count) *p.bad_count = bad;
+        p.hdr->pad[2] = 0;
     }
 }
 
 // ---------------------------------------------------------------------------
-// K4: segmented sums.
+// segsum: segmented sums.
 // ---------------------------------------------------------------------------
 
 __device__ __forceinline__ float4 f4add(float4 a, float4 b) {
@@ -411,8 +473,8 @@ __device__ __noinline__ void tile_done(const IdxParams &p, int32_t k, int32_t p0
 
 // Work of 32 consecutive keys, one per lane, cut into groups of gs members
 // (gs = 8, or the tile width when it is smaller) aligned to the row start.
-// An unsplit row is the warp's whole; of a split row the warp takes the tiles
-// whose first member lies in its share [P0, P1).
+// The warp takes an unsplit row whole if it starts in its share [P0, P1), and
+// of a split row the tiles whose first member lies there.
 struct KeyRows {
     int32_t st, L, G, inc;  // first member taken, members taken, groups, inclusive prefix of G
     int32_t ga0, sp;        // group index (within the row) of the first group taken; split row
@@ -435,7 +497,7 @@ __device__ __forceinline__ KeyRows key_rows(int32_t kc, int32_t k_end, int32_t s
     const int32_t L = en - st;
     R.sp = (split_on && L > kSplitMin) ? 1 : 0;
     R.st = st;
-    R.L = L;
+    R.L = (st >= P0 && st < P1) ? L : 0;  // an unsplit row is the warp's if it starts in [P0, P1)
     R.ga0 = 0;
     if (R.sp) {
         const int32_t n_t = (L + kSegTile - 1) / kSegTile;
@@ -689,20 +751,9 @@ __device__ __forceinline__ void consume_group(const IdxParams &p, const float4 *
 // quad (4 groups) ahead; source rows land in the warp's shared-memory ring
 // kStages - 1 groups ahead of the sums.
 __device__ void walk(const IdxParams &p, int32_t P0, int32_t P1, int lane, float4 *ring, int32_t *dring) {
-    int32_t k_first, k_end;
-    {
-        const int32_t s0 = p.skey[P0];
-        const int32_t k0 = s0 & kKeyMask;
-        const int32_t kb = P0 > 0 ? (p.skey[P0 - 1] & kKeyMask) : -1;
-        k_first = (k0 != kb || (s0 & kSplitBit)) ? k0 : k0 + 1;
-        if (P1 < p.N) {
-            const int32_t k1 = p.skey[P1] & kKeyMask;
-            k_end = k1 != (p.skey[P1 - 1] & kKeyMask) ? k1 : k1 + 1;
-        } else {
-            k_end = p.R + 1;
-        }
-    }
-    if (k_first >= k_end) return;
+    // keys from the one at P0 to the one at P1: key_rows keeps what starts in [P0, P1)
+    const int32_t k_first = p.skey[P0];
+    const int32_t k_end = P1 < p.N ? p.skey[P1] + 1 : p.R + 1;
     const int gs = min(8, p.seg_tile);
     const int gpt = p.seg_tile / gs;
     const bool split_on = p.seg_tile == kSegTile;
@@ -844,15 +895,13 @@ __global__ void __launch_bounds__(kSegThreads, 1) segsum_kernel(const IdxParams 
 
 static_assert(2 * kFoldTiles * 32 * 16 <= kSegSmemBytes, "fold stage fits the segsum shared memory");
 struct IdxLayout {
-    int32_t nb, n_buckets, n_pblk, max_fold_rows;
-    size_t keys_a, vals_a, perm, skey, hist, offs, bucket_start, seg_start, tickets, slots;
-    size_t bucket_negmin, bucket_max, bucket_key, heavy, total;
+    int32_t nb, n_pblk, max_fold_rows;
+    size_t keys_a, vals_a, perm, skey, hist, cnt, incl, seg_start, tickets, slots, heavy, total;
 };
 
 IdxLayout idx_layout(int64_t N, int64_t R, int64_t D) {
     IdxLayout L{};
-    L.nb = static_cast<int32_t>((N + kBlockElems - 1) / kBlockElems);
-    L.n_buckets = static_cast<int32_t>((R + 1 + 255) / 256);
+    L.nb = static_cast<int32_t>((N + kSortTile - 1) / kSortTile);
     L.n_pblk = static_cast<int32_t>((N + 127) / 128);
     L.max_fold_rows = static_cast<int32_t>(N / (kWarpFoldTiles * kSegTile + 1) + 1);
     size_t o = sizeof(WsHeader);
@@ -865,15 +914,12 @@ IdxLayout idx_layout(int64_t N, int64_t R, int64_t D) {
     L.vals_a = take(N * 4);
     L.perm = take(N * 4);
     L.skey = take(N * 4);
-    L.hist = take(static_cast<size_t>(kDigits) * L.nb * 4);
-    L.offs = take(static_cast<size_t>(kDigits) * L.nb * 4);
-    L.bucket_start = take((kDigits + 1) * 4);
+    L.hist = take(2 * kDigits * 4);
+    L.cnt = take(static_cast<size_t>(2) * L.nb * kDigits * 4);
+    L.incl = take(static_cast<size_t>(2) * L.nb * kDigits * 4);
     L.seg_start = take((R + 2) * 4);
     L.tickets = take((R + 1) * 4);
     L.slots = take(static_cast<size_t>(L.n_pblk) * 2 * D * 4);
-    L.bucket_negmin = take(kDigits * 4);
-    L.bucket_max = take(kDigits * 4);
-    L.bucket_key = take(kDigits * 4);
     L.heavy = take(static_cast<size_t>(L.max_fold_rows) * 4);
     L.total = o;
     return L;
@@ -925,7 +971,6 @@ extern "C" dgr_status dgr_det_index_add(float *out, int64_t R, int64_t D, int64_
     p.R = static_cast<int32_t>(R);
     p.D = static_cast<int32_t>(D);
     p.nb = L.nb;
-    p.n_buckets = L.n_buckets;
     p.n_pblk = L.n_pblk;
     p.seg_tile = seg_tile;
     p.src = src;
@@ -940,26 +985,22 @@ extern "C" dgr_status dgr_det_index_add(float *out, int64_t R, int64_t D, int64_
     p.perm = reinterpret_cast<int32_t *>(w + L.perm);
     p.skey = reinterpret_cast<int32_t *>(w + L.skey);
     p.hist = reinterpret_cast<int32_t *>(w + L.hist);
-    p.offs = reinterpret_cast<int32_t *>(w + L.offs);
-    p.bucket_start = reinterpret_cast<int32_t *>(w + L.bucket_start);
+    p.cnt = reinterpret_cast<int32_t *>(w + L.cnt);
+    p.incl = reinterpret_cast<int32_t *>(w + L.incl);
     p.seg_start = reinterpret_cast<int32_t *>(w + L.seg_start);
     p.tickets = reinterpret_cast<int32_t *>(w + L.tickets);
     p.slots = reinterpret_cast<float *>(w + L.slots);
-    p.bucket_negmin = reinterpret_cast<int32_t *>(w + L.bucket_negmin);
-    p.bucket_max = reinterpret_cast<int32_t *>(w + L.bucket_max);
-    p.bucket_key = reinterpret_cast<int32_t *>(w + L.bucket_key);
     p.heavy_rows = reinterpret_cast<int32_t *>(w + L.heavy);
-    count_kernel<<<L.nb, kThreads, 0, s>>>(p);
-    scatter_high_kernel<<<L.nb, kThreads, 0, s>>>(p);
-    bucket_kernel<<<L.n_buckets, kThreads, 0, s>>>(p);
-    if (D > 0) {  // persistent: one block per SM, each warp one share of the sorted order
-        int dev = 0, sms = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            cudaFuncSetAttribute(segsum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSegSmemBytes) !=
-                cudaSuccess)
-            return DGR_ERR_CUDA;
-        segsum_kernel<<<static_cast<unsigned>(sms), kSegThreads, kSegSmemBytes, s>>>(p);
-    }
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaFuncSetAttribute(segsum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSegSmemBytes) != cudaSuccess)
+        return DGR_ERR_CUDA;
+    hist_kernel<<<L.nb, kSortThreads, 0, s>>>(p);
+    pass_kernel<0><<<L.nb, kPassThreads, 0, s>>>(p);
+    pass_kernel<1><<<L.nb, kPassThreads, 0, s>>>(p);
+    segstart_kernel<<<static_cast<unsigned>((N + kSegStartThreads - 1) / kSegStartThreads), kSegStartThreads, 0, s>>>(p);
+    // persistent: one block per SM, each warp one share of the sorted order
+    if (D > 0) segsum_kernel<<<static_cast<unsigned>(sms), kSegThreads, kSegSmemBytes, s>>>(p);
     return launch_status();
 }
