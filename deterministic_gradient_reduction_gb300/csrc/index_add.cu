@@ -79,6 +79,13 @@ __device__ __forceinline__ unsigned lanemask_lt() {
     return m;
 }
 
+// Programmatic dependent launch: the next launch of the call may start its
+// blocks early (launch_dependents); a launch reads what the previous one
+// wrote only after grid_dep_wait, which returns once that launch has
+// completed and its writes are visible.
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------
 // hist: global digit histograms of the two passes, and the bad-index count.
 // ---------------------------------------------------------------------------
@@ -86,6 +93,7 @@ __global__ void __launch_bounds__(kSortThreads) hist_kernel(const IdxParams p) {
     __shared__ int32_t h[2][kDigits];
     __shared__ int32_t bad_block;
     const int tid = threadIdx.x;
+    launch_dependents();
     h[0][tid] = 0;
     h[1][tid] = 0;
     if (tid == 0) bad_block = 0;
@@ -244,6 +252,8 @@ __global__ void __launch_bounds__(kPassThreads) pass_kernel(const IdxParams p) {
     const int32_t *cnt_g = p.cnt + PASS * tiles;
     int32_t *incl_g = p.incl + PASS * tiles;
     for (int q = tid; q < kSortWarps * kDigits; q += kPassThreads) (&cnt[0][0])[q] = 0;
+    launch_dependents();
+    grid_dep_wait();
     __syncthreads();
     int32_t key[kSortItems], val[kSortItems], rank[kSortItems];
     int32_t gx = 0, my_count = 0;
@@ -376,6 +386,8 @@ __global__ void __launch_bounds__(kPassThreads) pass_kernel(const IdxParams p) {
 __global__ void __launch_bounds__(kSegStartThreads) segstart_kernel(const IdxParams p) {
     const int64_t gid = static_cast<int64_t>(blockIdx.x) * kSegStartThreads + threadIdx.x;
     const int64_t n_threads = static_cast<int64_t>(gridDim.x) * kSegStartThreads;
+    launch_dependents();
+    grid_dep_wait();
     for (int64_t i = gid; i < static_cast<int64_t>(p.nb) * kDigits; i += n_threads) {
         p.cnt[static_cast<int64_t>(p.nb) * kDigits + i] = 0;   // pass 1's tile counts (added up by pass 0)
         p.incl[static_cast<int64_t>(p.nb) * kDigits + i] = 0;  // pass 1's inclusive words
@@ -875,6 +887,7 @@ __device__ void fold_rows(const IdxParams &p, int first, int stride, int n_rows,
 __global__ void __launch_bounds__(kSegThreads, 1) segsum_kernel(const IdxParams p) {
     extern __shared__ __align__(16) float4 seg_smem[];
     const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
+    grid_dep_wait();
     const int n_fold_rows = p.seg_tile == kSegTile ? p.hdr->pad[3] : 0;
     const int n_fold = min(n_fold_rows, min(kMaxFoldBlocks, static_cast<int>(gridDim.x) - 1));
     if (static_cast<int>(blockIdx.x) < n_fold) {
@@ -923,6 +936,24 @@ IdxLayout idx_layout(int64_t N, int64_t R, int64_t D) {
     L.heavy = take(static_cast<size_t>(L.max_fold_rows) * 4);
     L.total = o;
     return L;
+}
+
+// Launch that may overlap the previous launch's tail on the stream (the kernel
+// waits for it with grid_dep_wait before touching its results).
+template <typename Kernel>
+cudaError_t launch_after(Kernel kernel, unsigned grid, unsigned block, size_t smem, cudaStream_t s,
+                         const IdxParams &p) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
 }  // namespace
@@ -997,10 +1028,13 @@ extern "C" dgr_status dgr_det_index_add(float *out, int64_t R, int64_t D, int64_
         cudaFuncSetAttribute(segsum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSegSmemBytes) != cudaSuccess)
         return DGR_ERR_CUDA;
     hist_kernel<<<L.nb, kSortThreads, 0, s>>>(p);
-    pass_kernel<0><<<L.nb, kPassThreads, 0, s>>>(p);
-    pass_kernel<1><<<L.nb, kPassThreads, 0, s>>>(p);
-    segstart_kernel<<<static_cast<unsigned>((N + kSegStartThreads - 1) / kSegStartThreads), kSegStartThreads, 0, s>>>(p);
+    if (launch_after(pass_kernel<0>, L.nb, kPassThreads, 0, s, p) != cudaSuccess ||
+        launch_after(pass_kernel<1>, L.nb, kPassThreads, 0, s, p) != cudaSuccess ||
+        launch_after(segstart_kernel, static_cast<unsigned>((N + kSegStartThreads - 1) / kSegStartThreads),
+                     kSegStartThreads, 0, s, p) != cudaSuccess)
+        return DGR_ERR_CUDA;
     // persistent: one block per SM, each warp one share of the sorted order
-    if (D > 0) segsum_kernel<<<static_cast<unsigned>(sms), kSegThreads, kSegSmemBytes, s>>>(p);
+    if (D > 0 && launch_after(segsum_kernel, static_cast<unsigned>(sms), kSegThreads, kSegSmemBytes, s, p) != cudaSuccess)
+        return DGR_ERR_CUDA;
     return launch_status();
 }
