@@ -304,20 +304,18 @@ __global__ void __launch_bounds__(kThreadsW, 1)
             float *xt = xpose + (warp - 4) * 32 * 33;
             const int64_t row0 = static_cast<int64_t>(e) * p.N + nb * BM + 32 * q;
             float *mg = p.main_grad + row0 * p.K + kb * BN + 128 * h + lane;
+            // slice j (32 rows x 32 columns): all 32 reads in flight
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) xt[lane * 33 + i] = F[32 * j + i];
                 __syncwarp();
-                float m[16];
+                float m[32];
 #pragma unroll
-                for (int r0 = 0; r0 < 32; r0 += 16) {
+                for (int r = 0; r < 32; ++r) m[r] = mg[static_cast<int64_t>(r) * p.K + 32 * j];
 #pragma unroll
-                    for (int r = 0; r < 16; ++r) m[r] = mg[static_cast<int64_t>(r0 + r) * p.K + 32 * j];
-#pragma unroll
-                    for (int r = 0; r < 16; ++r)
-                        mg[static_cast<int64_t>(r0 + r) * p.K + 32 * j] = __fadd_rn(m[r], xt[(r0 + r) * 33 + lane]);
-                }
+                for (int r = 0; r < 32; ++r)
+                    mg[static_cast<int64_t>(r) * p.K + 32 * j] = __fadd_rn(m[r], xt[r * 33 + lane]);
                 __syncwarp();
             }
         }
