@@ -217,14 +217,27 @@ __device__ void produce(const ColsumParams &p, int unit, float *sm) {
 // between row groups at lane distance V, 2V, ... - aligned windows, so the
 // tree is exactly the canonical one, with no shared memory and no block
 // barrier. Lanes of row group 0 then hold the tile partial.
+// The tile's slot row is written here; its fence and ready count are left
+// to the caller (publish_tile), which issues them once the warp's next tile
+// has its first loads in flight, so the fence's wait overlaps theirs.
+// `pending` is the warp's previous unpublished tile (-1: none).
+__device__ __forceinline__ void publish_tile(const ColsumParams &p, int pending) {
+    __threadfence();  // this lane's slot-row writes before the count
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) atomicAdd(&p.counters[pending / kGroupTiles], 1);
+}
+
 template <int DT, int VE, int RPL>
-__device__ __forceinline__ void produce_warp_tile(const ColsumParams &p, int64_t wunit) {
+__device__ __forceinline__ void produce_warp_tile(const ColsumParams &p, int64_t wunit, int pending) {
     using E = Elem<DT>;
     constexpr int BATCH = RPL < 8 ? RPL : 8;
     constexpr int NB = RPL / BATCH;  // batches, a power of two <= 16
     constexpr int LV = NB >= 16 ? 4 : NB >= 8 ? 3 : NB >= 4 ? 2 : NB >= 2 ? 1 : 0;
     const int lane = threadIdx.x & 31;
-    if (wunit >= p.n_tiles) return;
+    if (wunit >= p.n_tiles) {
+        if (pending >= 0) publish_tile(p, pending);
+        return;
+    }
     const int j = static_cast<int>(wunit);
     const int V = p.V;
     const int g = lane / V;
@@ -246,6 +259,7 @@ __device__ __forceinline__ void produce_warp_tile(const ColsumParams &p, int64_t
                 raw[r] = ldg_nc_v4(p.x + (token_offset(p, t) + c0) * E::kSize);
             }
         }
+        if (bi == 0 && pending >= 0) publish_tile(p, pending);
         // the batch's subtree (rows rb .. rb+BATCH-1), absent rows skipped;
         // level 1 is taken while widening, pair by pair
         const int nb_rows = max(0, min(BATCH, nrows - rb));
@@ -326,10 +340,7 @@ __device__ __forceinline__ void produce_warp_tile(const ColsumParams &p, int64_t
         for (int e = 0; e < VE; ++e) {
             p.slots[slot_index(p, c0 + e, j)] = acc[e];
         }
-        __threadfence();
     }
-    __syncwarp();
-    if (lane == 0) atomicAdd(&p.counters[j / kGroupTiles], 1);
 }
 
 // One folder CTA: columns [f*FC, f*FC + FC), all tiles in ascending order.
@@ -474,9 +485,13 @@ __global__ void __launch_bounds__(kWarpThreads, 1) colsum_warp_kernel(const Cols
     } else {
         const int64_t wpc = kWarpThreads / 32;
         const int64_t n_warps = static_cast<int64_t>(gridDim.x - p.n_fcb) * wpc;
+        int pending = -1;
         for (int64_t w = static_cast<int64_t>(blockIdx.x - p.n_fcb) * wpc + (threadIdx.x >> 5); w < p.n_tiles;
-             w += n_warps)
-            produce_warp_tile<DT, VE, RPL>(p, w);
+             w += n_warps) {
+            produce_warp_tile<DT, VE, RPL>(p, w, pending);
+            pending = static_cast<int>(w);
+        }
+        if (pending >= 0) publish_tile(p, pending);
     }
 }
 
