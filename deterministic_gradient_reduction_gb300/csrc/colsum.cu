@@ -227,10 +227,12 @@ __device__ __forceinline__ void publish_tile(const ColsumParams &p, int pending)
     if ((threadIdx.x & 31) == 0) atomicAdd(&p.counters[pending / kGroupTiles], 1);
 }
 
-template <int DT, int VE, int RPL>
+// MAXB: raw 16-byte loads a lane keeps in flight (a batch); the tree is the
+// same for any batch size (batches are aligned subtrees of the tile).
+template <int DT, int VE, int RPL, int MAXB = 8>
 __device__ __forceinline__ void produce_warp_tile(const ColsumParams &p, int64_t wunit, int pending) {
     using E = Elem<DT>;
-    constexpr int BATCH = RPL < 8 ? RPL : 8;
+    constexpr int BATCH = RPL < MAXB ? RPL : MAXB;
     constexpr int NB = RPL / BATCH;  // batches, a power of two <= 16
     constexpr int LV = NB >= 16 ? 4 : NB >= 8 ? 3 : NB >= 4 ? 2 : NB >= 2 ? 1 : 0;
     const int lane = threadIdx.x & 31;
@@ -495,6 +497,50 @@ __global__ void __launch_bounds__(kWarpThreads, 1) colsum_warp_kernel(const Cols
     }
 }
 
+// Small inputs (at most kSmallTiles tiles): one warp per tile writes its
+// slot row and takes an integer ticket; the warp that takes the last ticket
+// folds every column over the tiles in ascending order and writes out. No
+// folder CTA, no waiting.
+constexpr int kSmallTiles = 512;
+constexpr int kSmallWarps = 4;
+
+template <int DT, int VE, int RPL>
+__global__ void __launch_bounds__(kSmallWarps * 32) colsum_small_kernel(const ColsumParams p) {
+    const int lane = threadIdx.x & 31;
+    const int w = static_cast<int>(blockIdx.x) * kSmallWarps + (threadIdx.x >> 5);
+    if (w >= p.n_tiles) return;
+    produce_warp_tile<DT, VE, RPL, 16>(p, w, -1);
+    __threadfence();  // this lane's slot-row writes before the ticket
+    __syncwarp();
+    int t = 0;
+    if (lane == 0) t = atomicAdd(&p.hdr->pad[0], 1);
+    t = __shfl_sync(0xffffffffu, t, 0);
+    if (t != p.n_tiles - 1) return;
+    __threadfence();  // every other warp's slot rows are visible after its ticket
+    const int n4 = (p.n_tiles + 3) / 4;  // 16-byte groups of 4 tiles per column (the stride is padded to 4)
+    for (int c = lane; c < p.H; c += 32) {
+        const float4 *s4 = reinterpret_cast<const float4 *>(p.slots + slot_index(p, c, 0));
+        float F = 0.0f;
+        for (int q0 = 0; q0 < n4; q0 += 8) {
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (q0 + u < n4) v[u] = __ldcg(s4 + q0 + u);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (q0 + u >= n4) break;
+                const int k = 4 * (q0 + u);
+                const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (k + i < p.n_tiles) F = (k + i == 0) ? e[i] : __fadd_rn(F, e[i]);
+            }
+        }
+        p.out[c] = p.accumulate ? __fadd_rn(p.out[c], F) : F;
+    }
+    if (lane == 0) p.hdr->pad[0] = 0;
+}
+
 template <int DT, int VE, int RPT>
 dgr_status launch_one(const ColsumParams &p, int grid, size_t smem, cudaStream_t st) {
     colsum_kernel<DT, VE, RPT><<<grid, kThreads, smem, st>>>(p);
@@ -520,6 +566,26 @@ dgr_status launch_warp_one(const ColsumParams &p, int grid, cudaStream_t st) {
         return DGR_ERR_CUDA;
     colsum_warp_kernel<DT, VE, RPL><<<grid, kWarpThreads, kWarpSmemBytes, st>>>(p);
     return launch_status();
+}
+
+template <int DT, int VE, int RPL>
+dgr_status launch_small_one(const ColsumParams &p, cudaStream_t st) {
+    colsum_small_kernel<DT, VE, RPL><<<(p.n_tiles + kSmallWarps - 1) / kSmallWarps, kSmallWarps * 32, 0, st>>>(p);
+    return launch_status();
+}
+
+template <int DT, int VE>
+dgr_status launch_small(const ColsumParams &p, int rpl, cudaStream_t st) {
+    switch (rpl) {
+        case 2: return launch_small_one<DT, VE, 2>(p, st);
+        case 4: return launch_small_one<DT, VE, 4>(p, st);
+        case 8: return launch_small_one<DT, VE, 8>(p, st);
+        case 16: return launch_small_one<DT, VE, 16>(p, st);
+        case 32: return launch_small_one<DT, VE, 32>(p, st);
+        case 64: return launch_small_one<DT, VE, 64>(p, st);
+        case 128: return launch_small_one<DT, VE, 128>(p, st);
+        default: return DGR_ERR_INVALID_ARG;
+    }
 }
 
 template <int DT, int VE>
@@ -665,6 +731,11 @@ extern "C" dgr_status dgr_ordered_colsum(const void *x, int32_t dtype, int64_t B
     }
     const int64_t grid = static_cast<int64_t>(p.n_fcb) + n_prod_ctas;
     if (grid > INT32_MAX) return DGR_ERR_UNSUPPORTED;
+    if (p.stream_mode && p.n_tiles <= kSmallTiles) {
+        p.n_pcb = 1;
+        if (dtype == DGR_DTYPE_BF16) return launch_small<DGR_DTYPE_BF16, 8>(p, rpl, s);
+        return launch_small<DGR_DTYPE_F32, 4>(p, rpl, s);
+    }
     if (p.stream_mode) {
         p.n_pcb = 1;
         if (dtype == DGR_DTYPE_BF16) return launch_warp<DGR_DTYPE_BF16, 8>(p, rpl, static_cast<int>(grid), s);
