@@ -54,7 +54,7 @@ ALGO = {
     "wgrad_flop": 2 * 4096 * 2048 * 32768,
     "wgrad": 32768 * 4096 * 2 + 32768 * 2048 * 2 + 2 * 8 * 4096 * 2048 * 4,
 }
-LAUNCHES = {"colsum_large": 1, "colsum_small": 1, "dprob": 1, "colsum_strided": 1, "index_add": 5, "wgrad": 1}
+LAUNCHES = {"colsum_large": 1, "colsum_small": 1, "dprob": 1, "colsum_strided": 1, "index_add": 4, "wgrad": 1}
 
 WORKLOAD = ("deterministic reduction step: colsum bf16 8388608x64 + colsum bf16 2048x16 + dprob bf16 "
             "65536x4096 + colsum bf16 4x2048x64 (token stride 128) + index_add fp32 262144x128 -> 16385 rows "

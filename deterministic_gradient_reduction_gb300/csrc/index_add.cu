@@ -3,11 +3,12 @@
 //
 // Megatron-LM PR #7441 (DSv4 --deterministic-mode), Source 3: the atomic-free
 // dK is an index_add done as a stable sort plus a (prefix) sum, with padding
-// slots spread over dummy rows that the caller drops. Five launches:
+// slots spread over dummy rows that the caller drops. Four launches:
 //   hist     - map idx to keys (idx outside [0, R) -> R; outside [-1, R) is
 //              counted); each 2048-element tile stores its low-byte digit
-//              counts and adds its low- and high-byte histograms to the
-//              global ones (integer atomics).
+//              counts and adds its low- and high-byte histograms and its
+//              per-key counts to the global ones (integer atomics; the
+//              padding key R summed in the block first).
 //   pass 0/1 - stable LSD radix passes by the low, then the high byte. Each
 //              tile ranks its elements in original order with warp
 //              match/ballot and per-warp digit counters; a digit's offset is
@@ -16,11 +17,10 @@
 //              published its inclusive count. Every count is there before the
 //              pass starts (pass 0 adds, per element, to the digit counts of
 //              the pass-1 tile it lands in), so nothing waits. Pass 1 writes
-//              the sorted keys and the permutation.
-//   segstart - segment starts from the key changes of the sorted keys, and
-//              the list of rows longer than 32 tiles.
-// Every scratch word a launch leaves non-zero is cleared by a later launch of
-// the same call, so a workspace zeroed once serves every call.
+//              the sorted keys and the permutation. Its first tiles also
+//              turn the per-key counts into seg_start[], one 256-key bucket
+//              each (the bucket's base from the high-byte histogram plus a
+//              scan of its keys' counts), and list rows longer than 32 tiles.
 //   segsum   - persistent warps, each an equal share of the sorted order: the
 //              rows starting in the share as one stream of 8-member groups,
 //              summed by the pairwise tree over tiles of 128 members and
@@ -29,6 +29,9 @@
 //              go to slots and are folded in order by the warp completing the
 //              last tile (an integer ticket) or, for rows longer than 32
 //              tiles, by a fold block.
+// Every scratch word a launch leaves non-zero is cleared by a later launch of
+// the same call (segsum clears the sort's counters, even with no columns), so
+// a workspace zeroed once serves every call.
 // Integer atomics only count or hand out tile numbers; no floating-point
 // value depends on timing.
 #include "dgr_common.cuh"
@@ -45,12 +48,12 @@ constexpr int kSegTile = 128;
 constexpr int kSplitMin = kSegTile;    // rows longer than one tile are split by tile
 constexpr int kWarpFoldTiles = 32;     // split rows up to 32 tiles: folded by one warp
 constexpr int kMaxFoldBlocks = 16;     // longer rows: folded by up to 16 fold blocks
-constexpr int kSegStartThreads = 256;
 
 struct IdxParams {
     const int32_t *idx;
     int32_t N, R, D;
-    int32_t nb;      // sort tiles
+    int32_t nb;         // sort tiles
+    int32_t n_buckets;  // 256-key buckets of the keys 0..R (segment starts, one pass-1 block each)
     int32_t n_pblk;  // 128-position blocks of the sorted order (slot indexing)
     int32_t seg_tile;
     const float *src;
@@ -60,6 +63,7 @@ struct IdxParams {
     int32_t *bad_count;
     int32_t *keys_a, *vals_a, *perm, *skey, *seg_start, *tickets;
     int32_t *hist;               // [2][256] global digit histograms (low byte, high byte)
+    int32_t *count;              // [R + 1] elements per key
     int32_t *cnt;                // [2][nb][256] per-tile digit counts of the two passes
     int32_t *incl;               // [2][nb][256] published inclusive counts (bit 31: published)
     int32_t *heavy_rows;         // split rows longer than kWarpFoldTiles tiles (fold-block work)
@@ -91,12 +95,15 @@ __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.w
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kSortThreads) hist_kernel(const IdxParams p) {
     __shared__ int32_t h[2][kDigits];
-    __shared__ int32_t bad_block;
+    __shared__ int32_t bad_block, pad_block;
     const int tid = threadIdx.x;
     launch_dependents();
     h[0][tid] = 0;
     h[1][tid] = 0;
-    if (tid == 0) bad_block = 0;
+    if (tid == 0) {
+        bad_block = 0;
+        pad_block = 0;
+    }
     if (blockIdx.x == 0 && tid == 0) p.hdr->pad[3] = 0;  // fold-row list of this call starts empty
     __syncthreads();
     int32_t v[kSortItems];
@@ -116,9 +123,12 @@ __global__ void __launch_bounds__(kSortThreads) hist_kernel(const IdxParams p) {
         my_bad += bad ? 1 : 0;
         atomicAdd(&h[0][k & 255], 1);
         atomicAdd(&h[1][k >> 8], 1);
+        if (k == p.R) atomicAdd(&pad_block, 1);
+        else atomicAdd(&p.count[k], 1);
     }
     if (my_bad) atomicAdd(&bad_block, my_bad);
     __syncthreads();
+    if (tid == 0 && pad_block) atomicAdd(&p.count[p.R], pad_block);
     p.cnt[static_cast<int64_t>(blockIdx.x) * kDigits + tid] = h[0][tid];
     if (h[0][tid]) atomicAdd(&p.hist[tid], h[0][tid]);
     if (h[1][tid]) atomicAdd(&p.hist[kDigits + tid], h[1][tid]);
@@ -240,23 +250,29 @@ template <int PASS>
 __global__ void __launch_bounds__(kPassThreads) pass_kernel(const IdxParams p) {
     __shared__ int32_t cnt[kSortWarps][kDigits];
     __shared__ int32_t red[kSortWarps][kDigits];
-    __shared__ int32_t gbase[kDigits];  // global position of this tile's first element of each digit
-    __shared__ int32_t lbase[kDigits];  // local position of the same
+    __shared__ int32_t gbase[kDigits];    // global position of this tile's first element of each digit
+    __shared__ int32_t lbase[kDigits];    // local position of the same
     __shared__ int32_t excl_s[kDigits];
+    __shared__ int32_t dbase_s[kDigits];  // global position of each digit's first element
     __shared__ int32_t wsum[kSortWarps];
     __shared__ int32_t lsum[kSortWarps];
+    __shared__ int32_t csum[kSortWarps];
     __shared__ int32_t sk[kSortTile], sv[kSortTile];
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     const int32_t b = blockIdx.x;
     const int64_t tiles = static_cast<int64_t>(p.nb) * kDigits;
     const int32_t *cnt_g = p.cnt + PASS * tiles;
     int32_t *incl_g = p.incl + PASS * tiles;
+    // pass 1's first n_buckets tiles also own the segment starts of bucket b
+    const bool seg_owner = PASS == 1 && b < p.n_buckets;
+    const bool sort_tile = b < p.nb;  // pass 1 may have more blocks than tiles (more buckets)
     for (int q = tid; q < kSortWarps * kDigits; q += kPassThreads) (&cnt[0][0])[q] = 0;
     launch_dependents();
     grid_dep_wait();
     __syncthreads();
     int32_t key[kSortItems], val[kSortItems], rank[kSortItems];
     int32_t gx = 0, my_count = 0;
+    int32_t kc = 0, kx = 0;  // prefix warps of a segment-start owner: the key's count, warp prefix
     if (w < kSortWarps) {
         // ranking warps: warp w owns elements [b*2048 + w*256, +256) in 8 rounds of 32
         const int64_t e0 = static_cast<int64_t>(b) * kSortTile + w * (kSortItems * 32) + lane;
@@ -273,7 +289,7 @@ __global__ void __launch_bounds__(kPassThreads) pass_kernel(const IdxParams p) {
             }
         }
         const int32_t hc = __ldcg(&p.hist[PASS * kDigits + tid]);
-        my_count = __ldcg(&cnt_g[static_cast<int64_t>(b) * kDigits + tid]);
+        if (sort_tile) my_count = __ldcg(&cnt_g[static_cast<int64_t>(b) * kDigits + tid]);
 #pragma unroll
         for (int r = 0; r < kSortItems; ++r) {
             const int64_t e = e0 + r * 32;
@@ -305,8 +321,20 @@ __global__ void __launch_bounds__(kPassThreads) pass_kernel(const IdxParams p) {
         }
         gx = gi - hc;
         lbase[tid] = li - my_count;
-    } else if (b < kDirectTiles) {
-        direct_prefix(cnt_g, b, w - kSortWarps, lane, red);
+    } else {
+        if (seg_owner) {  // the counts of keys 256b .. 256b + 255, scanned within each warp
+            const int32_t k = b * kDigits + (tid - kSortThreads);
+            if (k <= p.R) kc = __ldcg(&p.count[k]);
+            int32_t ci = kc;
+#pragma unroll
+            for (int s = 1; s < 32; s <<= 1) {
+                const int32_t tv = __shfl_up_sync(0xffffffffu, ci, s);
+                if (lane >= s) ci += tv;
+            }
+            if (lane == 31) csum[w - kSortWarps] = ci;
+            kx = ci - kc;
+        }
+        if (sort_tile && b < kDirectTiles) direct_prefix(cnt_g, b, w - kSortWarps, lane, red);
     }
     __syncthreads();
     if (w < kSortWarps) {
@@ -316,6 +344,7 @@ __global__ void __launch_bounds__(kPassThreads) pass_kernel(const IdxParams p) {
             lx += lsum[ww];
         }
         lbase[tid] = lx;
+        dbase_s[tid] = gx;
         int32_t run = 0;
 #pragma unroll
         for (int ww = 0; ww < kSortWarps; ++ww) {
@@ -325,9 +354,10 @@ __global__ void __launch_bounds__(kPassThreads) pass_kernel(const IdxParams p) {
         }
     } else {
         const int d = tid - kSortThreads;
-        const int32_t mine = __ldcg(&cnt_g[static_cast<int64_t>(b) * kDigits + d]);
+        const int32_t mine = sort_tile ? __ldcg(&cnt_g[static_cast<int64_t>(b) * kDigits + d]) : 0;
         int32_t excl = 0;
-        if (b < kDirectTiles) {
+        if (!sort_tile) {
+        } else if (b < kDirectTiles) {
 #pragma unroll
             for (int v = 0; v < kSortWarps; ++v) excl += red[v][d];
             asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(incl_g + static_cast<int64_t>(b) * kDigits + d),
@@ -339,6 +369,8 @@ __global__ void __launch_bounds__(kPassThreads) pass_kernel(const IdxParams p) {
             excl = look_finish(L, cnt_g, incl_g, b, d, mine);
         }
         excl_s[d] = excl;
+        if (seg_owner)
+            for (int ww = 0; ww < w - kSortWarps; ++ww) kx += csum[ww];
     }
     __syncthreads();
     if (w < kSortWarps) {
@@ -351,6 +383,23 @@ __global__ void __launch_bounds__(kPassThreads) pass_kernel(const IdxParams p) {
             const int32_t lp = lbase[d] + cnt[w][d] + rank[r];
             sk[lp] = key[r];
             sv[lp] = val[r];
+        }
+    } else if (seg_owner) {
+        // segment starts of bucket b: the bucket's first position plus the
+        // counts of its smaller keys; its long rows go on the fold-block list
+        // (in any order: each row is folded by one block, the same way)
+        const int32_t k = b * kDigits + (tid - kSortThreads);
+        if (k <= p.R) {
+            p.seg_start[k] = dbase_s[b] + kx;
+            if (k == p.R) p.seg_start[p.R + 1] = p.N;
+            if (p.seg_tile == kSegTile && kc > kWarpFoldTiles * kSegTile)
+                p.heavy_rows[atomicAdd(&p.hdr->pad[3], 1)] = k;
+            p.count[k] = 0;  // read no more: cleared for the next call
+        }
+        if (b == 0 && tid == kSortThreads) {  // every hist block has counted by now
+            const int32_t bad = atomicAdd(&p.hdr->pad[2], 0);
+            if (p.bad_count) *p.bad_count = bad;
+            p.hdr->pad[2] = 0;
         }
     }
     __syncthreads();
@@ -374,42 +423,7 @@ __global__ void __launch_bounds__(kPassThreads) pass_kernel(const IdxParams p) {
         }
     }
     // pass 0's inclusive words are read no more: clear them for the next call
-    if (PASS == 1 && tid < kDigits) p.incl[static_cast<int64_t>(b) * kDigits + tid] = 0;
-}
-
-// ---------------------------------------------------------------------------
-// segstart: seg_start[] from the key changes of the sorted keys; rows longer
-// than kWarpFoldTiles tiles go on the fold blocks' list (its order is
-// immaterial: each row is folded by one block, the same way). Also clears
-// what the sort passes leave behind for the next call.
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kSegStartThreads) segstart_kernel(const IdxParams p) {
-    const int64_t gid = static_cast<int64_t>(blockIdx.x) * kSegStartThreads + threadIdx.x;
-    const int64_t n_threads = static_cast<int64_t>(gridDim.x) * kSegStartThreads;
-    launch_dependents();
-    grid_dep_wait();
-    for (int64_t i = gid; i < static_cast<int64_t>(p.nb) * kDigits; i += n_threads) {
-        p.cnt[static_cast<int64_t>(p.nb) * kDigits + i] = 0;   // pass 1's tile counts (added up by pass 0)
-        p.incl[static_cast<int64_t>(p.nb) * kDigits + i] = 0;  // pass 1's inclusive words
-    }
-    if (gid < 2 * kDigits) p.hist[gid] = 0;
-    if (gid < p.N) {
-        const int32_t k = p.skey[gid];
-        const int32_t kp = gid > 0 ? p.skey[gid - 1] : -1;
-        if (k != kp) {
-            for (int32_t j = kp + 1; j <= k; ++j) p.seg_start[j] = static_cast<int32_t>(gid);
-            const int64_t far = gid + static_cast<int64_t>(kWarpFoldTiles) * kSegTile;
-            if (p.seg_tile == kSegTile && far < p.N && p.skey[far] == k)
-                p.heavy_rows[atomicAdd(&p.hdr->pad[3], 1)] = k;
-        }
-        if (gid == p.N - 1)
-            for (int32_t j = k + 1; j <= p.R + 1; ++j) p.seg_start[j] = p.N;
-    }
-    if (gid == 0) {
-        const int32_t bad = atomicAdd(&p.hdr->pad[2], 0);
-        if (p.bad_count) *p.bad_count = bad;
-        p.hdr->pad[2] = 0;
-    }
+    if (PASS == 1 && sort_tile && tid < kDigits) p.incl[static_cast<int64_t>(b) * kDigits + tid] = 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -888,6 +902,16 @@ __global__ void __launch_bounds__(kSegThreads, 1) segsum_kernel(const IdxParams 
     extern __shared__ __align__(16) float4 seg_smem[];
     const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
     grid_dep_wait();
+    {  // what the sort passes leave behind, cleared for the next call
+        const int64_t tiles = static_cast<int64_t>(p.nb) * kDigits;
+        const int64_t g = static_cast<int64_t>(blockIdx.x) * kSegThreads + threadIdx.x;
+        for (int64_t i = g; i < tiles; i += static_cast<int64_t>(gridDim.x) * kSegThreads) {
+            p.cnt[tiles + i] = 0;   // pass 1's tile counts (added up by pass 0)
+            p.incl[tiles + i] = 0;  // pass 1's inclusive words
+        }
+        if (g < 2 * kDigits) p.hist[g] = 0;
+    }
+    if (p.D == 0) return;
     const int n_fold_rows = p.seg_tile == kSegTile ? p.hdr->pad[3] : 0;
     const int n_fold = min(n_fold_rows, min(kMaxFoldBlocks, static_cast<int>(gridDim.x) - 1));
     if (static_cast<int>(blockIdx.x) < n_fold) {
@@ -909,7 +933,7 @@ __global__ void __launch_bounds__(kSegThreads, 1) segsum_kernel(const IdxParams 
 static_assert(2 * kFoldTiles * 32 * 16 <= kSegSmemBytes, "fold stage fits the segsum shared memory");
 struct IdxLayout {
     int32_t nb, n_pblk, max_fold_rows;
-    size_t keys_a, vals_a, perm, skey, hist, cnt, incl, seg_start, tickets, slots, heavy, total;
+    size_t keys_a, vals_a, perm, skey, hist, count, cnt, incl, seg_start, tickets, slots, heavy, total;
 };
 
 IdxLayout idx_layout(int64_t N, int64_t R, int64_t D) {
@@ -928,12 +952,15 @@ IdxLayout idx_layout(int64_t N, int64_t R, int64_t D) {
     L.perm = take(N * 4);
     L.skey = take(N * 4);
     L.hist = take(2 * kDigits * 4);
+    L.count = take((R + 1) * 4);
     L.cnt = take(static_cast<size_t>(2) * L.nb * kDigits * 4);
     L.incl = take(static_cast<size_t>(2) * L.nb * kDigits * 4);
     L.seg_start = take((R + 2) * 4);
     L.tickets = take((R + 1) * 4);
-    L.slots = take(static_cast<size_t>(L.n_pblk) * 2 * D * 4);
     L.heavy = take(static_cast<size_t>(L.max_fold_rows) * 4);
+    // last: the only region whose size depends on D, so a workspace for
+    // (N, R, D) has the layout of (N, R, D') for every D' <= D
+    L.slots = take(static_cast<size_t>(L.n_pblk) * 2 * D * 4);
     L.total = o;
     return L;
 }
@@ -1002,6 +1029,7 @@ extern "C" dgr_status dgr_det_index_add(float *out, int64_t R, int64_t D, int64_
     p.R = static_cast<int32_t>(R);
     p.D = static_cast<int32_t>(D);
     p.nb = L.nb;
+    p.n_buckets = static_cast<int32_t>((R + 1 + kDigits - 1) / kDigits);
     p.n_pblk = L.n_pblk;
     p.seg_tile = seg_tile;
     p.src = src;
@@ -1016,6 +1044,7 @@ extern "C" dgr_status dgr_det_index_add(float *out, int64_t R, int64_t D, int64_
     p.perm = reinterpret_cast<int32_t *>(w + L.perm);
     p.skey = reinterpret_cast<int32_t *>(w + L.skey);
     p.hist = reinterpret_cast<int32_t *>(w + L.hist);
+    p.count = reinterpret_cast<int32_t *>(w + L.count);
     p.cnt = reinterpret_cast<int32_t *>(w + L.cnt);
     p.incl = reinterpret_cast<int32_t *>(w + L.incl);
     p.seg_start = reinterpret_cast<int32_t *>(w + L.seg_start);
@@ -1028,13 +1057,13 @@ extern "C" dgr_status dgr_det_index_add(float *out, int64_t R, int64_t D, int64_
         cudaFuncSetAttribute(segsum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSegSmemBytes) != cudaSuccess)
         return DGR_ERR_CUDA;
     hist_kernel<<<L.nb, kSortThreads, 0, s>>>(p);
+    // pass 1 also has one block per 256-key bucket, where there are more buckets than tiles
+    const unsigned pass1_blocks = static_cast<unsigned>(L.nb > p.n_buckets ? L.nb : p.n_buckets);
+    // segsum (persistent: one block per SM, each warp one share of the sorted
+    // order) runs even without columns: it clears the sort's counters
     if (launch_after(pass_kernel<0>, L.nb, kPassThreads, 0, s, p) != cudaSuccess ||
-        launch_after(pass_kernel<1>, L.nb, kPassThreads, 0, s, p) != cudaSuccess ||
-        launch_after(segstart_kernel, static_cast<unsigned>((N + kSegStartThreads - 1) / kSegStartThreads),
-                     kSegStartThreads, 0, s, p) != cudaSuccess)
-        return DGR_ERR_CUDA;
-    // persistent: one block per SM, each warp one share of the sorted order
-    if (D > 0 && launch_after(segsum_kernel, static_cast<unsigned>(sms), kSegThreads, kSegSmemBytes, s, p) != cudaSuccess)
+        launch_after(pass_kernel<1>, pass1_blocks, kPassThreads, 0, s, p) != cudaSuccess ||
+        launch_after(segsum_kernel, static_cast<unsigned>(sms), kSegThreads, kSegSmemBytes, s, p) != cudaSuccess)
         return DGR_ERR_CUDA;
     return launch_status();
 }

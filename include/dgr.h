@@ -20,8 +20,11 @@
  *   - Workspaces: query the size with the matching *_workspace_bytes() call,
  *     allocate at least that many bytes (256-byte aligned) and ZERO them once
  *     before first use. Every successful call leaves its workspace ready for
- *     the next call (all counters back to zero). One workspace must not be used
- *     by two calls that can run at the same time on the GPU.
+ *     the next call with the same sizes (all counters back to zero); its
+ *     layout depends on the sizes, so before a call with other sizes it must
+ *     be zeroed again (unless the operation's entry allows that change).
+ *     One workspace must not be used by two calls that can run at the same
+ *     time on the GPU.
  *   - Device-side anomalies (a bounded wait that ran out) are recorded in the
  *     workspace's status word, read with dgr_read_device_status(). After such
  *     an error the outputs of that call are unspecified and the workspace must
@@ -173,7 +176,9 @@ dgr_status dgr_ordered_rowdot_dprob(const void *dY, const void *Y, int32_t dtype
  *           of idx entries outside [-1, R); those rows go to the dummy row.
  * Limits:   R + 1 <= 65536, N <= 2^31 - 1, D <= 4096. Rows of out and src
  *           need 16-byte alignment (ld_* and D multiples of 4).
- * ws:       dgr_index_add_workspace_bytes(N, R, D) bytes, zeroed once.
+ * ws:       dgr_index_add_workspace_bytes(N, R, D) bytes, zeroed once; it
+ *           then serves every call with the same N and R and any D' <= D
+ *           (D' = 0 included: the call then only counts bad indices).
  * out must not overlap src, idx, bad_count or ws.
  */
 size_t dgr_index_add_workspace_bytes(int64_t N, int64_t R, int64_t D);

@@ -54,7 +54,10 @@ CASES = [
     (1, 1, 8, None, torch.bfloat16, 128),
     (1, 70000, 520, None, torch.bfloat16, 128),  # several column blocks and folders
     (1, 3000, 4096, None, torch.bfloat16, 128),  # the H limit
-    # contiguous rows and many tiles: the bulk-copy producers
+    # warp producers: up to 512 tiles one launch with a ticket, beyond it folders
+    (1, 65536, 64, None, torch.bfloat16, 128),   # 512 tiles: the ticket path's largest
+    (1, 65537, 64, None, torch.bfloat16, 128),   # 513 tiles: warp producers and folders
+    (4, 16, 8, 24, torch.bfloat16, 128),         # ticket path, strided, one tile across batches
     (1, 100000, 64, None, torch.bfloat16, 128),  # ragged last tile
     (3, 40000, 16, None, torch.bfloat16, 128),
     (1, 50000, 32, None, torch.float32, 128),

@@ -135,3 +135,35 @@ def test_full_workload_and_nondeterministic_control():
         torch.cuda.synchronize()
         patterns.add(hash(o.view(torch.int32).cpu().numpy().tobytes()))
     assert len(patterns) > 1
+
+
+def test_workspace_reused_with_fewer_columns():
+    # a workspace zeroed once for (N, R, D) serves calls of the same N and R
+    # with any D' <= D, in any order; a call with no columns still sorts and
+    # counts, and must leave every counter cleared like any other call
+    for i, (N, D, R) in enumerate([(70000, 128, 60000), (3000, 8, 5000), (20000, 64, 700)]):
+        ws = dgr.workspace(dgr.index_add_workspace_bytes(N, R, D))
+        badc = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+        ia = gi.index_add_input(N, D, R, seed=900 + i, out_init="random")
+        idx = ia.idx.clone()
+        idx[[0, N // 2]] = torch.tensor([R + 5, -3], dtype=torch.int32)
+        ib = gi.IndexAddInput(ia.src, idx, ia.out, R)
+        want, bad = _oracle(ib)
+        half = gi.IndexAddInput(ib.src[:, :D // 2].contiguous(), idx, ib.out[:, :D // 2].contiguous(), R)
+        want_half, _ = _oracle(half)
+        assert bad == 2
+        src, idx_d = ib.src.cuda(), ib.idx.cuda()
+        for rep in range(2):
+            # no columns (through the C ABI: torch gives a zero-element view
+            # a null pointer): only the bad-index count comes out
+            wide = torch.zeros((R + 1, 4), device="cuda")
+            rc = dgr.lib().dgr_det_index_add(wide.data_ptr(), R, 0, 4, src.data_ptr(), D, idx_d.data_ptr(), N, 128,
+                                             badc.data_ptr(), ws.data_ptr(), ws.numel(), None)
+            assert rc == 0
+            assert int(badc.item()) == 2 and torch.count_nonzero(wide) == 0
+            got = _gpu(ib, dev=(src, idx_d, ib.out.cuda()), ws=ws, bad=badc)
+            assert_bits_equal(got.cpu().numpy(), want, f"N={N} D={D} R={R} after a no-column call")
+            assert int(badc.item()) == 2
+            got = _gpu(half, ws=ws)
+            assert_bits_equal(got.cpu().numpy(), want_half, f"N={N} D={D // 2} R={R} in a D={D} workspace")
+        assert dgr.read_device_status(ws) == 0
