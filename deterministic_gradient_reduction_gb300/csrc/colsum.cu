@@ -8,8 +8,8 @@
 //     vector loads, the pairwise tree of the tile (in registers over the rows a
 //     thread owns, then across threads in shared memory, always over aligned
 //     sub-windows so the tree is exactly the canonical one), one FP32 slot row
-//     per tile, then a release increment of the ready counter of its group of
-//     32 tiles;
+//     per tile, then an increment of the ready counter of its group of 32
+//     tiles;
 //   - folder CTAs (the first blockIdx values), one per block of FC columns
 //     (4 for H <= 256, at most 64 folders):
 //     they wait (bounded) for each batch of tiles to be ready, stage the slots
@@ -17,7 +17,12 @@
 //     tile order on one thread per column. The fold overlaps the stream, so a
 //     long dependent chain of adds (65,536 tiles for 1 GiB of bf16 at H = 64)
 //     hides under the HBM time instead of following it.
-// Producers never wait, so the folders' waits always end.
+// Each slot word says itself whether it has been written: a partial is stored
+// as the complement of its bits (0 = empty), and the folder zeroes the words
+// it consumes. So no producer fences its slot writes before the count: the
+// counters only tell the folder when to look, and a word the folder reads
+// before its write has arrived is read again (bounded). Producers never wait,
+// so the folders' waits always end.
 #include "dgr_common.cuh"
 
 namespace dgr {
@@ -89,6 +94,45 @@ struct Elem<DGR_DTYPE_F32> {
 // four consecutive tiles of its column with one 16-byte load.
 __device__ __forceinline__ int64_t slot_index(const ColsumParams &p, int c, int j) {
     return static_cast<int64_t>(c) * p.col_stride + j;
+}
+
+// Slot words: the complement of the partial's bits, so that 0 means "not
+// written yet". The one partial whose complement is 0 (the NaN with every bit
+// set) is stored as the NaN next to it, which can change a NaN's payload and
+// nothing else.
+__device__ __forceinline__ uint32_t slot_word(float v) {
+    const uint32_t w = ~__float_as_uint(v);
+    return w != 0u ? w : 1u;
+}
+__device__ __forceinline__ float slot_value(uint32_t w) { return __uint_as_float(~w); }
+
+__device__ __forceinline__ void st_slot(const ColsumParams &p, int c, int j, float v) {
+    asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p.slots + slot_index(p, c, j)), "r"(slot_word(v))
+                 : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_slot4(const float *a) {
+    uint4 v;
+    asm volatile("ld.relaxed.gpu.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(a)
+                 : "memory");
+    return v;
+}
+
+// The first n (1..4) words of a slot quad, all written: read again until
+// none is 0, at most kWaitLimitNs. Returns false on timeout.
+__device__ __noinline__ bool wait_slot4(const float *a, int n, uint4 &v) {
+    const uint64_t t0 = globaltimer_ns();
+    unsigned ns = 32;
+    while (true) {
+        const bool ready = v.x != 0u && (n < 2 || v.y != 0u) && (n < 3 || v.z != 0u) && (n < 4 || v.w != 0u);
+        if (ready) return true;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        __nanosleep(ns);
+        if (ns < 1024) ns <<= 1;
+        v = ld_slot4(a);
+    }
 }
 
 __device__ __forceinline__ int64_t token_offset(const ColsumParams &p, int32_t t) {
@@ -194,11 +238,8 @@ __device__ void produce(const ColsumParams &p, int unit, float *sm) {
 #pragma unroll
         for (int e = 0; e < VE; ++e) {
             const int c = (cv0 + v) * VE + e;
-            if (c < p.H) {
-                p.slots[slot_index(p, c, j)] = root[e];
-            }
+            if (c < p.H) st_slot(p, c, j, root[e]);
         }
-        __threadfence();
     }
     __syncthreads();
     if (tid == 0) {
@@ -217,12 +258,11 @@ __device__ void produce(const ColsumParams &p, int unit, float *sm) {
 // between row groups at lane distance V, 2V, ... - aligned windows, so the
 // tree is exactly the canonical one, with no shared memory and no block
 // barrier. Lanes of row group 0 then hold the tile partial.
-// The tile's slot row is written here; its fence and ready count are left
-// to the caller (publish_tile), which issues them once the warp's next tile
-// has its first loads in flight, so the fence's wait overlaps theirs.
-// `pending` is the warp's previous unpublished tile (-1: none).
+// The tile's slot row is written here; its ready count is left to the
+// caller (publish_tile), which issues it once the warp's next tile has its
+// first loads in flight. `pending` is the warp's previous unpublished tile
+// (-1: none).
 __device__ __forceinline__ void publish_tile(const ColsumParams &p, int pending) {
-    __threadfence();  // this lane's slot-row writes before the count
     __syncwarp();
     if ((threadIdx.x & 31) == 0) atomicAdd(&p.counters[pending / kGroupTiles], 1);
 }
@@ -339,9 +379,7 @@ __device__ __forceinline__ void produce_warp_tile(const ColsumParams &p, int64_t
     }
     if (g == 0) {
 #pragma unroll
-        for (int e = 0; e < VE; ++e) {
-            p.slots[slot_index(p, c0 + e, j)] = acc[e];
-        }
+        for (int e = 0; e < VE; ++e) st_slot(p, c0 + e, j, acc[e]);
     }
 }
 
@@ -380,14 +418,32 @@ __device__ void fold(const ColsumParams &p, int f, float *sm) {
         }
         asm volatile("bar.sync 1, %0;" ::"r"(loader_threads) : "memory");
         if (abort_flag) return;
+        // the counts said the batch is written: its words are read (again,
+        // bounded, where one has not arrived yet), decoded into shared memory
+        // and zeroed for the next call
         const int q4 = (j1 - j0 + 3) / 4;  // float4 per column (the column stride is padded to 4)
         const int n4 = q4 * p.FC;
         float4 *d4 = reinterpret_cast<float4 *>(sm + (i & 1) * p.batch * p.FC);
+        bool ok = true;
         for (int q = ltid; q < n4; q += loader_threads) {
             const int cc = q / q4;
             const int k4 = q - cc * q4;
-            const float4 *s4 = reinterpret_cast<const float4 *>(p.slots + slot_index(p, f * p.FC + cc, j0));
-            d4[cc * (p.batch / 4) + k4] = __ldcg(s4 + k4);
+            if (f * p.FC + cc >= p.H) continue;  // a column past H: never written, never folded
+            float *s4 = p.slots + slot_index(p, f * p.FC + cc, j0) + 4 * k4;
+            const int n = min(4, j1 - j0 - 4 * k4);  // words of real tiles (the stride pads to 4)
+            uint4 v = ld_slot4(s4);
+            const bool ready = v.x != 0u && (n < 2 || v.y != 0u) && (n < 3 || v.z != 0u) && (n < 4 || v.w != 0u);
+            if (!ready && !wait_slot4(s4, n, v)) {
+                ok = false;
+                break;
+            }
+            d4[cc * (p.batch / 4) + k4] = make_float4(slot_value(v.x), slot_value(v.y), slot_value(v.z),
+                                                      slot_value(v.w));
+            *reinterpret_cast<uint4 *>(s4) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (!ok) {
+            record_error(p.hdr, DGR_ERR_TIMEOUT, 2);
+            abort_flag = 1;
         }
     };
 
@@ -519,18 +575,21 @@ __global__ void __launch_bounds__(kSmallWarps * 32) colsum_small_kernel(const Co
     __threadfence();  // every other warp's slot rows are visible after its ticket
     const int n4 = (p.n_tiles + 3) / 4;  // 16-byte groups of 4 tiles per column (the stride is padded to 4)
     for (int c = lane; c < p.H; c += 32) {
-        const float4 *s4 = reinterpret_cast<const float4 *>(p.slots + slot_index(p, c, 0));
+        uint4 *s4 = reinterpret_cast<uint4 *>(p.slots + slot_index(p, c, 0));
         float F = 0.0f;
         for (int q0 = 0; q0 < n4; q0 += 8) {
-            float4 v[8];
+            uint4 v[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u)
                 if (q0 + u < n4) v[u] = __ldcg(s4 + q0 + u);
 #pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (q0 + u < n4) s4[q0 + u] = make_uint4(0u, 0u, 0u, 0u);  // empty again for the next call
+#pragma unroll
             for (int u = 0; u < 8; ++u) {
                 if (q0 + u >= n4) break;
                 const int k = 4 * (q0 + u);
-                const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                const float e[4] = {slot_value(v[u].x), slot_value(v[u].y), slot_value(v[u].z), slot_value(v[u].w)};
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                     if (k + i < p.n_tiles) F = (k + i == 0) ? e[i] : __fadd_rn(F, e[i]);
@@ -805,10 +864,9 @@ extern "C" dgr_status dgr_ordered_colsum_noalloc(const void *x, int32_t dtype, i
     void *ws = nullptr;
     dgr_status st = static_scratch(&ws);
     if (st != DGR_OK) return st;
-    // The array keeps whatever the previous call left; the header (status word,
-    // folder ticket) and the ready counters must start at zero.
-    if (B * S > 0 && H > 0 &&
-        cudaMemsetAsync(ws, 0, L.slots_off, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    // The array keeps whatever the previous call (of any shape, or one that
+    // ended in an error) left; the call's region must start at zero.
+    if (B * S > 0 && H > 0 && cudaMemsetAsync(ws, 0, L.total, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return DGR_ERR_CUDA;
     return dgr_ordered_colsum(x, dtype, B, S, H, stride_b, stride_s, out, accumulate, tile_rows, ws,
                               kStaticScratchBytes, stream);

@@ -112,3 +112,28 @@ def test_full_workload_large():
     got = assert_replays_identical(lambda: _gpu(ci, base_dev=base, ws=ws), n=20)
     assert_bits_equal(got.view(np.float32), want, "colsum_large")
     assert dgr.read_device_status(ws) == 0
+
+
+@pytest.mark.parametrize("S,H,W", [
+    (600 * 128 + 1, 32, 128),  # warp producers and folders; the last tile is one row
+    (3001, 12, 1),             # block producers (3 vectors a row), one-row tiles
+    (200 * 128 + 1, 32, 128),  # one launch with a ticket
+])
+def test_nan_partial_and_workspace_back_to_zero(S, H, W):
+    # A slot word holds the complement of a tile partial, 0 meaning "not
+    # written yet"; the NaN with every bit set (complement 0) is stored as
+    # another NaN. Here it is a whole tile's partial (a one-row tile): its
+    # column must come out NaN, every other column bit-exact, and every word
+    # of the workspace must be zero again after each call.
+    ci = gi.colsum_input(1, S, H, seed=S + H, dtype=torch.float32)
+    ci.base.view(torch.int32)[(S - 1) * H + 3] = -1
+    want = _oracle(ci, W)
+    assert np.isnan(want[3])
+    keep = np.arange(H) != 3
+    ws = dgr.workspace(dgr.colsum_workspace_bytes(S, H, W))
+    base = ci.base.cuda()
+    for _ in range(2):
+        got = _gpu(ci, W, ws=ws, base_dev=base).cpu().numpy()
+        assert np.isnan(got[3])
+        assert_bits_equal(got[keep], want[keep], f"colsum {S}x{H} W={W} beside a NaN column")
+        assert int(torch.count_nonzero(ws)) == 0
