@@ -23,6 +23,10 @@ The five workloads (shapes, distributions and draw order):
                  counts -> offsets; G bf16 [32768, 4096], X bf16 [32768, 2048]
                  ~ N(0, 1), rows grouped by expert; main_grad fp32
                  [8, 4096, 2048] ~ N(0, 1e-3^2)                              seed 5
+  dbias          expert of each of 65536 rows ~ multinomial(uniform over 8),
+                 counts -> offsets; dY bf16 [65536, 2048] ~ N(0, 1), rows
+                 grouped by expert (the cuDNN-frontend dsReLU example's
+                 valid_m 64k, n 2048); dbias fp32 [8, 2048] zeros             seed 6
 """
 from __future__ import annotations
 
@@ -278,3 +282,47 @@ def tc_step_input(kind: str, n: int, seed: int) -> TcStepInput:
     else:
         raise ValueError(kind)
     return TcStepInput(_bf16_bits_np(A), _bf16_bits_np(B), C, acc)
+
+
+# --------------------------------------------------------------------------
+# grouped dbias
+# --------------------------------------------------------------------------
+
+@dataclass
+class DbiasInput:
+    dY: torch.Tensor         # [T, ld] storage; the rows' first H columns are the data
+    offs: torch.Tensor       # int64 [E+1]
+    out: torch.Tensor        # fp32 [E, H]
+    T: int
+    H: int
+    ld: int
+    E: int
+
+
+def dbias_input(T: int, H: int, E: int, *, seed: int, dist: str = "normal", dtype: torch.dtype = torch.bfloat16,
+                counts: list[int] | None = None, ld: int | None = None, out_init: str = "zeros") -> DbiasInput:
+    """Rows grouped by expert: counts from a multinomial over E experts (or
+    given); with ld > H the unused columns hold NaN so a stray read shows."""
+    g = _gen(seed)
+    if counts is None:
+        ex = torch.multinomial(torch.ones(E), T, replacement=True, generator=g)
+        cnt = torch.bincount(ex, minlength=E)
+    else:
+        assert len(counts) == E and sum(counts) == T
+        cnt = torch.tensor(counts, dtype=torch.int64)
+    offs = torch.zeros(E + 1, dtype=torch.int64)
+    offs[1:] = torch.cumsum(cnt, 0)
+    ld = H if ld is None else ld
+    assert ld >= H
+    dY = _draw((T, ld), dist, g).to(dtype)
+    if ld > H:
+        dY[:, H:] = float("nan")
+    if out_init == "zeros":
+        out = torch.zeros((E, H), dtype=torch.float32)
+    else:
+        out = _draw((E, H), dist, g).to(torch.float32)
+    return DbiasInput(dY, offs, out, T, H, ld, E)
+
+
+def dbias_full() -> DbiasInput:
+    return dbias_input(65536, 2048, 8, seed=6)

@@ -78,6 +78,8 @@ def lib() -> ctypes.CDLL:
         L.dgro_grouped_wgrad_accumulate.restype = I32
         L.dgro_wgrad_elements.argtypes = [P, P, P, I64, I64, P, I64, I64, P, P, P, P, P]
         L.dgro_wgrad_elements.restype = I32
+        L.dgro_grouped_dbias.argtypes = [P, I32, I64, I64, I64, P, I64, I64, P, I64, I32]
+        L.dgro_grouped_dbias.restype = I32
         _lib = L
     return _lib
 
@@ -210,3 +212,17 @@ def wgrad_elements(G_bits: np.ndarray, X_bits: np.ndarray, offs: np.ndarray, N: 
 
 if __name__ == "__main__":  # pragma: no cover - manual build helper
     print(build(force="--force" in sys.argv))
+
+
+def grouped_dbias(dY: np.ndarray, T: int, H: int, ld: int, offs: np.ndarray, out: np.ndarray, *,
+                  ld_out: int | None = None, accumulate: bool = False, tile_rows: int = 128) -> None:
+    """out[e][h] (+)= ordered column sum of dY over expert e's rows offs[e] .. offs[e+1]-1
+    (flat buffers, elements; tiles counted from each expert's first row)."""
+    o = np.ascontiguousarray(offs, dtype=np.int64)
+    E = o.size - 1
+    ld_out = H if ld_out is None else ld_out
+    assert dY.ndim == 1 and out.dtype == np.float32 and out.ndim == 1 and out.flags.c_contiguous
+    assert E >= 1 and (E == 0 or out.size >= (E - 1) * ld_out + H)
+    rc = lib().dgro_grouped_dbias(_ptr(dY), _dtype_code(dY), T, H, ld, _ptr(o), E, tile_rows, _ptr(out),
+                                  ld_out, int(accumulate))
+    _check(rc, "grouped_dbias")

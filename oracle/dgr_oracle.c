@@ -11,7 +11,7 @@
  * built with -ffp-contract=off and without fast-math, so that no a*b+c is
  * ever fused into one rounding (GCC contracts by default on aarch64).
  *
- * The four operations and the pages they follow:
+ * The operations and the pages they follow:
  *   ordered column sum   - Megatron-LM PR #8244 "ordered reduction for the fused
  *                          pre-GDR gate backward", description: each program
  *                          writes independent FP32 partial sums, the caller
@@ -29,8 +29,10 @@
  *                          "Design and numerics": out <- RN32(out + dW) with a
  *                          deterministic dW; the 512-token k tile is the
  *                          weight-gradient main stage.
+ *   grouped dbias        - cuDNN-frontend PR #521, commit "Cover dbias": FP32
+ *                          partials per M-block and a per-expert segment sum.
  *
- * Canonical order (the same for all four): partial sums are taken over tiles;
+ * Canonical order (the same for all): partial sums are taken over tiles;
  * inside a tile the leaves are summed by a fixed-width pairwise tree; the tile
  * partials are folded in ascending tile order; the result overwrites the
  * output or is added to it with one rounding.
@@ -636,5 +638,67 @@ int dgro_wgrad_elements(const uint16_t *G, const uint16_t *X, const int64_t *off
         float mg = main_grad_in[i];
         res[i] = wgrad_element(G, X, offs, N, K, chunk, e, n, k, mg, 0, m);
     }
+    return DGRO_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* 5. Grouped dbias: a column sum per expert's row range                      */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * dbias[e][h] = fold_j pw_W( dY[t][h] : t in tile j of expert e ).
+ * cuDNN-frontend PR #521, commit "Cover dbias": dbias contends across M-tiles,
+ * so each M-block gets its own FP32 partials and a per-expert segment sum
+ * reduces them, with the accumulate semantics of the dprob reduction (commit
+ * "Address PR review", item 3). Expert e owns rows offs[e] .. offs[e+1]-1 of
+ * dY; its tiles are W consecutive rows counted from its first row (the page
+ * keeps every M-block inside one expert by padding the expert ranges; tiles
+ * counted from each expert's start give the same blocks there and need no
+ * padding). dY[t][h] is at t*ld + h (elements). With accumulate, out[e][h] =
+ * out[e][h] + F (one rounding); an expert with no rows gets +0.0 (overwrite)
+ * or is left unchanged (accumulate). offs must be non-decreasing with
+ * offs[0] = 0 and offs[E] = T; out[e][h] is at e*ld_out + h.
+ */
+int dgro_grouped_dbias(const void *dY, int32_t dtype, int64_t T, int64_t H, int64_t ld,
+                       const int64_t *offs, int64_t E, int64_t W, float *out, int64_t ld_out,
+                       int32_t accumulate)
+{
+    if (T < 0 || H < 0 || E < 1 || ld < H || ld_out < H || !is_pow2(W) || (dtype != 0 && dtype != 1))
+        return DGRO_ERR_ARG;
+    if (offs[0] != 0 || offs[E] != T)
+        return DGRO_ERR_ARG;
+    for (int64_t e = 0; e < E; ++e)
+        if (offs[e + 1] < offs[e])
+            return DGRO_ERR_ARG;
+    float *leaf = (float *)malloc((size_t)W * sizeof(float));
+    float *part = (float *)malloc((size_t)((T + W - 1) / W + 1) * sizeof(float));
+    if (!leaf || !part) {
+        free(leaf);
+        free(part);
+        return DGRO_ERR_NOMEM;
+    }
+    for (int64_t e = 0; e < E; ++e) {
+        int64_t a = offs[e], rows = offs[e + 1] - offs[e];
+        int64_t n_tiles = (rows + W - 1) / W;
+        for (int64_t h = 0; h < H; ++h) {
+            float *o = out + e * ld_out + h;
+            if (n_tiles == 0) {
+                if (!accumulate)
+                    *o = 0.0f;
+                continue;
+            }
+            for (int64_t j = 0; j < n_tiles; ++j) {
+                int64_t r0 = j * W;
+                int64_t count = (rows - r0 < W) ? (rows - r0) : W;
+                for (int64_t i = 0; i < count; ++i)
+                    leaf[i] = load_elem(dY, dtype, (a + r0 + i) * ld + h);
+                part[j] = dgro_pairwise(leaf, count, W);
+            }
+            float f = dgro_fold(part, n_tiles);
+            *o = accumulate ? *o + f : f;
+        }
+    }
+    free(leaf);
+    free(part);
     return DGRO_OK;
 }
