@@ -59,6 +59,8 @@ def lib() -> ctypes.CDLL:
             "dgr_det_index_add": ([P, I64, I64, I64, P, I64, P, I64, I32, P, P, SZ, P], I32),
             "dgr_wgrad_workspace_bytes": ([I32, I64, I64], SZ),
             "dgr_grouped_wgrad_accumulate": ([P, P, P, I32, I64, I64, I64, P, I32, P, SZ, P], I32),
+            "dgr_dbias_workspace_bytes": ([I64, I64, I32, I32], SZ),
+            "dgr_grouped_dbias": ([P, I32, I64, I64, I64, P, I32, P, I64, I32, I32, P, SZ, P], I32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -182,3 +184,23 @@ def grouped_wgrad_accumulate(G: torch.Tensor, X: torch.Tensor, offs: torch.Tenso
         _ptr(G), _ptr(X), _ptr(offs), E, T, N, K, _ptr(main_grad), chunk_tokens, _ptr(ws), ws.numel(),
         _stream(stream)))
     return main_grad
+
+
+def dbias_workspace_bytes(T: int, H: int, E: int, tile_rows: int = 128) -> int:
+    return int(lib().dgr_dbias_workspace_bytes(T, H, E, tile_rows))
+
+
+def grouped_dbias(dY: torch.Tensor, offs: torch.Tensor, out: torch.Tensor, *, accumulate: bool = False,
+                  tile_rows: int = 128, ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """out[e] (+)= ordered column sum of dY over expert e's rows offs[e] .. offs[e+1]-1
+    (offs: int64 device [E+1]; out: fp32 [E, H])."""
+    T, H = dY.shape
+    E = offs.numel() - 1
+    if out.dim() != 2 or out.shape != (E, H) or out.dtype != torch.float32 or offs.dtype != torch.int64:
+        raise ValueError("dY [T, H], offs int64 [E+1], out fp32 [E, H] expected")
+    if ws is None:
+        ws = workspace(dbias_workspace_bytes(T, H, E, tile_rows), dY.device)
+    _check("dgr_grouped_dbias", lib().dgr_grouped_dbias(
+        _ptr(dY), _dtype(dY), T, H, dY.stride(0), _ptr(offs), E, _ptr(out), out.stride(0), int(accumulate),
+        tile_rows, _ptr(ws), ws.numel(), _stream(stream)))
+    return out

@@ -218,6 +218,41 @@ dgr_status dgr_grouped_wgrad_accumulate(const void *G, const void *X, const int6
                                         int64_t T_total, int64_t N, int64_t K, float *main_grad,
                                         int32_t chunk_tokens, void *ws, size_t ws_bytes, void *stream);
 
+/* ------------------------------------------------------------------------ */
+/* 5. Grouped dbias: an ordered column sum per expert's rows                 */
+/* ------------------------------------------------------------------------ */
+/*
+ * cuDNN-frontend PR #521, commit "Cover dbias": dbias contends across M-tiles,
+ * so each (row block, column) gets one FP32 partial with a single writer and a
+ * per-expert segment sum reduces the partials in a fixed order; the reduction
+ * accumulates into dbias like the dprob one (commit "Address PR review").
+ *
+ *   expert e owns rows d_offs[e] .. d_offs[e+1]-1 of dY; its tiles are
+ *   tile_rows consecutive rows counted from its first row (the last one
+ *   ragged);
+ *   dbias[e][h] = fold_j pw_W( dY[t][h] : t in tile j of expert e ),
+ *   written (accumulate = 0) or added with one rounding (accumulate != 0);
+ *   an expert with no rows gets +0.0 (overwrite) or is left unchanged.
+ *
+ * dY:       [T, H] bf16 or fp32 (dtype), row stride ld_dy (elements).
+ * d_offs:   [E+1] int64 DEVICE array, non-decreasing, d_offs[0] = 0,
+ *           d_offs[E] = T (never read by the host: no synchronisation). Offsets
+ *           outside this contract are detected on the device: the call then
+ *           writes nothing and records DGR_ERR_INVALID_ARG in the status word.
+ * dbias:    [E, H] fp32, row stride ld_out (elements).
+ * tile_rows: power of two 8 .. 128 (128 canonical).
+ * Limits:   1 <= E <= 1024, T < 2^31, H <= 2^20. dY 16-byte aligned with H
+ *           and ld_dy multiples of 16 bytes' worth of elements (8 bf16, 4 fp32):
+ *           DGR_ERR_MISALIGNED otherwise.
+ * ws:       dgr_dbias_workspace_bytes(T, H, E, tile_rows) bytes, zeroed once
+ *           (status word, per-(expert, column block) tickets, FP32 partials).
+ * dbias must not overlap dY, d_offs or ws.
+ */
+size_t dgr_dbias_workspace_bytes(int64_t T, int64_t H, int32_t E, int32_t tile_rows);
+dgr_status dgr_grouped_dbias(const void *dY, int32_t dtype, int64_t T, int64_t H, int64_t ld_dy,
+                             const int64_t *d_offs, int32_t E, float *dbias, int64_t ld_out,
+                             int32_t accumulate, int32_t tile_rows, void *ws, size_t ws_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

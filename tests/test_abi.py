@@ -105,3 +105,23 @@ def test_host_rejects_bad_arguments_before_any_launch(L):
     # index_add: workspace too small
     assert L.dgr_det_index_add(_p(0x40000), 10, 8, 8, _p(0x80000), 8, _p(0xC0000), 4, 128, None, _p(0x100000),
                                64, None) == 3
+    # dbias: bad dtype, tile not a power of two, E = 0, E beyond the limit, tile below 8
+    dy, offs, db = _p(0x100000), _p(0x200000), _p(0x300000)
+    ws = _p(0x400000)
+    assert L.dgr_grouped_dbias(dy, 7, 256, 16, 16, offs, 2, db, 16, 0, 128, ws, 1 << 20, None) == 1
+    assert L.dgr_grouped_dbias(dy, 1, 256, 16, 16, offs, 2, db, 16, 0, 100, ws, 1 << 20, None) == 1
+    assert L.dgr_grouped_dbias(dy, 1, 256, 16, 16, offs, 0, db, 16, 0, 128, ws, 1 << 20, None) == 1
+    assert L.dgr_grouped_dbias(dy, 1, 256, 16, 16, offs, 2000, db, 16, 0, 128, ws, 1 << 20, None) == 2
+    assert L.dgr_grouped_dbias(dy, 1, 256, 16, 16, offs, 2, db, 16, 0, 4, ws, 1 << 20, None) == 2
+    # dbias: H not a multiple of 8 bf16 elements, workspace too small, dbias overlapping dY
+    assert L.dgr_grouped_dbias(dy, 1, 256, 12, 12, offs, 2, db, 12, 0, 128, ws, 1 << 20, None) == 5
+    assert L.dgr_grouped_dbias(dy, 1, 256, 16, 16, offs, 2, db, 16, 0, 128, ws, 64, None) == 3
+    assert L.dgr_grouped_dbias(dy, 1, 256, 16, 16, offs, 2, _p(0x100040), 16, 0, 128, ws, 1 << 20, None) == 4
+
+
+def test_dbias_workspace_size(L):
+    # header + tickets [E, ceil(H / 128)] + FP32 partials [ceil(T / W) + E tiles, H]
+    n = dgr.dbias_workspace_bytes(65536, 2048, 8)
+    assert n >= (512 + 8) * 2048 * 4 + 8 * 16 * 4
+    assert dgr.dbias_workspace_bytes(100, 16, 0) == 0
+    assert dgr.dbias_workspace_bytes(100, 16, 2, 3) == 0
