@@ -7,41 +7,98 @@
 // offs[e+1]-1 (device offsets, never read by the host); its tiles are W rows
 // counted from its first row.
 //
-// One persistent launch. A work item is (tile g, block of 32*VE columns):
-//   - 8 warps; warp w sums rows [w*W/8, (w+1)*W/8) of the tile in registers
-//     (every row's 16-byte load in flight at once), the tree's lower levels;
-//   - one thread per column then combines the 8 warp partials by the tree's
-//     top three levels (absent row groups pass their sibling up) and writes
-//     the tile's slot;
-//   - the CTA fences its slots and takes the (expert, column block) ticket;
-//     the CTA that takes the expert's last ticket folds the expert's slots in
-//     ascending tile order, writes (or adds into) dbias and resets the ticket.
-// Integer atomics only count; no floating-point value depends on timing.
+// Two launches:
+//   produce - persistent, one CTA of 16 warps per SM. A work item is (tile g,
+//             block of V 16-byte column vectors) and belongs to one warp:
+//             lane = (row group, vector), 32 / V row groups of consecutive
+//             rows. A lane sums its rows by the tile tree's lower levels in
+//             registers, 8 rows' loads in flight at a time (batches are
+//             aligned subtrees, combined through a binary-counter stack); the
+//             upper levels are xor-shuffles between row groups; row group 0
+//             stores the item's partials. No barrier, no fence, no atomic.
+//   fold    - one thread per (expert, column), started early by programmatic
+//             dependent launch and waiting for the producers' grid: the
+//             expert's partials folded in ascending tile order, then written
+//             or added to dbias with one rounding; an expert with no rows
+//             gets +0.0 on overwrite.
+// No floating-point value depends on timing.
 #include "dgr_common.cuh"
 
 namespace dgr {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
+constexpr int kProdThreads = 512;
+constexpr int kProdWarps = kProdThreads / 32;
+constexpr int kFoldThreads = 256;
 constexpr int kMaxExperts = 1024;
 
 struct DbiasParams {
     const char *dY;
     int64_t ld;            // elements
     int32_t T, H, E, W;
-    int32_t n_cb;          // column blocks of 32 * VE columns
+    int32_t n_cb;          // column blocks of V * VE columns
     const int64_t *offs;   // [E + 1], device
     float *out;            // [E, H], row stride ld_out
     int64_t ld_out;
     int32_t accumulate;
     float *slots;          // [tiles, H]
-    int32_t *tickets;      // [E, n_cb]
     WsHeader *hdr;
 };
 
-__device__ __forceinline__ void unpack(const uint4 &v, float *f, int dtype_bf16) {
-    if (dtype_bf16) {
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// tbase[e] = first tile of expert e (tbase[E] = all tiles), from the device
+// offsets, by the whole block (every block computes the same). Returns false
+// when the offsets break the contract (decreasing, offs[0] != 0, offs[E] != T).
+__device__ bool tile_bases(const DbiasParams &p, int32_t *tbase, int64_t *soffs, int32_t *wsum, int32_t *bad) {
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, nt = blockDim.x, nw = nt >> 5;
+    if (tid == 0) *bad = 0;
+    __syncthreads();
+    int32_t run = 0;
+    for (int e0 = 0; e0 < p.E; e0 += nt) {
+        const int e = e0 + tid;
+        int32_t c = 0;
+        if (e < p.E) {
+            const int64_t a = p.offs[e], b = p.offs[e + 1];
+            soffs[e] = a;
+            if (e == p.E - 1) soffs[p.E] = b;
+            if (b < a || (e == 0 && a != 0) || (e == p.E - 1 && b != p.T)) *bad = 1;
+            else c = static_cast<int32_t>((b - a + p.W - 1) / p.W);
+        }
+        int32_t incl = c;
+#pragma unroll
+        for (int s = 1; s < 32; s <<= 1) {
+            const int32_t o = __shfl_up_sync(0xffffffffu, incl, s);
+            if (lane >= s) incl += o;
+        }
+        if (lane == 31) wsum[w] = incl;
+        __syncthreads();
+        int32_t before = run;
+        for (int v = 0; v < w; ++v) before += wsum[v];
+        if (e < p.E) tbase[e] = before + incl - c;
+        for (int v = 0; v < nw; ++v) run += wsum[v];
+        __syncthreads();
+    }
+    if (tid == 0) tbase[p.E] = run;
+    __syncthreads();
+    return *bad == 0;
+}
+
+
+// The same predicated 16-byte load with a 256-byte L2 fetch: a 128-byte
+// access brings its neighbour (the next item's columns) with it.
+__device__ __forceinline__ void ldg_v4u_l2_256_if(uint4 &v, const void *ptr, bool pred) {
+    asm volatile(
+        "{ .reg .pred q; setp.ne.b32 q, %5, 0;\n\t"
+        "@q ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4]; }"
+        : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w)
+        : "l"(ptr), "r"(static_cast<int>(pred)));
+}
+
+template <int DT_BF16>
+__device__ __forceinline__ void unpack(const uint4 &v, float *f) {
+    if (DT_BF16) {
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -56,76 +113,39 @@ __device__ __forceinline__ void unpack(const uint4 &v, float *f, int dtype_bf16)
     }
 }
 
-// Pairwise tree over the first n (1..L) of L leaves held in v[] (L a power
-// of two), in place: v[0] ends as the root. A node whose right child holds no
-// present leaf is its left child, unchanged.
-template <int L, int VE>
-__device__ __forceinline__ void tree_prefix(float (*v)[VE], int n) {
-#pragma unroll
-    for (int s = 1; s < L; s *= 2) {
-#pragma unroll
-        for (int i = 0; i + s < L; i += 2 * s)
-            if (i + s < n) {
-#pragma unroll
-                for (int e = 0; e < VE; ++e) v[i][e] = __fadd_rn(v[i][e], v[i + s][e]);
-            }
-    }
-}
+// 16-byte column vectors of an item (a warp): 8 row groups of W / 8 rows.
+// Measured on the 65536 x 2048 workload: 8 vectors (4 row groups) 71.6 us,
+// 4 vectors 56.4 us, 2 vectors 70.0 us; narrow items give many small units
+// of work, each a short chain of loads.
+constexpr int kItemVectors = 4;
 
-// DT_BF16: 1 for bf16 rows (8 a vector), 0 for fp32 (4 a vector). RW: rows a
-// warp sums (W / 8).
-template <int DT_BF16, int RW>
-__global__ void __launch_bounds__(kThreads, 2) dbias_kernel(const DbiasParams p) {
+// DT_BF16: 1 for bf16 rows (8 a vector), 0 for fp32 (4 a vector); W: tile
+// rows; V: column vectors of an item.
+template <int DT_BF16, int W, int V>
+__global__ void __launch_bounds__(kProdThreads, 1) dbias_produce(const DbiasParams p) {
     constexpr int VE = DT_BF16 ? 8 : 4;
-    constexpr int CBW = 32 * VE;  // columns of a block
+    constexpr int CBW = V * VE;                  // columns of a block
     constexpr int es = DT_BF16 ? 2 : 4;
-    __shared__ float red[kWarps][CBW];
-    __shared__ int32_t tbase[kMaxExperts + 1];  // first tile of each expert; tbase[E] = tiles
-    __shared__ int32_t wsum[kWarps];
-    __shared__ int32_t bad, ticket;
-    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-
-    // the experts' tile bases (every CTA the same), and the offsets' contract
-    if (tid == 0) bad = 0;
-    __syncthreads();
-    int32_t run = 0;
-    for (int e0 = 0; e0 < p.E; e0 += kThreads) {
-        const int e = e0 + tid;
-        int32_t c = 0;
-        if (e < p.E) {
-            const int64_t a = p.offs[e], b = p.offs[e + 1];
-            if (b < a || (e == 0 && a != 0) || (e == p.E - 1 && b != p.T)) bad = 1;
-            else c = static_cast<int32_t>((b - a + p.W - 1) / p.W);
-        }
-        int32_t incl = c;
-#pragma unroll
-        for (int s = 1; s < 32; s <<= 1) {
-            const int32_t o = __shfl_up_sync(0xffffffffu, incl, s);
-            if (lane >= s) incl += o;
-        }
-        if (lane == 31) wsum[w] = incl;
-        __syncthreads();
-        int32_t before = run;
-        for (int v = 0; v < w; ++v) before += wsum[v];
-        if (e < p.E) tbase[e] = before + incl - c;
-        for (int v = 0; v < kWarps; ++v) run += wsum[v];
-        __syncthreads();
-    }
-    if (tid == 0) tbase[p.E] = run;
-    __syncthreads();
-    if (bad) {
-        if (blockIdx.x == 0 && tid == 0) record_error(p.hdr, DGR_ERR_INVALID_ARG, 20);
+    constexpr int RGW = 32 / V;                  // row groups
+    constexpr int RPL = W / RGW;                 // rows a lane
+    static_assert(RPL >= 1, "a row a lane at least");
+    constexpr int BATCH = RPL < 8 ? RPL : 8;     // rows in flight a lane
+    constexpr int NB = RPL / BATCH;              // batches, a power of two <= 16
+    constexpr int LV = NB >= 16 ? 4 : NB >= 8 ? 3 : NB >= 4 ? 2 : NB >= 2 ? 1 : 0;
+    __shared__ int32_t tbase[kMaxExperts + 1];
+    __shared__ int64_t soffs[kMaxExperts + 1];  // the offsets, read once
+    __shared__ int32_t wsum[kProdWarps];
+    __shared__ int32_t bad;
+    launch_dependents();  // the fold launch may start its blocks; it waits for this grid
+    if (!tile_bases(p, tbase, soffs, wsum, &bad)) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) record_error(p.hdr, DGR_ERR_INVALID_ARG, 20);
         return;
     }
-    // overwrite: an expert with no rows gets +0.0
-    if (blockIdx.x == 0 && !p.accumulate) {
-        for (int e = 0; e < p.E; ++e)
-            if (tbase[e + 1] == tbase[e])
-                for (int h = tid; h < p.H; h += kThreads) p.out[static_cast<int64_t>(e) * p.ld_out + h] = 0.0f;
-    }
-
+    const int lane = threadIdx.x & 31;
     const int64_t n_items = static_cast<int64_t>(tbase[p.E]) * p.n_cb;
-    for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const int64_t n_warps = static_cast<int64_t>(gridDim.x) * kProdWarps;
+    for (int64_t item = static_cast<int64_t>(blockIdx.x) * kProdWarps + (threadIdx.x >> 5); item < n_items;
+         item += n_warps) {
         const int32_t g = static_cast<int32_t>(item / p.n_cb);
         const int cb = static_cast<int>(item - static_cast<int64_t>(g) * p.n_cb);
         // expert of tile g: the last e with tbase[e] <= g (empty experts share a base)
@@ -135,108 +155,180 @@ __global__ void __launch_bounds__(kThreads, 2) dbias_kernel(const DbiasParams p)
             if (tbase[mid] <= g) lo = mid;
             else hi = mid - 1;
         }
-        const int e = lo;
-        const int32_t j = g - tbase[e];
-        const int64_t r_first = p.offs[e] + static_cast<int64_t>(j) * p.W;
-        const int count = static_cast<int>(min(static_cast<int64_t>(p.W), p.offs[e + 1] - r_first));
-        const int col = cb * CBW + lane * VE;
+        const int64_t r_first = soffs[lo] + static_cast<int64_t>(g - tbase[lo]) * W;
+        const int count = static_cast<int>(min(static_cast<int64_t>(W), soffs[lo + 1] - r_first));
+        const int rg = lane / V;
+        const int col = cb * CBW + (lane - rg * V) * VE;
         const bool col_ok = col < p.H;
-
-        // rows [w*RW, w*RW + RW) of the tile: all loads in flight, then the tree
-        const int n_here = max(0, min(RW, count - w * RW));
-        uint4 raw[RW];
+        const int nrows = max(0, min(RPL, count - rg * RPL));  // this lane's rows present
+        const char *src = p.dY + ((r_first + rg * RPL) * p.ld + col) * es;
+        float stack[LV + 1][VE];
+        float acc[VE];
 #pragma unroll
-        for (int r = 0; r < RW; ++r) {
-            raw[r] = make_uint4(0u, 0u, 0u, 0u);
-            ldg_nc_v4u_if(raw[r], p.dY + ((r_first + w * RW + r) * p.ld + col) * es, col_ok && r < n_here);
-        }
-        float v[RW][VE];
+        for (int bi = 0; bi < NB; ++bi) {
+            const int rb = bi * BATCH;
+            uint4 raw[BATCH];
 #pragma unroll
-        for (int r = 0; r < RW; ++r) unpack(raw[r], v[r], DT_BF16);
-        tree_prefix<RW, VE>(v, n_here);
-        if (n_here > 0) {
-#pragma unroll
-            for (int e2 = 0; e2 < VE; ++e2) red[w][lane * VE + e2] = v[0][e2];
-        }
-        __syncthreads();
-        // top levels across the warps' row groups, one thread per column
-        const int nw = (count + RW - 1) / RW;  // row groups present (>= 1)
-        const int c = cb * CBW + tid;
-        if (tid < CBW && c < p.H) {
-            float u[kWarps][1];
-#pragma unroll
-            for (int q = 0; q < kWarps; ++q) u[q][0] = q < nw ? red[q][tid] : 0.0f;
-            tree_prefix<kWarps, 1>(u, nw);
-            p.slots[static_cast<int64_t>(g) * p.H + c] = u[0][0];
-        }
-        __threadfence();  // this thread's slot before the ticket
-        __syncthreads();
-        const int32_t n_tiles_e = tbase[e + 1] - tbase[e];
-        if (tid == 0) ticket = atomicAdd(&p.tickets[e * p.n_cb + cb], 1);
-        __syncthreads();
-        if (ticket == n_tiles_e - 1) {
-            // the expert's last tile of this column block: fold its slots in
-            // ascending tile order (every other CTA fenced its slot before
-            // its ticket)
-            __threadfence();
-            if (tid < CBW && c < p.H) {
-                const float *s = p.slots + static_cast<int64_t>(tbase[e]) * p.H + c;
-                float F = 0.0f;
-                for (int j0 = 0; j0 < n_tiles_e; j0 += 16) {
-                    float x[16];
-#pragma unroll
-                    for (int u = 0; u < 16; ++u)
-                        if (j0 + u < n_tiles_e) x[u] = __ldcg(s + static_cast<int64_t>(j0 + u) * p.H);
-#pragma unroll
-                    for (int u = 0; u < 16; ++u)
-                        if (j0 + u < n_tiles_e) F = (j0 + u == 0) ? x[u] : __fadd_rn(F, x[u]);
-                }
-                float *o = p.out + static_cast<int64_t>(e) * p.ld_out + c;
-                *o = p.accumulate ? __fadd_rn(*o, F) : F;
+            for (int r = 0; r < BATCH; ++r) {
+                raw[r] = make_uint4(0u, 0u, 0u, 0u);
+                ldg_v4u_l2_256_if(raw[r], src + static_cast<int64_t>(rb + r) * p.ld * es, col_ok && rb + r < nrows);
             }
-            if (tid == 0) p.tickets[e * p.n_cb + cb] = 0;  // ready for the next call
+            // the batch's subtree (rows rb .. rb+BATCH-1), absent rows skipped;
+            // level 1 is taken while widening, pair by pair
+            const int nb_rows = max(0, min(BATCH, nrows - rb));
+            constexpr int NP = BATCH > 1 ? BATCH / 2 : 1;
+            float lv[NP][VE];
+#pragma unroll
+            for (int i = 0; i < NP; ++i) {
+                unpack<DT_BF16>(raw[2 * i], lv[i]);
+                if (BATCH > 1 && 2 * i + 1 < nb_rows) {
+                    float b2[VE];
+                    unpack<DT_BF16>(raw[2 * i + 1], b2);
+#pragma unroll
+                    for (int e = 0; e < VE; ++e) lv[i][e] = __fadd_rn(lv[i][e], b2[e]);
+                }
+            }
+            const int np_present = (nb_rows + 1) / 2;
+#pragma unroll
+            for (int sft = 1; sft < NP; sft *= 2) {
+#pragma unroll
+                for (int i = 0; i + sft < NP; i += 2 * sft)
+                    if (i + sft < np_present) {
+#pragma unroll
+                        for (int e = 0; e < VE; ++e) lv[i][e] = __fadd_rn(lv[i][e], lv[i + sft][e]);
+                    }
+            }
+            // push batch bi (a compile-time index) onto the binary-counter stack
+            if (nb_rows > 0) {
+#pragma unroll
+                for (int e = 0; e < VE; ++e) acc[e] = lv[0][e];
+                int lvl = 0;
+#pragma unroll
+                for (int l = 0; l < LV; ++l) {
+                    if (((bi >> l) & 1) == 0) break;
+#pragma unroll
+                    for (int e = 0; e < VE; ++e) acc[e] = __fadd_rn(stack[l][e], acc[e]);
+                    lvl = l + 1;
+                }
+#pragma unroll
+                for (int l = 0; l <= LV; ++l)
+                    if (l == lvl) {
+#pragma unroll
+                        for (int e = 0; e < VE; ++e) stack[l][e] = acc[e];
+                    }
+            }
         }
-        __syncthreads();  // red[] and ticket are reused by the next item
+        // ragged end: complete blocks of the set bits of the present batch
+        // count, smallest first, each larger (earlier) block on the left
+        const int nbp = (nrows + BATCH - 1) / BATCH;
+        bool have = false;
+#pragma unroll
+        for (int l = 0; l <= LV; ++l) {
+            if ((nbp >> l) & 1) {
+#pragma unroll
+                for (int e = 0; e < VE; ++e) acc[e] = have ? __fadd_rn(stack[l][e], acc[e]) : stack[l][e];
+                have = true;
+            }
+        }
+        // upper levels: row group q absorbs q + s (lane distance s * V)
+        bool present = nrows > 0;
+#pragma unroll
+        for (int s = 1; s < RGW; s *= 2) {
+            const bool left_is_me = (rg & s) == 0;
+            const bool o_present = __shfl_xor_sync(0xffffffffu, present ? 1 : 0, s * V) != 0;
+            const bool left_present = left_is_me ? present : o_present;
+            const bool right_present = left_is_me ? o_present : present;
+#pragma unroll
+            for (int e = 0; e < VE; ++e) {
+                const float o = __shfl_xor_sync(0xffffffffu, acc[e], s * V);
+                if (left_present && right_present) acc[e] = __fadd_rn(acc[e], o);
+                else if (!left_is_me && left_present) acc[e] = o;
+            }
+            present = left_present;
+        }
+        if (rg == 0 && col_ok) {
+            float4 *dst = reinterpret_cast<float4 *>(p.slots + static_cast<int64_t>(g) * p.H + col);
+#pragma unroll
+            for (int q = 0; q < VE / 4; ++q)
+                dst[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+        }
     }
+}
+
+__global__ void __launch_bounds__(kFoldThreads) dbias_fold(const DbiasParams p) {
+    __shared__ int32_t tbase[kMaxExperts + 1];
+    __shared__ int64_t soffs[kMaxExperts + 1];
+    __shared__ int32_t wsum[kFoldThreads / 32];
+    __shared__ int32_t bad;
+    const bool ok = tile_bases(p, tbase, soffs, wsum, &bad);  // the offsets only: no producer output yet
+    grid_dep_wait();  // the producers' grid has completed and its partials are visible
+    if (!ok) return;  // the producers recorded the error
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * kFoldThreads + threadIdx.x;
+    if (i >= static_cast<int64_t>(p.E) * p.H) return;
+    const int e = static_cast<int>(i / p.H);
+    const int h = static_cast<int>(i - static_cast<int64_t>(e) * p.H);
+    const int32_t n = tbase[e + 1] - tbase[e];
+    float *o = p.out + static_cast<int64_t>(e) * p.ld_out + h;
+    if (n == 0) {
+        if (!p.accumulate) *o = 0.0f;
+        return;
+    }
+    const float *s = p.slots + static_cast<int64_t>(tbase[e]) * p.H + h;
+    float F = 0.0f;
+    for (int j0 = 0; j0 < n; j0 += 32) {
+        float x[32];
+#pragma unroll
+        for (int u = 0; u < 32; ++u)
+            if (j0 + u < n) x[u] = __ldcg(s + static_cast<int64_t>(j0 + u) * p.H);
+#pragma unroll
+        for (int u = 0; u < 32; ++u)
+            if (j0 + u < n) F = (j0 + u == 0) ? x[u] : __fadd_rn(F, x[u]);
+    }
+    *o = p.accumulate ? __fadd_rn(*o, F) : F;
 }
 
 struct DbiasLayout {
     int64_t n_tiles_max;
-    int32_t n_cb_max;
-    size_t tickets, slots, total;
+    size_t slots, total;
 };
 
 // Tiles: at most ceil(T / W) + E (each expert's last tile may be partial).
-// Tickets are sized for the narrower fp32 column blocks (128 columns).
 DbiasLayout dbias_layout(int64_t T, int64_t H, int64_t E, int64_t W) {
     DbiasLayout L{};
     L.n_tiles_max = (T + W - 1) / W + E;
-    L.n_cb_max = static_cast<int32_t>((H + 127) / 128);
-    size_t o = sizeof(WsHeader);
-    L.tickets = o;
-    o += align_up(static_cast<size_t>(E) * L.n_cb_max * 4);
-    L.slots = o;
-    o += align_up(static_cast<size_t>(L.n_tiles_max) * H * 4);
-    L.total = o;
+    L.slots = sizeof(WsHeader);
+    L.total = L.slots + align_up(static_cast<size_t>(L.n_tiles_max) * H * 4);
     return L;
 }
 
-template <int DT_BF16, int RW>
-dgr_status launch_dbias(const DbiasParams &p, int grid, cudaStream_t s) {
-    dbias_kernel<DT_BF16, RW><<<grid, kThreads, 0, s>>>(p);
+template <int DT_BF16>
+dgr_status launch_produce(const DbiasParams &p, int grid, cudaStream_t s) {
+    switch (p.W) {
+        case 8: dbias_produce<DT_BF16, 8, kItemVectors><<<grid, kProdThreads, 0, s>>>(p); break;
+        case 16: dbias_produce<DT_BF16, 16, kItemVectors><<<grid, kProdThreads, 0, s>>>(p); break;
+        case 32: dbias_produce<DT_BF16, 32, kItemVectors><<<grid, kProdThreads, 0, s>>>(p); break;
+        case 64: dbias_produce<DT_BF16, 64, kItemVectors><<<grid, kProdThreads, 0, s>>>(p); break;
+        case 128: dbias_produce<DT_BF16, 128, kItemVectors><<<grid, kProdThreads, 0, s>>>(p); break;
+        default: return DGR_ERR_UNSUPPORTED;
+    }
     return launch_status();
 }
 
-template <int DT_BF16>
-dgr_status launch_dbias_w(const DbiasParams &p, int grid, cudaStream_t s) {
-    switch (p.W) {
-        case 8: return launch_dbias<DT_BF16, 1>(p, grid, s);
-        case 16: return launch_dbias<DT_BF16, 2>(p, grid, s);
-        case 32: return launch_dbias<DT_BF16, 4>(p, grid, s);
-        case 64: return launch_dbias<DT_BF16, 8>(p, grid, s);
-        case 128: return launch_dbias<DT_BF16, 16>(p, grid, s);
-        default: return DGR_ERR_UNSUPPORTED;
-    }
+// The fold may start its blocks while the producers finish (it computes the
+// tile bases from the offsets first) and reads the partials only after
+// griddepcontrol.wait.
+dgr_status launch_fold(const DbiasParams &p, cudaStream_t s) {
+    const int64_t n = static_cast<int64_t>(p.E) * p.H;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>((n + kFoldThreads - 1) / kFoldThreads));
+    cfg.blockDim = dim3(kFoldThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, dbias_fold, p) == cudaSuccess ? DGR_OK : DGR_ERR_CUDA;
 }
 
 }  // namespace
@@ -291,21 +383,23 @@ extern "C" dgr_status dgr_grouped_dbias(const void *dY, int32_t dtype, int64_t T
     p.H = static_cast<int32_t>(H);
     p.E = E;
     p.W = tile_rows;
-    p.n_cb = static_cast<int32_t>((H + 32 * ve - 1) / (32 * ve));
+    p.n_cb = static_cast<int32_t>((H + kItemVectors * ve - 1) / (kItemVectors * ve));
     p.offs = d_offs;
     p.out = dbias;
     p.ld_out = ld_out;
     p.accumulate = accumulate ? 1 : 0;
     char *w = static_cast<char *>(ws);
     p.hdr = reinterpret_cast<WsHeader *>(w);
-    p.tickets = reinterpret_cast<int32_t *>(w + L.tickets);
     p.slots = reinterpret_cast<float *>(w + L.slots);
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return DGR_ERR_CUDA;
-    // persistent: two CTAs per SM, never more than the items there can be
+    // producers: one 16-warp CTA per SM, never more than the items need
     const int64_t items_max = L.n_tiles_max * p.n_cb;
-    const int grid = static_cast<int>(items_max < 2LL * sms ? items_max : 2LL * sms);
-    return dtype == DGR_DTYPE_BF16 ? launch_dbias_w<1>(p, grid, s) : launch_dbias_w<0>(p, grid, s);
+    const int64_t want = (items_max + kProdWarps - 1) / kProdWarps;
+    const int grid = static_cast<int>(want < sms ? want : sms);
+    st = dtype == DGR_DTYPE_BF16 ? launch_produce<1>(p, grid, s) : launch_produce<0>(p, grid, s);
+    if (st != DGR_OK) return st;
+    return launch_fold(p, s);
 }

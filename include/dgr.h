@@ -245,7 +245,7 @@ dgr_status dgr_grouped_wgrad_accumulate(const void *G, const void *X, const int6
  *           and ld_dy multiples of 16 bytes' worth of elements (8 bf16, 4 fp32):
  *           DGR_ERR_MISALIGNED otherwise.
  * ws:       dgr_dbias_workspace_bytes(T, H, E, tile_rows) bytes, zeroed once
- *           (status word, per-(expert, column block) tickets, FP32 partials).
+ *           (status word, FP32 partials).
  * dbias must not overlap dY, d_offs or ws.
  */
 size_t dgr_dbias_workspace_bytes(int64_t T, int64_t H, int32_t E, int32_t tile_rows);
