@@ -53,8 +53,12 @@ ALGO = {
     "index_add": 262144 * 128 * 4 + 262144 * 4 + 2 * 16385 * 128 * 4,
     "wgrad_flop": 2 * 4096 * 2048 * 32768,
     "wgrad": 32768 * 4096 * 2 + 32768 * 2048 * 2 + 2 * 8 * 4096 * 2048 * 4,
+    "dbias": 65536 * 2048 * 2 + 8 * 2048 * 4,
 }
-LAUNCHES = {"colsum_large": 1, "colsum_small": 1, "dprob": 1, "colsum_strided": 1, "index_add": 4, "wgrad": 1}
+LAUNCHES = {"colsum_large": 1, "colsum_small": 1, "dprob": 1, "colsum_strided": 1, "index_add": 4, "wgrad": 1,
+            "dbias": 2}
+# operations beyond the step (the next rows of the scope), timed on their own after it
+EXTRAS = ["dbias"]
 
 WORKLOAD = ("deterministic reduction step: colsum bf16 8388608x64 + colsum bf16 2048x16 + dprob bf16 "
             "65536x4096 + colsum bf16 4x2048x64 (token stride 128) + index_add fp32 262144x128 -> 16385 rows "
@@ -193,8 +197,15 @@ def make_ops(dev, torch, dgr, with_wgrad, only=None, small=False):
         ops["wgrad"] = lambda: dgr.grouped_wgrad_accumulate(G, X, offs, mg, ws=wws)
         host["wgrad"] = ([wi.G, wi.X, wi.offs, wi.main_grad], [G, X, offs, mg])
         outs["wgrad"] = mg
-    order = [n for n in ["colsum_large", "colsum_small", "dprob", "colsum_strided", "index_add", "wgrad"]
-             if n in ops]
+    if want("dbias"):
+        db = gi.dbias_full() if not small else gi.dbias_input(16384, 2048, 8, seed=6)
+        dY, doffs, dout = db.dY.to(dev), db.offs.to(dev), db.out.to(dev)
+        dws = dgr.workspace(dgr.dbias_workspace_bytes(db.T, db.H, db.E), dev)
+        ops["dbias"] = lambda: dgr.grouped_dbias(dY, doffs, dout, ws=dws)
+        host["dbias"] = ([db.dY, db.offs], [dY, doffs])
+        outs["dbias"] = dout
+    steps = ["colsum_large", "colsum_small", "dprob", "colsum_strided", "index_add", "wgrad"]
+    order = [n for n in steps + (EXTRAS if only in EXTRAS else []) if n in ops]
     return order, ops, host, outs
 
 
@@ -279,6 +290,26 @@ def run_ours(args, rank, world, local_rank):
         per_ms = {n: float(t[i + 1]) for i, n in enumerate(order)}
 
     # end to end through host buffers: pinned host inputs copied in, outputs read back, every step
+    # the next rows of the scope, each timed on its own after the step (not in
+    # the step, its value or its launch count)
+    extra_ms = {}
+    for n in [x for x in EXTRAS if x in ops]:
+        for _ in range(args.warmup):
+            ops[n]()
+        evx = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        barrier()
+        torch.cuda.synchronize()
+        for a, b in evx:
+            a.record(stream)
+            ops[n]()
+            b.record(stream)
+        torch.cuda.synchronize()
+        extra_ms[n] = sum(a.elapsed_time(b) for a, b in evx) / K
+        if world > 1:
+            t = torch.tensor([extra_ms[n]], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            extra_ms[n] = float(t[0])
+
     e2e = run_e2e(args, torch, order, ops, host, outs, stream, world, dev)
 
     if rank != 0:
@@ -299,6 +330,12 @@ def run_ours(args, rank, world, local_rank):
             gbs = ALGO[n] / (ms * 1e-3) / 1e9
             parts[n] = {"us": round(ms * 1e3, 2), "gbs": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm"], 4),
                         "launches": LAUNCHES[n], "dram_traffic": traffic.get(n)}
+    next_rows = {}
+    for n, ms in extra_ms.items():
+        gbs = ALGO[n] / (ms * 1e-3) / 1e9
+        next_rows[n] = {"us": round(ms * 1e3, 2), "gbs": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm"], 4),
+                        "launches": LAUNCHES[n], "dram_traffic": traffic.get(n),
+                        "workload": "grouped dbias bf16 65536x2048, 8 experts (multinomial rows) -> fp32 [8, 2048]"}
     dom = max(order, key=lambda n: per_ms[n])
     if dom == "wgrad":
         ach = ALGO["wgrad_flop"] / (per_ms[dom] * 1e-3) / 1e12
@@ -318,7 +355,7 @@ def run_ours(args, rank, world, local_rank):
                    "parallelism": f"replicas x{world}", "wgrad": "included" if with_wgrad else "not built"},
         "reductions_frac_hbm": round(value / world / peaks["hbm"], 4),
         "wgrad_tflops": parts.get("wgrad", {}).get("tflops"),
-        "parts": parts, "roofline": roof, "e2e": e2e, "clocks": clocks,
+        "parts": parts, "next_rows": next_rows, "roofline": roof, "e2e": e2e, "clocks": clocks,
         "gpu_launches": K * sum(LAUNCHES[n] for n in order),
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -447,7 +484,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["colsum_large", "colsum_small", "dprob", "colsum_strided", "index_add",
-                                       "wgrad"], help="profiling: run one operation only (no JSON bench line)")
+                                       "wgrad", "dbias"], help="profiling: run one operation only (no JSON bench line)")
     ap.add_argument("--small", action="store_true",
                     help="profiling: colsum 2097152x64, dprob 16384x4096, wgrad T=8192 (same widths)")
     args = ap.parse_args()
