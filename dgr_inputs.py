@@ -27,6 +27,10 @@ The five workloads (shapes, distributions and draw order):
                  counts -> offsets; dY bf16 [65536, 2048] ~ N(0, 1), rows
                  grouped by expert (the cuDNN-frontend dsReLU example's
                  valid_m 64k, n 2048); dbias fp32 [8, 2048] zeros             seed 6
+  topk           65536 rows of 128 slots: one id a slot, unique in the row
+                 (slot k's id in [k*512, (k+1)*512) of 65536 keys), slots
+                 shuffled per row; 10 % of the slots then padding (-1) and
+                 every 64th row all padding; logits ~ N(0, 3^2) fp32          seed 7
 """
 from __future__ import annotations
 
@@ -326,3 +330,34 @@ def dbias_input(T: int, H: int, E: int, *, seed: int, dist: str = "normal", dtyp
 
 def dbias_full() -> DbiasInput:
     return dbias_input(65536, 2048, 8, seed=6)
+
+
+# --------------------------------------------------------------------------
+# canonical compact top-K
+# --------------------------------------------------------------------------
+
+@dataclass
+class TopkInput:
+    ids: torch.Tensor     # int32 [R, K], padding -1
+    logits: torch.Tensor  # fp32 [R, K]
+
+
+def topk_input(R: int, K: int, *, seed: int, n_keys: int = 65536, pad_frac: float = 0.1,
+               pad_row_every: int = 64, scale: float = 3.0) -> TopkInput:
+    """Ids unique within a row (slot k draws from its own block of n_keys / K keys), in a
+    shuffled slot order; then padding slots and all-padding rows."""
+    g = _gen(seed)
+    width = max(1, n_keys // K)
+    ids = torch.randint(0, width, (R, K), generator=g) + torch.arange(K) * width
+    order = torch.argsort(torch.rand((R, K), generator=g), dim=1)
+    ids = torch.gather(ids, 1, order)
+    pad = torch.rand((R, K), generator=g) < pad_frac
+    ids[pad] = -1
+    if pad_row_every:
+        ids[::pad_row_every] = -1
+    logits = torch.randn((R, K), generator=g) * scale
+    return TopkInput(ids.to(torch.int32), logits.to(torch.float32))
+
+
+def topk_full() -> TopkInput:
+    return topk_input(65536, 128, seed=7)

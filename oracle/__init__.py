@@ -34,7 +34,7 @@ def build(force: bool = False) -> str:
             and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
         return _LIB
     tmp = _LIB + f".tmp{os.getpid()}"
-    cmd = ["gcc", *CFLAGS, "-o", tmp, _SRC]
+    cmd = ["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB)
     return _LIB
@@ -80,6 +80,8 @@ def lib() -> ctypes.CDLL:
         L.dgro_wgrad_elements.restype = I32
         L.dgro_grouped_dbias.argtypes = [P, I32, I64, I64, I64, P, I64, I64, P, I64, I32]
         L.dgro_grouped_dbias.restype = I32
+        L.dgro_topk_canonicalize.argtypes = [P, I64, P, I64, I64, I64, P, P, P, I64]
+        L.dgro_topk_canonicalize.restype = I32
         _lib = L
     return _lib
 
@@ -226,3 +228,18 @@ def grouped_dbias(dY: np.ndarray, T: int, H: int, ld: int, offs: np.ndarray, out
     rc = lib().dgro_grouped_dbias(_ptr(dY), _dtype_code(dY), T, H, ld, _ptr(o), E, tile_rows, _ptr(out),
                                   ld_out, int(accumulate))
     _check(rc, "grouped_dbias")
+
+
+def topk_canonicalize(ids: np.ndarray, logits: np.ndarray):
+    """Per row: slots stably sorted by id (padding, id < 0, last), logits permuted alike, and the
+    softmax of the valid slots recomputed in that order. Returns (ids, logits, probs)."""
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    logits = np.ascontiguousarray(logits, dtype=np.float32)
+    R, K = ids.shape
+    assert logits.shape == (R, K)
+    oi = np.empty_like(ids)
+    ol = np.empty_like(logits)
+    pr = np.empty_like(logits)
+    rc = lib().dgro_topk_canonicalize(_ptr(ids), K, _ptr(logits), K, R, K, _ptr(oi), _ptr(ol), _ptr(pr), K)
+    _check(rc, "topk_canonicalize")
+    return oi, ol, pr

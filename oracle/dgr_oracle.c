@@ -31,12 +31,16 @@
  *                          weight-gradient main stage.
  *   grouped dbias        - cuDNN-frontend PR #521, commit "Cover dbias": FP32
  *                          partials per M-block and a per-expert segment sum.
+ *   canonical top-K      - Megatron-LM PR #7441, Source 1: ids sorted per row
+ *                          (padding last), logits permuted alike, softmax
+ *                          recomputed in that order.
  *
  * Canonical order (the same for all): partial sums are taken over tiles;
  * inside a tile the leaves are summed by a fixed-width pairwise tree; the tile
  * partials are folded in ascending tile order; the result overwrites the
  * output or is added to it with one rounding.
  */
+#include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -699,6 +703,97 @@ int dgro_grouped_dbias(const void *dY, int32_t dtype, int64_t T, int64_t H, int6
         }
     }
     free(leaf);
+    free(part);
+    return DGRO_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* 6. Canonical compact top-K                                                 */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Megatron-LM PR #7441, Source 1 and its fix _canonicalize_compact_topk: the
+ * compact top-K returns each row's selected ids in a run-dependent slot order
+ * and its softmax is accumulated in that order; the fix sorts the ids of each
+ * row (padding last), permutes the logits with the same permutation and
+ * recomputes the softmax in that order, and rows that are all padding become 0
+ * rather than NaN (review "Checked, no issues found").
+ *
+ * Per row r (K slots; an id < 0 is padding):
+ *   perm = stable sort of the slots by id, padding after every id (padding
+ *          slots keep their order);
+ *   out_ids[k] = ids[perm[k]], out_logits[k] = logits[perm[k]];
+ *   n valid slots (ids >= 0) come first. n = 0: probs = +0.0 everywhere. Else
+ *   m = max of the valid logits; d_k = RN(logit_k - m); e_k = exp(d_k)
+ *   rounded to binary32 (computed in double, then rounded);
+ *   Z = the canonical sum of e_0 .. e_{n-1} in sorted order (tiles of 128,
+ *   pairwise inside, ascending fold); probs[k] = RN(e_k / Z) for k < n, +0.0
+ *   for the padding slots.
+ * Arrays are [R, K] with row strides ld_* (elements).
+ */
+int dgro_topk_canonicalize(const int32_t *ids, int64_t ld_ids, const float *logits, int64_t ld_logits,
+                           int64_t R, int64_t K, int32_t *out_ids, float *out_logits, float *probs,
+                           int64_t ld_out)
+{
+    if (R < 0 || K < 1 || ld_ids < K || ld_logits < K || ld_out < K)
+        return DGRO_ERR_ARG;
+    int64_t *perm = (int64_t *)malloc((size_t)K * sizeof(int64_t));
+    float *e = (float *)malloc((size_t)K * sizeof(float));
+    float *part = (float *)malloc((size_t)((K + 127) / 128) * sizeof(float));
+    if (!perm || !e || !part) {
+        free(perm);
+        free(e);
+        free(part);
+        return DGRO_ERR_NOMEM;
+    }
+    for (int64_t r = 0; r < R; ++r) {
+        const int32_t *id = ids + r * ld_ids;
+        const float *lg = logits + r * ld_logits;
+        /* stable insertion sort of the slot numbers by (padding, id) */
+        for (int64_t k = 0; k < K; ++k) {
+            int64_t j = k;
+            while (j > 0) {
+                int32_t a = id[perm[j - 1]], b = id[k];
+                int a_pad = a < 0, b_pad = b < 0;
+                int after = a_pad ? !b_pad ? 1 : 0 : (!b_pad && a > b);
+                if (!after)
+                    break;
+                perm[j] = perm[j - 1];
+                --j;
+            }
+            perm[j] = k;
+        }
+        int64_t n = 0;
+        for (int64_t k = 0; k < K; ++k) {
+            out_ids[r * ld_out + k] = id[perm[k]];
+            out_logits[r * ld_out + k] = lg[perm[k]];
+            if (id[perm[k]] >= 0)
+                n = k + 1;
+        }
+        float *p = probs + r * ld_out;
+        for (int64_t k = 0; k < K; ++k)
+            p[k] = 0.0f;
+        if (n == 0)
+            continue;
+        float m = lg[perm[0]];
+        for (int64_t k = 1; k < n; ++k)
+            if (lg[perm[k]] > m)
+                m = lg[perm[k]];
+        for (int64_t k = 0; k < n; ++k) {
+            float d = lg[perm[k]] - m;
+            e[k] = (float)exp((double)d);
+        }
+        int64_t n_tiles = (n + 127) / 128;
+        for (int64_t j = 0; j < n_tiles; ++j) {
+            int64_t c = (n - j * 128 < 128) ? n - j * 128 : 128;
+            part[j] = dgro_pairwise(e + j * 128, c, 128);
+        }
+        float z = dgro_fold(part, n_tiles);
+        for (int64_t k = 0; k < n; ++k)
+            p[k] = e[k] / z;
+    }
+    free(perm);
+    free(e);
     free(part);
     return DGRO_OK;
 }
