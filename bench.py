@@ -54,11 +54,16 @@ ALGO = {
     "wgrad_flop": 2 * 4096 * 2048 * 32768,
     "wgrad": 32768 * 4096 * 2 + 32768 * 2048 * 2 + 2 * 8 * 4096 * 2048 * 4,
     "dbias": 65536 * 2048 * 2 + 8 * 2048 * 4,
+    "topk": 65536 * 128 * 4 * 5,
 }
 LAUNCHES = {"colsum_large": 1, "colsum_small": 1, "dprob": 1, "colsum_strided": 1, "index_add": 4, "wgrad": 1,
-            "dbias": 2}
+            "dbias": 2, "topk": 1}
 # operations beyond the step (the next rows of the scope), timed on their own after it
-EXTRAS = ["dbias"]
+EXTRAS = ["dbias", "topk"]
+EXTRA_WORKLOADS = {
+    "dbias": "grouped dbias bf16 65536x2048, 8 experts (multinomial rows) -> fp32 [8, 2048]",
+    "topk": "canonical compact top-K, 65536 rows x 128 slots (int32 ids, fp32 logits; 10 % padding)",
+}
 
 WORKLOAD = ("deterministic reduction step: colsum bf16 8388608x64 + colsum bf16 2048x16 + dprob bf16 "
             "65536x4096 + colsum bf16 4x2048x64 (token stride 128) + index_add fp32 262144x128 -> 16385 rows "
@@ -180,30 +185,39 @@ def make_ops(dev, torch, dgr, with_wgrad, only=None, small=False):
         dp = gi.dprob_full() if not small else gi.dprob_input(16384, 4096, seed=3)
         dY, Y = dp.dY.to(dev), dp.Y.to(dev)
         dprob = torch.zeros(dp.M, device=dev)
-        ops["dprob"] = lambda: dgr.ordered_rowdot_dprob(dY, Y, dprob)
+        ops["dprob"] = lambda dY=dY, Y=Y, dprob=dprob: dgr.ordered_rowdot_dprob(dY, Y, dprob)
         host["dprob"] = ([dp.dY, dp.Y], [dY, Y])
         outs["dprob"] = dprob
     if want("index_add"):
         ia = gi.index_add_full()
         src, idx, iout = ia.src.to(dev), ia.idx.to(dev), ia.out.to(dev)
         iws = dgr.workspace(dgr.index_add_workspace_bytes(262144, 16384, 128), dev)
-        ops["index_add"] = lambda: dgr.det_index_add(iout, src, idx, ws=iws)
+        ops["index_add"] = lambda iout=iout, src=src, idx=idx, iws=iws: dgr.det_index_add(iout, src, idx, ws=iws)
         host["index_add"] = ([ia.src, ia.idx, ia.out], [src, idx, iout])
         outs["index_add"] = iout
     if with_wgrad and want("wgrad"):
         wi = gi.wgrad_full() if not small else gi.wgrad_input(8, 8192, 4096, 2048, seed=5)
         G, X, offs, mg = wi.G.to(dev), wi.X.to(dev), wi.offs.to(dev), wi.main_grad.to(dev)
         wws = dgr.workspace(dgr.wgrad_workspace_bytes(8, 4096, 2048), dev)
-        ops["wgrad"] = lambda: dgr.grouped_wgrad_accumulate(G, X, offs, mg, ws=wws)
+        ops["wgrad"] = (lambda G=G, X=X, offs=offs, mg=mg, wws=wws:
+                        dgr.grouped_wgrad_accumulate(G, X, offs, mg, ws=wws))
         host["wgrad"] = ([wi.G, wi.X, wi.offs, wi.main_grad], [G, X, offs, mg])
         outs["wgrad"] = mg
     if want("dbias"):
         db = gi.dbias_full() if not small else gi.dbias_input(16384, 2048, 8, seed=6)
-        dY, doffs, dout = db.dY.to(dev), db.offs.to(dev), db.out.to(dev)
-        dws = dgr.workspace(dgr.dbias_workspace_bytes(db.T, db.H, db.E), dev)
-        ops["dbias"] = lambda: dgr.grouped_dbias(dY, doffs, dout, ws=dws)
-        host["dbias"] = ([db.dY, db.offs], [dY, doffs])
-        outs["dbias"] = dout
+        bdY, boffs, bout = db.dY.to(dev), db.offs.to(dev), db.out.to(dev)
+        bws = dgr.workspace(dgr.dbias_workspace_bytes(db.T, db.H, db.E), dev)
+        ops["dbias"] = (lambda bdY=bdY, boffs=boffs, bout=bout, bws=bws:
+                        dgr.grouped_dbias(bdY, boffs, bout, ws=bws))
+        host["dbias"] = ([db.dY, db.offs], [bdY, boffs])
+        outs["dbias"] = bout
+    if want("topk"):
+        tk = gi.topk_full()
+        tids, tlg = tk.ids.to(dev), tk.logits.to(dev)
+        tout = (torch.empty_like(tids), torch.empty_like(tlg), torch.empty_like(tlg))
+        ops["topk"] = lambda tids=tids, tlg=tlg, tout=tout: dgr.topk_canonicalize(tids, tlg, *tout)
+        host["topk"] = ([tk.ids, tk.logits], [tids, tlg])
+        outs["topk"] = tout[2]
     steps = ["colsum_large", "colsum_small", "dprob", "colsum_strided", "index_add", "wgrad"]
     order = [n for n in steps + (EXTRAS if only in EXTRAS else []) if n in ops]
     return order, ops, host, outs
@@ -334,8 +348,7 @@ def run_ours(args, rank, world, local_rank):
     for n, ms in extra_ms.items():
         gbs = ALGO[n] / (ms * 1e-3) / 1e9
         next_rows[n] = {"us": round(ms * 1e3, 2), "gbs": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm"], 4),
-                        "launches": LAUNCHES[n], "dram_traffic": traffic.get(n),
-                        "workload": "grouped dbias bf16 65536x2048, 8 experts (multinomial rows) -> fp32 [8, 2048]"}
+                        "launches": LAUNCHES[n], "dram_traffic": traffic.get(n), "workload": EXTRA_WORKLOADS[n]}
     dom = max(order, key=lambda n: per_ms[n])
     if dom == "wgrad":
         ach = ALGO["wgrad_flop"] / (per_ms[dom] * 1e-3) / 1e12
@@ -484,7 +497,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["colsum_large", "colsum_small", "dprob", "colsum_strided", "index_add",
-                                       "wgrad", "dbias"], help="profiling: run one operation only (no JSON bench line)")
+                                       "wgrad", "dbias", "topk"],
+                    help="profiling: run one operation only (no JSON bench line)")
     ap.add_argument("--small", action="store_true",
                     help="profiling: colsum 2097152x64, dprob 16384x4096, wgrad T=8192 (same widths)")
     args = ap.parse_args()

@@ -61,6 +61,7 @@ def lib() -> ctypes.CDLL:
             "dgr_grouped_wgrad_accumulate": ([P, P, P, I32, I64, I64, I64, P, I32, P, SZ, P], I32),
             "dgr_dbias_workspace_bytes": ([I64, I64, I32, I32], SZ),
             "dgr_grouped_dbias": ([P, I32, I64, I64, I64, P, I32, P, I64, I32, I32, P, SZ, P], I32),
+            "dgr_topk_canonicalize": ([P, I64, P, I64, I64, I32, P, P, P, I64, P], I32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -204,3 +205,24 @@ def grouped_dbias(dY: torch.Tensor, offs: torch.Tensor, out: torch.Tensor, *, ac
         _ptr(dY), _dtype(dY), T, H, dY.stride(0), _ptr(offs), E, _ptr(out), out.stride(0), int(accumulate),
         tile_rows, _ptr(ws), ws.numel(), _stream(stream)))
     return out
+
+
+def topk_canonicalize(ids: torch.Tensor, logits: torch.Tensor, out_ids: torch.Tensor | None = None,
+                      out_logits: torch.Tensor | None = None, probs: torch.Tensor | None = None, *,
+                      stream=None):
+    """Per row: slots sorted stably by id (padding, id < 0, last), logits permuted alike, softmax of
+    the valid slots recomputed in that order. ids int32 [R, K], logits fp32 [R, K]."""
+    if ids.dim() != 2 or ids.dtype != torch.int32 or logits.shape != ids.shape or logits.dtype != torch.float32:
+        raise ValueError("ids int32 [R, K] and logits fp32 [R, K] expected")
+    R, K = ids.shape
+    out_ids = torch.empty_like(ids) if out_ids is None else out_ids
+    out_logits = torch.empty_like(logits) if out_logits is None else out_logits
+    probs = torch.empty_like(logits) if probs is None else probs
+    ld = out_ids.stride(0)
+    if out_logits.stride(0) != ld or probs.stride(0) != ld or any(t.stride(1) != 1 for t in
+                                                                  (ids, logits, out_ids, out_logits, probs)):
+        raise ValueError("outputs must share one row stride; rows contiguous")
+    _check("dgr_topk_canonicalize", lib().dgr_topk_canonicalize(
+        _ptr(ids), ids.stride(0), _ptr(logits), logits.stride(0), R, K, _ptr(out_ids), _ptr(out_logits),
+        _ptr(probs), ld, _stream(stream)))
+    return out_ids, out_logits, probs

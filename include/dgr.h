@@ -253,6 +253,32 @@ dgr_status dgr_grouped_dbias(const void *dY, int32_t dtype, int64_t T, int64_t H
                              const int64_t *d_offs, int32_t E, float *dbias, int64_t ld_out,
                              int32_t accumulate, int32_t tile_rows, void *ws, size_t ws_bytes, void *stream);
 
+/* ------------------------------------------------------------------------ */
+/* 6. Canonical compact top-K                                                */
+/* ------------------------------------------------------------------------ */
+/*
+ * Megatron-LM PR #7441, Source 1 and its fix _canonicalize_compact_topk: the
+ * compact top-K returns each row's ids in a run-dependent slot order and
+ * accumulates its softmax in that order; the ids are sorted per row with
+ * padding last, the logits permuted alike and the softmax recomputed in that
+ * order; rows that are all padding become 0 rather than NaN.
+ *
+ *   per row: slots sorted stably by id, ids < 0 (padding) after every id;
+ *   out_ids[k] = ids[perm[k]], out_logits[k] = logits[perm[k]];
+ *   over the n valid slots (they come first): m = max logit, d = RN(l - m),
+ *   e = expf(d), Z = canonical sum of e in sorted order (tiles of 128,
+ *   pairwise inside, ascending fold), probs[k] = RN(e_k / Z); padding slots
+ *   and all-padding rows get +0.0.
+ *
+ * ids:      [R, K] int32, row stride ld_ids; logits: [R, K] fp32, ld_logits.
+ * out_ids, out_logits, probs: [R, K], row stride ld_out; none may overlap an
+ *           input or each other.
+ * Limits:   1 <= K <= 256. No workspace: rows are independent.
+ */
+dgr_status dgr_topk_canonicalize(const int32_t *ids, int64_t ld_ids, const float *logits, int64_t ld_logits,
+                                 int64_t R, int32_t K, int32_t *out_ids, float *out_logits, float *probs,
+                                 int64_t ld_out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

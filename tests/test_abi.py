@@ -125,3 +125,13 @@ def test_dbias_workspace_size(L):
     assert n >= 256 + (512 + 8) * 2048 * 4
     assert dgr.dbias_workspace_bytes(100, 16, 0) == 0
     assert dgr.dbias_workspace_bytes(100, 16, 2, 3) == 0
+
+
+def test_topk_host_checks(L):
+    a, b, c, d, e = (_p(x) for x in (0x100000, 0x200000, 0x300000, 0x400000, 0x500000))
+    assert L.dgr_topk_canonicalize(a, 128, b, 128, 10, 0, c, d, e, 128, None) == 1     # K = 0
+    assert L.dgr_topk_canonicalize(a, 300, b, 300, 10, 300, c, d, e, 300, None) == 2   # K beyond 256
+    assert L.dgr_topk_canonicalize(a, 100, b, 128, 10, 128, c, d, e, 128, None) == 1   # ld below K
+    assert L.dgr_topk_canonicalize(a, 128, b, 128, 10, 128, _p(0x100100), d, e, 128, None) == 4  # output on input
+    assert L.dgr_topk_canonicalize(a, 128, b, 128, 10, 128, c, c, e, 128, None) == 4   # outputs overlap
+    assert L.dgr_topk_canonicalize(_p(0x100002), 128, b, 128, 10, 128, c, d, e, 128, None) == 5
