@@ -31,6 +31,10 @@ The five workloads (shapes, distributions and draw order):
                  (slot k's id in [k*512, (k+1)*512) of 65536 keys), slots
                  shuffled per row; 10 % of the slots then padding (-1) and
                  every 64th row all padding; logits ~ N(0, 3^2) fp32          seed 7
+  aux loss       router probs fp32 [65536, 128] = softmax over the experts of
+                 N(0, 1) logits; tokens_per_expert int32 [128] = counts of a
+                 top-8 routing (8 experts drawn per token without
+                 replacement); scale = 1e-2 * E / (topk * N^2)               seed 8
 """
 from __future__ import annotations
 
@@ -361,3 +365,31 @@ def topk_input(R: int, K: int, *, seed: int, n_keys: int = 65536, pad_frac: floa
 
 def topk_full() -> TopkInput:
     return topk_input(65536, 128, seed=7)
+
+
+# --------------------------------------------------------------------------
+# aux-loss scalar
+# --------------------------------------------------------------------------
+
+@dataclass
+class AuxInput:
+    probs: torch.Tensor   # fp32 [N, E]
+    tpe: torch.Tensor     # int32 [E]
+    scale: float
+
+
+def aux_input(N: int, E: int, *, seed: int, topk: int = 8, dist: str = "softmax", coeff: float = 1e-2) -> AuxInput:
+    g = _gen(seed)
+    if dist == "softmax":
+        probs = torch.softmax(torch.randn((N, E), generator=g), dim=1)
+    else:
+        probs = _draw((N, E), dist, g)
+    k = min(topk, E)
+    picks = torch.argsort(torch.rand((max(N, 1), E), generator=g), dim=1)[:N, :k]
+    tpe = torch.bincount(picks.reshape(-1), minlength=E)
+    scale = coeff * E / (k * max(N, 1) ** 2)
+    return AuxInput(probs.to(torch.float32), tpe.to(torch.int32), scale)
+
+
+def aux_full() -> AuxInput:
+    return aux_input(65536, 128, seed=8)

@@ -82,6 +82,8 @@ def lib() -> ctypes.CDLL:
         L.dgro_grouped_dbias.restype = I32
         L.dgro_topk_canonicalize.argtypes = [P, I64, P, I64, I64, I64, P, P, P, I64]
         L.dgro_topk_canonicalize.restype = I32
+        L.dgro_aux_loss.argtypes = [P, I64, I64, I64, P, F32, P]
+        L.dgro_aux_loss.restype = I32
         _lib = L
     return _lib
 
@@ -243,3 +245,16 @@ def topk_canonicalize(ids: np.ndarray, logits: np.ndarray):
     rc = lib().dgro_topk_canonicalize(_ptr(ids), K, _ptr(logits), K, R, K, _ptr(oi), _ptr(ol), _ptr(pr), K)
     _check(rc, "topk_canonicalize")
     return oi, ol, pr
+
+
+def aux_loss(probs: np.ndarray, tokens_per_expert: np.ndarray, scale: float) -> np.float32:
+    """RN(scale * S): S = the canonical sum over tokens (tiles of 128) of each token's canonical
+    row dot of probs[t] with tokens_per_expert (expert tiles of 128)."""
+    p = np.ascontiguousarray(probs, dtype=np.float32)
+    tpe = np.ascontiguousarray(tokens_per_expert, dtype=np.int32)
+    N, E = p.shape
+    assert tpe.shape == (E,)
+    out = np.zeros(1, np.float32)
+    rc = lib().dgro_aux_loss(_ptr(p), N, E, E, _ptr(tpe), np.float32(scale), _ptr(out))
+    _check(rc, "aux_loss")
+    return out[0]

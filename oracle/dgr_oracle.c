@@ -34,6 +34,9 @@
  *   canonical top-K      - Megatron-LM PR #7441, Source 1: ids sorted per row
  *                          (padding last), logits permuted alike, softmax
  *                          recomputed in that order.
+ *   aux-loss scalar      - Megatron-LM PR #7441, Source 5: the router aux loss
+ *                          summed in a fixed order instead of by a float
+ *                          atomicAdd across blocks.
  *
  * Canonical order (the same for all): partial sums are taken over tiles;
  * inside a tile the leaves are summed by a fixed-width pairwise tree; the tile
@@ -795,5 +798,65 @@ int dgro_topk_canonicalize(const int32_t *ids, int64_t ld_ids, const float *logi
     free(perm);
     free(e);
     free(part);
+    return DGRO_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* 7. Deterministic aux-loss scalar                                           */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Megatron-LM PR #7441, Source 5 and the follow-up note on determinism.py:
+ * the fused router aux loss reduces its scalar with a cross-block float
+ * atomicAdd, and its gradient with respect to probs[t][e] is the closed form
+ * coeff*E/(topk*N^2)*tokens_per_expert[e], so the loss is that factor times
+ * sum over t, e of probs[t][e] * tokens_per_expert[e]. The deterministic form
+ * takes that sum in the canonical order, in two levels:
+ *   x[t] = fold over expert tiles of pw_128( RN(probs[t][e] * tpe[e]) )
+ *          (the row dot of the dprob reduction, with tpe as the other row);
+ *   S    = fold over token tiles of pw_128( x[t] )  (the column sum at H = 1);
+ *   aux  = RN(scale * S), scale = coeff*E/(topk*N^2) given by the caller.
+ * tokens_per_expert are counts, exact in binary32 below 2^24. With N = 0 the
+ * sum is +0.0. probs[t][e] is at t*ld + e.
+ */
+int dgro_aux_loss(const float *probs, int64_t N, int64_t E, int64_t ld, const int32_t *tpe, float scale,
+                  float *aux)
+{
+    if (N < 0 || E < 1 || ld < E)
+        return DGRO_ERR_ARG;
+    int64_t e_tiles = (E + 127) / 128, t_tiles = (N + 127) / 128;
+    float *leaf = (float *)malloc(128 * sizeof(float));
+    float *epart = (float *)malloc((size_t)e_tiles * sizeof(float));
+    float *x = (float *)malloc((size_t)(N > 0 ? N : 1) * sizeof(float));
+    float *tpart = (float *)malloc((size_t)(t_tiles > 0 ? t_tiles : 1) * sizeof(float));
+    if (!leaf || !epart || !x || !tpart) {
+        free(leaf);
+        free(epart);
+        free(x);
+        free(tpart);
+        return DGRO_ERR_NOMEM;
+    }
+    for (int64_t t = 0; t < N; ++t) {
+        for (int64_t k = 0; k < e_tiles; ++k) {
+            int64_t c = (E - k * 128 < 128) ? E - k * 128 : 128;
+            for (int64_t i = 0; i < c; ++i)
+                leaf[i] = probs[t * ld + k * 128 + i] * (float)tpe[k * 128 + i];
+            epart[k] = dgro_pairwise(leaf, c, 128);
+        }
+        x[t] = dgro_fold(epart, e_tiles);
+    }
+    float s = 0.0f;
+    if (N > 0) {
+        for (int64_t j = 0; j < t_tiles; ++j) {
+            int64_t c = (N - j * 128 < 128) ? N - j * 128 : 128;
+            tpart[j] = dgro_pairwise(x + j * 128, c, 128);
+        }
+        s = dgro_fold(tpart, t_tiles);
+    }
+    *aux = scale * s;
+    free(leaf);
+    free(epart);
+    free(x);
+    free(tpart);
     return DGRO_OK;
 }
