@@ -55,14 +55,16 @@ ALGO = {
     "wgrad": 32768 * 4096 * 2 + 32768 * 2048 * 2 + 2 * 8 * 4096 * 2048 * 4,
     "dbias": 65536 * 2048 * 2 + 8 * 2048 * 4,
     "topk": 65536 * 128 * 4 * 5,
+    "aux_loss": 65536 * 128 * 4 + 128 * 4 + 4,
 }
 LAUNCHES = {"colsum_large": 1, "colsum_small": 1, "dprob": 1, "colsum_strided": 1, "index_add": 4, "wgrad": 1,
-            "dbias": 2, "topk": 1}
+            "dbias": 2, "topk": 1, "aux_loss": 1}
 # operations beyond the step (the next rows of the scope), timed on their own after it
-EXTRAS = ["dbias", "topk"]
+EXTRAS = ["dbias", "topk", "aux_loss"]
 EXTRA_WORKLOADS = {
     "dbias": "grouped dbias bf16 65536x2048, 8 experts (multinomial rows) -> fp32 [8, 2048]",
     "topk": "canonical compact top-K, 65536 rows x 128 slots (int32 ids, fp32 logits; 10 % padding)",
+    "aux_loss": "router aux-loss scalar, fp32 probs 65536 x 128 with top-8 expert counts",
 }
 
 WORKLOAD = ("deterministic reduction step: colsum bf16 8388608x64 + colsum bf16 2048x16 + dprob bf16 "
@@ -218,6 +220,15 @@ def make_ops(dev, torch, dgr, with_wgrad, only=None, small=False):
         ops["topk"] = lambda tids=tids, tlg=tlg, tout=tout: dgr.topk_canonicalize(tids, tlg, *tout)
         host["topk"] = ([tk.ids, tk.logits], [tids, tlg])
         outs["topk"] = tout[2]
+    if want("aux_loss"):
+        ax = gi.aux_full()
+        aprobs, atpe = ax.probs.to(dev), ax.tpe.to(dev)
+        aout = torch.empty(1, device=dev)
+        aws = dgr.workspace(dgr.aux_loss_workspace_bytes(ax.probs.shape[0]), dev)
+        ops["aux_loss"] = (lambda aprobs=aprobs, atpe=atpe, aout=aout, aws=aws, sc=ax.scale:
+                           dgr.aux_loss(aprobs, atpe, sc, aout, ws=aws))
+        host["aux_loss"] = ([ax.probs, ax.tpe], [aprobs, atpe])
+        outs["aux_loss"] = aout
     steps = ["colsum_large", "colsum_small", "dprob", "colsum_strided", "index_add", "wgrad"]
     order = [n for n in steps + (EXTRAS if only in EXTRAS else []) if n in ops]
     return order, ops, host, outs
@@ -305,20 +316,43 @@ def run_ours(args, rank, world, local_rank):
 
     # end to end through host buffers: pinned host inputs copied in, outputs read back, every step
     # the next rows of the scope, each timed on its own after the step (not in
-    # the step, its value or its launch count)
-    extra_ms = {}
+    # the step, its value or its launch count). Each is captured as a CUDA graph
+    # of 20 calls and the graph replayed, so that the device time of a short
+    # call is not hidden behind the host's per-call work (the library holds no
+    # host state and synchronises nothing, so its calls capture as they run);
+    # plain launches if capture is refused.
+    extra_ms, extra_how = {}, {}
     for n in [x for x in EXTRAS if x in ops]:
         for _ in range(args.warmup):
             ops[n]()
-        evx = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        torch.cuda.synchronize()
+        reps = 20
+        graph = None
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                for _ in range(reps):
+                    ops[n]()
+            graph.replay()
+            torch.cuda.synchronize()
+        except Exception:  # noqa: BLE001
+            graph = None
+            torch.cuda.synchronize()
+        n_rep = max(1, K // reps) if graph is not None else K
+        evx = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_rep)]
         barrier()
         torch.cuda.synchronize()
         for a, b in evx:
             a.record(stream)
-            ops[n]()
+            if graph is not None:
+                graph.replay()
+            else:
+                ops[n]()
             b.record(stream)
         torch.cuda.synchronize()
-        extra_ms[n] = sum(a.elapsed_time(b) for a, b in evx) / K
+        calls = n_rep * (reps if graph is not None else 1)
+        extra_ms[n] = sum(a.elapsed_time(b) for a, b in evx) / calls
+        extra_how[n] = f"CUDA graph of {reps} calls, {n_rep} replays" if graph is not None else "plain launches"
         if world > 1:
             t = torch.tensor([extra_ms[n]], device=dev)
             torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -348,7 +382,8 @@ def run_ours(args, rank, world, local_rank):
     for n, ms in extra_ms.items():
         gbs = ALGO[n] / (ms * 1e-3) / 1e9
         next_rows[n] = {"us": round(ms * 1e3, 2), "gbs": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm"], 4),
-                        "launches": LAUNCHES[n], "dram_traffic": traffic.get(n), "workload": EXTRA_WORKLOADS[n]}
+                        "launches": LAUNCHES[n], "dram_traffic": traffic.get(n), "workload": EXTRA_WORKLOADS[n],
+                        "timed_as": extra_how[n]}
     dom = max(order, key=lambda n: per_ms[n])
     if dom == "wgrad":
         ach = ALGO["wgrad_flop"] / (per_ms[dom] * 1e-3) / 1e12
@@ -497,7 +532,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["colsum_large", "colsum_small", "dprob", "colsum_strided", "index_add",
-                                       "wgrad", "dbias", "topk"],
+                                       "wgrad", "dbias", "topk", "aux_loss"],
                     help="profiling: run one operation only (no JSON bench line)")
     ap.add_argument("--small", action="store_true",
                     help="profiling: colsum 2097152x64, dprob 16384x4096, wgrad T=8192 (same widths)")

@@ -62,6 +62,8 @@ def lib() -> ctypes.CDLL:
             "dgr_dbias_workspace_bytes": ([I64, I64, I32, I32], SZ),
             "dgr_grouped_dbias": ([P, I32, I64, I64, I64, P, I32, P, I64, I32, I32, P, SZ, P], I32),
             "dgr_topk_canonicalize": ([P, I64, P, I64, I64, I32, P, P, P, I64, P], I32),
+            "dgr_aux_loss_workspace_bytes": ([I64], SZ),
+            "dgr_aux_loss": ([P, I64, I32, I64, P, ctypes.c_float, P, P, SZ, P], I32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -226,3 +228,25 @@ def topk_canonicalize(ids: torch.Tensor, logits: torch.Tensor, out_ids: torch.Te
         _ptr(ids), ids.stride(0), _ptr(logits), logits.stride(0), R, K, _ptr(out_ids), _ptr(out_logits),
         _ptr(probs), ld, _stream(stream)))
     return out_ids, out_logits, probs
+
+
+def aux_loss_workspace_bytes(N: int) -> int:
+    return int(lib().dgr_aux_loss_workspace_bytes(N))
+
+
+def aux_loss(probs: torch.Tensor, tokens_per_expert: torch.Tensor, scale: float, out: torch.Tensor | None = None, *,
+             ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """out[0] = RN(scale * S), S the canonical sum of probs * tokens_per_expert (each token's row dot,
+    then the column sum over tokens). probs fp32 [N, E]; tokens_per_expert int32 [E] on the device."""
+    if probs.dim() != 2 or probs.dtype != torch.float32 or tokens_per_expert.dtype != torch.int32:
+        raise ValueError("probs fp32 [N, E] and tokens_per_expert int32 [E] expected")
+    N, E = probs.shape
+    if tokens_per_expert.shape != (E,) or probs.stride(1) != 1:
+        raise ValueError("tokens_per_expert [E] and rows of probs contiguous expected")
+    out = torch.empty(1, dtype=torch.float32, device=probs.device) if out is None else out
+    if ws is None:
+        ws = workspace(aux_loss_workspace_bytes(N), probs.device)
+    _check("dgr_aux_loss", lib().dgr_aux_loss(
+        _ptr(probs), N, E, probs.stride(0), _ptr(tokens_per_expert), float(scale), _ptr(out), _ptr(ws), ws.numel(),
+        _stream(stream)))
+    return out

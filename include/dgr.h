@@ -279,6 +279,32 @@ dgr_status dgr_topk_canonicalize(const int32_t *ids, int64_t ld_ids, const float
                                  int64_t R, int32_t K, int32_t *out_ids, float *out_logits, float *probs,
                                  int64_t ld_out, void *stream);
 
+/* ------------------------------------------------------------------------ */
+/* 7. Deterministic aux-loss scalar                                          */
+/* ------------------------------------------------------------------------ */
+/*
+ * Megatron-LM PR #7441, Source 5: the fused router aux loss reduces its scalar
+ * with a cross-block float atomicAdd; its gradient is the closed form
+ * coeff*E/(topk*N^2)*tokens_per_expert[e], so the loss is that factor times
+ * sum over t, e of probs[t][e] * tokens_per_expert[e]. Here:
+ *
+ *   x[t] = fold over expert tiles of pw_128( RN(probs[t][e] * tpe[e]) );
+ *   S    = fold over token tiles of pw_128( x[t] );
+ *   *d_out = RN(scale * S)        (N = 0: RN(scale * +0.0)).
+ *
+ * probs:    [N, E] fp32, row stride ld (elements). tokens_per_expert: [E]
+ *           int32 DEVICE counts (exact in binary32 below 2^24).
+ * scale:    the caller's factor, e.g. coeff * E / (topk * N^2).
+ * d_out:    one DEVICE fp32 (overwritten).
+ * Limits:   1 <= E <= 1024, N < 2^31.
+ * ws:       dgr_aux_loss_workspace_bytes(N) bytes, zeroed once (a ticket and
+ *           one FP32 partial per tile of 128 tokens).
+ * d_out must not overlap probs, tokens_per_expert or ws.
+ */
+size_t dgr_aux_loss_workspace_bytes(int64_t N);
+dgr_status dgr_aux_loss(const float *probs, int64_t N, int32_t E, int64_t ld, const int32_t *d_tokens_per_expert,
+                        float scale, float *d_out, void *ws, size_t ws_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -135,3 +135,14 @@ def test_topk_host_checks(L):
     assert L.dgr_topk_canonicalize(a, 128, b, 128, 10, 128, _p(0x100100), d, e, 128, None) == 4  # output on input
     assert L.dgr_topk_canonicalize(a, 128, b, 128, 10, 128, c, c, e, 128, None) == 4   # outputs overlap
     assert L.dgr_topk_canonicalize(_p(0x100002), 128, b, 128, 10, 128, c, d, e, 128, None) == 5
+
+
+def test_aux_loss_host_checks(L):
+    pr, tp, o, ws = _p(0x100000), _p(0x200000), _p(0x300000), _p(0x400000)
+    F = ctypes.c_float
+    assert L.dgr_aux_loss(pr, 10, 0, 8, tp, F(1.0), o, ws, 1 << 20, None) == 1       # E = 0
+    assert L.dgr_aux_loss(pr, 10, 2000, 2000, tp, F(1.0), o, ws, 1 << 20, None) == 2  # E beyond 1024
+    assert L.dgr_aux_loss(pr, 10, 8, 4, tp, F(1.0), o, ws, 1 << 20, None) == 1       # ld below E
+    assert L.dgr_aux_loss(pr, 1000, 8, 8, tp, F(1.0), o, ws, 16, None) == 3          # workspace too small
+    assert L.dgr_aux_loss(pr, 10, 8, 8, tp, F(1.0), _p(0x100004), ws, 1 << 20, None) == 4  # out inside probs
+    assert dgr.aux_loss_workspace_bytes(65536) == 256 + 512 * 4
