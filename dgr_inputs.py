@@ -35,6 +35,10 @@ The five workloads (shapes, distributions and draw order):
                  N(0, 1) logits; tokens_per_expert int32 [128] = counts of a
                  top-8 routing (8 experts drawn per token without
                  replacement); scale = 1e-2 * E / (topk * N^2)               seed 8
+  dsrelu dprob   expert of each of 16384 tokens ~ multinomial(uniform over 8),
+                 counts -> offsets; A bf16 [16384, 2048] ~ N(0, 1), B bf16
+                 [8, 2048, 4096] ~ N(0, 1/2048) (so C ~ N(0, 1)), dY bf16
+                 [16384, 4096] ~ N(0, 1); dprob fp32 [16384] zeros           seed 9
 """
 from __future__ import annotations
 
@@ -393,3 +397,39 @@ def aux_input(N: int, E: int, *, seed: int, topk: int = 8, dist: str = "softmax"
 
 def aux_full() -> AuxInput:
     return aux_input(65536, 128, seed=8)
+
+
+# --------------------------------------------------------------------------
+# dprob fused into the grouped dsReLU GEMM
+# --------------------------------------------------------------------------
+
+@dataclass
+class DsreluInput:
+    A: torch.Tensor      # bf16 [T, K], rows grouped by expert
+    B: torch.Tensor      # bf16 [E, K, N]
+    dY: torch.Tensor     # bf16 [T, N]
+    offs: torch.Tensor   # int64 [E + 1]
+    dprob: torch.Tensor  # fp32 [T]
+
+
+def dsrelu_input(E: int, T: int, K: int, N: int, *, seed: int, dist: str = "normal",
+                 counts: list[int] | None = None, out_init: str = "zeros") -> DsreluInput:
+    g = _gen(seed)
+    if counts is None:
+        ex = torch.multinomial(torch.ones(E), T, replacement=True, generator=g)
+        cnt = torch.bincount(ex, minlength=E)
+    else:
+        assert len(counts) == E and sum(counts) == T
+        cnt = torch.tensor(counts, dtype=torch.int64)
+    offs = torch.zeros(E + 1, dtype=torch.int64)
+    offs[1:] = torch.cumsum(cnt, 0)
+    A = _draw((T, K), dist, g).to(torch.bfloat16)
+    Bs = 1.0 if dist == "ternary" else K ** -0.5
+    B = (_draw((E, K, N), dist, g) * Bs).to(torch.bfloat16)
+    dY = _draw((T, N), dist, g).to(torch.bfloat16)
+    dprob = torch.zeros(T, dtype=torch.float32) if out_init == "zeros" else _draw((T,), "normal", g)
+    return DsreluInput(A, B, dY, offs, dprob.to(torch.float32))
+
+
+def dsrelu_full() -> DsreluInput:
+    return dsrelu_input(8, 16384, 2048, 4096, seed=9)

@@ -84,6 +84,8 @@ def lib() -> ctypes.CDLL:
         L.dgro_topk_canonicalize.restype = I32
         L.dgro_aux_loss.argtypes = [P, I64, I64, I64, P, F32, P]
         L.dgro_aux_loss.restype = I32
+        L.dgro_dsrelu_dprob.argtypes = [P, P, P, I64, I64, I64, I64, P, P, I32, P, I64, P]
+        L.dgro_dsrelu_dprob.restype = I32
         _lib = L
     return _lib
 
@@ -258,3 +260,21 @@ def aux_loss(probs: np.ndarray, tokens_per_expert: np.ndarray, scale: float) -> 
     rc = lib().dgro_aux_loss(_ptr(p), N, E, E, _ptr(tpe), np.float32(scale), _ptr(out))
     _check(rc, "aux_loss")
     return out[0]
+
+
+def dsrelu_dprob(A_bits: np.ndarray, B_bits: np.ndarray, offs: np.ndarray, dY_bits: np.ndarray, dprob: np.ndarray,
+                 *, accumulate: bool = False, rows: np.ndarray | None = None, model: TcModel | None = None):
+    """dprob[m] (+)= fold over N-tiles of pw_128(RN(dY * RN(relu(C)^2))), C = A_e B_e by K16
+    tensor-core steps. A [T, K], B [E, K, N], dY [T, N] bf16 bits; with `rows`, dprob[i] is row rows[i]."""
+    A = np.ascontiguousarray(A_bits, dtype=np.uint16)
+    B = np.ascontiguousarray(B_bits, dtype=np.uint16)
+    dY = np.ascontiguousarray(dY_bits, dtype=np.uint16)
+    o = np.ascontiguousarray(offs, dtype=np.int64)
+    T, K = A.shape
+    E, K2, N = B.shape
+    assert K2 == K and dY.shape == (T, N) and o.size == E + 1 and dprob.dtype == np.float32
+    m = model or default_tc_model()
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    rc = lib().dgro_dsrelu_dprob(_ptr(A), _ptr(B), _ptr(o), E, T, K, N, _ptr(dY), _ptr(dprob), int(accumulate),
+                                 _ptr(r) if r is not None else None, 0 if r is None else r.size, ctypes.byref(m))
+    _check(rc, "dsrelu_dprob")

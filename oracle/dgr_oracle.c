@@ -37,6 +37,8 @@
  *   aux-loss scalar      - Megatron-LM PR #7441, Source 5: the router aux loss
  *                          summed in a fixed order instead of by a float
  *                          atomicAdd across blocks.
+ *   dsReLU dprob         - cuDNN-frontend PR #521: dprob from the grouped GEMM's
+ *                          relu(C)^2, one slot per N-tile, fixed-order reduce.
  *
  * Canonical order (the same for all): partial sums are taken over tiles;
  * inside a tile the leaves are summed by a fixed-width pairwise tree; the tile
@@ -858,5 +860,80 @@ int dgro_aux_loss(const float *probs, int64_t N, int64_t E, int64_t ld, const in
     free(epart);
     free(x);
     free(tpart);
+    return DGRO_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* 8. dprob fused into its grouped dsReLU GEMM                                */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * cuDNN-frontend PR #521 ("grouped gemm dsrelu deterministic dprob"): the
+ * backward kernel recomputes the grouped GEMM C = A_e B_e, reuses relu(C)^2
+ * between d_srelu and dprob, and dprob[m] is a float reduction over N; the
+ * deterministic form parks each N-tile's partial in its own slot (one writer
+ * per (token, tile_n)) and reduces the slots in a fixed order, accumulating
+ * into dprob. Here, for expert e (rows offs[e] .. offs[e+1]-1 of A and dY):
+ *   C[m][n] = K16 tensor-core steps over k ascending, from a fresh accumulator
+ *             (dgro_tc_k16), A [T][K] and B [E][K][N] bf16;
+ *   s = RN(r * r) with r = max(C, 0);  leaf = RN(fp32(dY[m][n]) * s);
+ *   dprob[m] = fold over N-tiles of 128 of pw_128(leaves), written or added
+ *   with one rounding.
+ * rows (nullable, n_rows entries) restricts the work to those rows of A.
+ */
+static float dsrelu_row(const uint16_t *A, const uint16_t *B, int64_t e, int64_t K, int64_t N,
+                        const uint16_t *dY, int64_t t, float *leaf, float *part, const dgro_tc_model *m)
+{
+    uint16_t a[16], b[16];
+    int64_t n_tiles = (N + 127) / 128;
+    for (int64_t j = 0; j < n_tiles; ++j) {
+        int64_t c = (N - j * 128 < 128) ? N - j * 128 : 128;
+        for (int64_t i = 0; i < c; ++i) {
+            int64_t n = j * 128 + i;
+            float acc = 0.0f;
+            for (int64_t s = 0; s < K / 16; ++s) {
+                for (int q = 0; q < 16; ++q) {
+                    a[q] = A[t * K + 16 * s + q];
+                    b[q] = B[(e * K + 16 * s + q) * N + n];
+                }
+                acc = dgro_tc_k16(acc, s > 0, a, b, m);
+            }
+            float r = acc > 0.0f ? acc : 0.0f;
+            float sq = r * r;
+            leaf[i] = dgro_bf16_to_f32(dY[t * N + n]) * sq;
+        }
+        part[j] = dgro_pairwise(leaf, c, 128);
+    }
+    return dgro_fold(part, n_tiles);
+}
+
+int dgro_dsrelu_dprob(const uint16_t *A, const uint16_t *B, const int64_t *offs, int64_t E, int64_t T,
+                      int64_t K, int64_t N, const uint16_t *dY, float *dprob, int32_t accumulate,
+                      const int64_t *rows, int64_t n_rows, const dgro_tc_model *m)
+{
+    if (E < 1 || T < 0 || K < 16 || K % 16 != 0 || N < 1 || offs[0] != 0 || offs[E] != T)
+        return DGRO_ERR_ARG;
+    for (int64_t e = 0; e < E; ++e)
+        if (offs[e + 1] < offs[e])
+            return DGRO_ERR_ARG;
+    float *leaf = (float *)malloc(128 * sizeof(float));
+    float *part = (float *)malloc((size_t)((N + 127) / 128) * sizeof(float));
+    if (!leaf || !part) {
+        free(leaf);
+        free(part);
+        return DGRO_ERR_NOMEM;
+    }
+    int64_t count = rows ? n_rows : T;
+    for (int64_t i = 0; i < count; ++i) {
+        int64_t t = rows ? rows[i] : i;
+        int64_t e = 0;
+        while (offs[e + 1] <= t)
+            ++e;
+        float f = dsrelu_row(A, B, e, K, N, dY, t, leaf, part, m);
+        float *o = rows ? &dprob[i] : &dprob[t];
+        *o = accumulate ? *o + f : f;
+    }
+    free(leaf);
+    free(part);
     return DGRO_OK;
 }
