@@ -64,6 +64,8 @@ def lib() -> ctypes.CDLL:
             "dgr_topk_canonicalize": ([P, I64, P, I64, I64, I32, P, P, P, I64, P], I32),
             "dgr_aux_loss_workspace_bytes": ([I64], SZ),
             "dgr_aux_loss": ([P, I64, I32, I64, P, ctypes.c_float, P, P, SZ, P], I32),
+            "dgr_dsrelu_dprob_workspace_bytes": ([I64, I64], SZ),
+            "dgr_dsrelu_dprob": ([P, P, P, I32, I64, I64, I64, P, P, I32, P, SZ, P], I32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -250,3 +252,26 @@ def aux_loss(probs: torch.Tensor, tokens_per_expert: torch.Tensor, scale: float,
         _ptr(probs), N, E, probs.stride(0), _ptr(tokens_per_expert), float(scale), _ptr(out), _ptr(ws), ws.numel(),
         _stream(stream)))
     return out
+
+
+def dsrelu_dprob_workspace_bytes(T: int, N: int) -> int:
+    return int(lib().dgr_dsrelu_dprob_workspace_bytes(T, N))
+
+
+def dsrelu_dprob(A: torch.Tensor, B: torch.Tensor, offs: torch.Tensor, dY: torch.Tensor, dprob: torch.Tensor, *,
+                 accumulate: bool = False, ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """dprob[m] (+)= fold over N-tiles of pw_128(RN(dY * RN(relu(C)^2))), C = A_e B_e on the tensor
+    cores (never written). A bf16 [T, K], B bf16 [E, K, N], offs int64 device [E+1], dY bf16 [T, N]."""
+    T, K = A.shape
+    E, K2, N = B.shape
+    if (A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16 or dY.dtype != torch.bfloat16 or K2 != K or
+            dY.shape != (T, N) or offs.shape != (E + 1,) or dprob.shape != (T,) or dprob.dtype != torch.float32):
+        raise ValueError("A [T, K], B [E, K, N], dY [T, N] bf16, offs int64 [E+1], dprob fp32 [T] expected")
+    if not (A.is_contiguous() and B.is_contiguous() and dY.is_contiguous()):
+        raise ValueError("A, B and dY must be contiguous")
+    if ws is None:
+        ws = workspace(dsrelu_dprob_workspace_bytes(T, N), A.device)
+    _check("dgr_dsrelu_dprob", lib().dgr_dsrelu_dprob(
+        _ptr(A), _ptr(B), _ptr(offs), E, T, K, N, _ptr(dY), _ptr(dprob), int(accumulate), _ptr(ws), ws.numel(),
+        _stream(stream)))
+    return dprob

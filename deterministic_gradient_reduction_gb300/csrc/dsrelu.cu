@@ -1,0 +1,445 @@
+// dprob fused into its grouped dsReLU GEMM:
+//   C = A_e B_e on the tensor cores (K16 steps ascending from a fresh
+//   accumulator), leaf[m][n] = RN(fp32(dY[m][n]) * RN(relu(C[m][n])^2)),
+//   dprob[m] = fold over N-tiles of 128 of pw_128(leaves), written or added.
+//
+// cuDNN-frontend PR #521 ("grouped gemm dsrelu deterministic dprob"): the
+// backward kernel recomputes the grouped GEMM and reuses relu(C)^2 for dprob;
+// determinism comes from one partial per (token, N-tile) with a single writer
+// and a fixed-order reduction of the partials, accumulated into dprob. The
+// GEMM output itself is never written: only its dprob partials leave the chip.
+//
+// Two launches:
+//   gemm - persistent, one CTA per SM, 12 warps. Tiles are (expert, 128-row
+//          block counted from the expert's first row, 256-column block),
+//          expert by expert. Warp 0 loads 64-deep k stages by TMA (A [T, K]
+//          K-major: one 128 x 64 box; B_e [K, N] N-major: four 64 x 64 boxes;
+//          128-byte swizzle, 4 stages); warp 1 issues tcgen05.mma (M 128,
+//          N 256, K 16, bf16 in, fp32 in TMEM) over all of K into one of two
+//          TMEM accumulators; warps 4-11 (lane quarter q, column half h) read
+//          their row's 128 columns, form the leaves with the row of dY (its
+//          loads issued before the accumulator is ready), sum them by the tile
+//          tree in registers and store one partial per (row, N-tile).
+//   fold - one thread per token (programmatic dependent launch): its N-tile
+//          partials folded in order into dprob.
+// Every wait is bounded; no floating-point value depends on timing.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "tc_common.cuh"
+
+namespace dgr {
+namespace {
+
+using namespace tc;
+
+constexpr int BM = 128;  // rows of a tile (TMEM lanes)
+constexpr int BN = 256;  // columns of a tile (TMEM columns per accumulator)
+constexpr int BK = 64;   // k per stage
+constexpr int kStages = 4;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = (4 + kEpiWarps) * 32;
+constexpr int kMaxExperts = 1024;
+constexpr int kRegsLow = 56;
+constexpr int kRegsHigh = 224;
+static_assert(128 * kRegsLow + 256 * kRegsHigh <= 384 * 168, "register split exceeds the launch's registers");
+constexpr uint32_t kBoxA = BM * 128;            // 128 rows x 64 k (128 bytes a row)
+constexpr uint32_t kBoxB = 64 * 128;            // 64 k rows x 64 n
+constexpr uint32_t kStageA = kBoxA;
+constexpr uint32_t kStageB = 4 * kBoxB;         // 64 k x 256 n
+constexpr uint32_t kStageBytes = kStageA + kStageB;
+constexpr uint32_t kSBO = 1024;                 // between 8-row groups
+constexpr uint32_t kLboA = 16;                  // K-major, 128-byte swizzle: one atom spans the K16 step
+constexpr uint32_t kLboB = kBoxB;               // N-major: between 64-wide atoms along n
+// tcgen05 instruction descriptor: fp32 D, bf16 A and B, A K-major, B N-major
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
+                            (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+constexpr uint32_t kTmemCols = 2 * BN;
+
+struct Ctl {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint32_t tmem_base;
+    int abort;
+};
+constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + sizeof(Ctl);
+
+struct DsParams {
+    const int64_t *offs;
+    int32_t E, T, K, N;
+    int32_t nbs;          // 256-column blocks
+    const uint16_t *dY;   // [T, N]
+    float *slots;         // [T, N / 128]
+    float *dprob;         // [T]
+    int32_t accumulate;
+    WsHeader *hdr;
+};
+
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// mb_base[e] = first m-block of expert e (mb_base[E] = all m-blocks), by the
+// whole block; false when the offsets break the contract.
+__device__ bool mblock_bases(const DsParams &p, int32_t *mb_base, int32_t *wsum, int32_t *bad) {
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, nt = blockDim.x, nw = nt >> 5;
+    if (tid == 0) *bad = 0;
+    __syncthreads();
+    int32_t run = 0;
+    for (int e0 = 0; e0 < p.E; e0 += nt) {
+        const int e = e0 + tid;
+        int32_t c = 0;
+        if (e < p.E) {
+            const int64_t a = p.offs[e], b = p.offs[e + 1];
+            if (b < a || (e == 0 && a != 0) || (e == p.E - 1 && b != p.T)) *bad = 1;
+            else c = static_cast<int32_t>((b - a + BM - 1) / BM);
+        }
+        int32_t incl = c;
+#pragma unroll
+        for (int s = 1; s < 32; s <<= 1) {
+            const int32_t o = __shfl_up_sync(0xffffffffu, incl, s);
+            if (lane >= s) incl += o;
+        }
+        if (lane == 31) wsum[w] = incl;
+        __syncthreads();
+        int32_t before = run;
+        for (int v = 0; v < w; ++v) before += wsum[v];
+        if (e < p.E) mb_base[e] = before + incl - c;
+        for (int v = 0; v < nw; ++v) run += wsum[v];
+        __syncthreads();
+    }
+    if (tid == 0) mb_base[p.E] = run;
+    __syncthreads();
+    return *bad == 0;
+}
+
+// tile tau -> expert, m-block within the expert, n-block
+__device__ __forceinline__ void tile_of(const DsParams &p, const int32_t *mb_base, int64_t tau, int &e, int &mb,
+                                        int &nb) {
+    const int32_t gmb = static_cast<int32_t>(tau / p.nbs);
+    nb = static_cast<int>(tau - static_cast<int64_t>(gmb) * p.nbs);
+    int lo = 0, hi = p.E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (mb_base[mid] <= gmb) lo = mid;
+        else hi = mid - 1;
+    }
+    e = lo;
+    mb = gmb - mb_base[lo];
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    dsrelu_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const DsParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Ctl *ctl = reinterpret_cast<Ctl *>(smem + kStages * kStageBytes);
+    __shared__ int32_t mb_base[kMaxExperts + 1];
+    __shared__ int32_t wsum[kThreads / 32];
+    __shared__ int32_t bad;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    volatile int *abort_flag = &ctl->abort;
+    launch_dependents();  // the fold may start its blocks; it waits for this grid
+
+    if (!mblock_bases(p, mb_base, wsum, &bad)) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) record_error(p.hdr, DGR_ERR_INVALID_ARG, 30);
+        return;
+    }
+    const int64_t n_tiles = static_cast<int64_t>(mb_base[p.E]) * p.nbs;
+    const int n_k = p.K / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&ctl->full[s], 1);
+            mbar_init(&ctl->empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&ctl->tfull[b], 1);
+            mbar_init(&ctl->tempty[b], kEpiWarps);
+        }
+        ctl->abort = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(&ctl->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem_base;
+
+    if (warp < 4) setmaxnreg_dec<kRegsLow>();
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            bool armed[kStages] = {};
+            uint32_t armed_phase[kStages] = {};
+            bool ok = true;
+            for (int64_t tau = blockIdx.x; ok && tau < n_tiles; tau += gridDim.x) {
+                int e, mb, nb;
+                tile_of(p, mb_base, tau, e, mb, nb);
+                const int32_t row0 = static_cast<int32_t>(p.offs[e]) + mb * BM;
+                for (int kb = 0; kb < n_k; ++kb) {
+                    if (!mbar_wait(&ctl->empty[stage], phase ^ 1, abort_flag, p.hdr, 31)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *sA = smem + stage * kStageBytes;
+                    uint8_t *sB = sA + kStageA;
+                    mbar_arrive_expect_tx(&ctl->full[stage], kStageBytes);
+                    armed[stage] = true;
+                    armed_phase[stage] = phase;
+                    tma_load_2d(sA, &tmA, &ctl->full[stage], kb * BK, row0);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        tma_load_2d(sB + q * kBoxB, &tmB, &ctl->full[stage], nb * BN + 64 * q, e * p.K + kb * BK);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) {  // aborted: let our copies in flight land before the CTA exits
+                int dummy = 0;
+                for (int s = 0; s < kStages; ++s)
+                    if (armed[s]) mbar_wait(&ctl->full[s], armed_phase[s], &dummy, nullptr, 0);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        uint32_t stage = 0, phase = 0, g = 0;
+        bool ok = true;
+        for (int64_t tau = blockIdx.x; ok && tau < n_tiles; tau += gridDim.x, ++g) {
+            const uint32_t buf = g & 1, tph = (g >> 1) & 1;
+            if (!mbar_wait(&ctl->tempty[buf], tph ^ 1, abort_flag, p.hdr, 32)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem + buf * BN;
+            for (int kb = 0; kb < n_k; ++kb) {
+                if (!mbar_wait(&ctl->full[stage], phase, abort_flag, p.hdr, 33)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t a0 = smem_u32(smem + stage * kStageBytes), b0 = a0 + kStageA;
+                    // the stage's four K16 steps back to back, descriptors ready
+                    uint64_t ad[4], bd[4];
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        ad[kk] = smem_desc_sw128(a0 + kk * 32, kLboA, kSBO);
+                        bd[kk] = smem_desc_sw128(b0 + kk * 2048, kLboB, kSBO);
+                    }
+                    mma_bf16(d_tmem, ad[0], bd[0], kIdesc, kb > 0 ? 1u : 0u);
+                    mma_bf16(d_tmem, ad[1], bd[1], kIdesc, 1u);
+                    mma_bf16(d_tmem, ad[2], bd[2], kIdesc, 1u);
+                    mma_bf16(d_tmem, ad[3], bd[3], kIdesc, 1u);
+                    mma_commit(&ctl->empty[stage]);
+                }
+                __syncwarp();
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+            if (!ok) break;
+            if (lane == 0) mma_commit(&ctl->tfull[buf]);
+            __syncwarp();
+        }
+    } else if (warp >= 4) {
+        // ---------------- epilogue: leaves, tile trees, partials ----------------
+        setmaxnreg_inc<kRegsHigh>();
+        const int q = warp & 3;           // TMEM lane quarter this warp may access
+        const int h = (warp - 4) >> 2;    // N-tile (128 columns) within the 256-column block
+        const int n_ntiles = p.N / 128;
+        uint32_t g = 0;
+        bool ok = true;
+        for (int64_t tau = blockIdx.x; ok && tau < n_tiles; tau += gridDim.x, ++g) {
+            int e, mb, nb;
+            tile_of(p, mb_base, tau, e, mb, nb);
+            const int64_t row = p.offs[e] + static_cast<int64_t>(mb) * BM + 32 * q + lane;
+            const bool mine = row < p.offs[e + 1];  // past the expert's end: not this expert's row
+            // the row's 128 dY values, in flight while the accumulator fills
+            const int col0 = nb * BN + 128 * h;
+            uint4 dy[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                dy[i] = make_uint4(0u, 0u, 0u, 0u);
+                ldg_nc_v4u_if(dy[i], p.dY + row * p.N + col0 + 8 * i, mine);
+            }
+            const uint32_t buf = g & 1, tph = (g >> 1) & 1;
+            if (!mbar_wait(&ctl->tfull[buf], tph, abort_flag, p.hdr, 34)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t base = tmem + (static_cast<uint32_t>(32 * q) << 16) + buf * BN + 128 * h;
+            float part[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t r[32];
+                tmem_ld32(base + 32 * j, r);
+                tmem_wait_ld();
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float c = __uint_as_float(r[i]);
+                    const float rl = c > 0.0f ? c : 0.0f;
+                    const uint32_t w = (i & 1) ? (reinterpret_cast<const uint32_t *>(&dy[4 * j + i / 8])[(i % 8) / 2] &
+                                                  0xffff0000u)
+                                               : (reinterpret_cast<const uint32_t *>(&dy[4 * j + i / 8])[(i % 8) / 2]
+                                                  << 16);
+                    v[i] = __fmul_rn(__uint_as_float(w), __fmul_rn(rl, rl));
+                }
+                // levels 1-5 of the N-tile's tree over these 32 columns
+#pragma unroll
+                for (int s = 1; s < 32; s *= 2)
+#pragma unroll
+                    for (int i = 0; i + s < 32; i += 2 * s) v[i] = __fadd_rn(v[i], v[i + s]);
+                part[j] = v[0];
+            }
+            // the accumulator is read: the MMA may refill it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->tempty[buf]);
+            // levels 6-7, then the partial of (row, N-tile 2 nb + h)
+            const float tile = __fadd_rn(__fadd_rn(part[0], part[1]), __fadd_rn(part[2], part[3]));
+            if (mine) p.slots[row * n_ntiles + 2 * nb + h] = tile;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+__global__ void __launch_bounds__(256) dsrelu_fold(const DsParams p) {
+    grid_dep_wait();  // the GEMM grid has completed; its partials are visible
+    if (p.hdr->status != 0) return;  // the GEMM gave up (offsets or a bounded wait): dprob untouched
+    const int64_t m = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
+    if (m >= p.T) return;
+    const int n = p.N / 128;
+    const float *s = p.slots + m * n;
+    float F = __ldcg(s);
+    for (int j = 1; j < n; ++j) F = __fadd_rn(F, __ldcg(s + j));
+    p.dprob[m] = p.accumulate ? __fadd_rn(p.dprob[m], F) : F;
+}
+
+// ---- host ---------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+dgr_status encode_fn(PFN_cuTensorMapEncodeTiled_v12000 *fn) {
+    std::call_once(g_encode_once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    if (!g_encode) return DGR_ERR_CUDA;
+    *fn = g_encode;
+    return DGR_OK;
+}
+
+// 2-D map over a row-major bf16 [rows, cols] matrix, box {64 columns, box_rows},
+// 128-byte swizzle, zero fill past the end.
+dgr_status make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, uint32_t box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    dgr_status st = encode_fn(&enc);
+    if (st != DGR_OK) return st;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? DGR_OK : DGR_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace dgr
+
+using namespace dgr;
+
+extern "C" size_t dgr_dsrelu_dprob_workspace_bytes(int64_t T, int64_t N) {
+    if (T < 0 || N < 0 || T > INT32_MAX || N > (1 << 20)) return 0;
+    return sizeof(WsHeader) + align_up(static_cast<size_t>(T) * static_cast<size_t>((N + 127) / 128) * 4);
+}
+
+extern "C" dgr_status dgr_dsrelu_dprob(const void *A, const void *B, const int64_t *d_offs, int32_t E, int64_t T,
+                                       int64_t K, int64_t N, const void *dY, float *dprob, int32_t accumulate,
+                                       void *ws, size_t ws_bytes, void *stream) {
+    if (E < 1 || T < 0 || K < 1 || N < 1) return DGR_ERR_INVALID_ARG;
+    if (E > kMaxExperts || T > INT32_MAX || (K % BK) != 0 || (N % BN) != 0 || N > (1 << 20) ||
+        static_cast<int64_t>(E) * K > INT32_MAX)
+        return DGR_ERR_UNSUPPORTED;
+    if (!d_offs || !dprob || (T > 0 && (!A || !B || !dY))) return DGR_ERR_INVALID_ARG;
+    if (!aligned(d_offs, 8) || !aligned(dprob, 4) || (A && !aligned(A, 16)) || (B && !aligned(B, 16)) ||
+        (dY && !aligned(dY, 16)))
+        return DGR_ERR_MISALIGNED;
+    const size_t need = dgr_dsrelu_dprob_workspace_bytes(T, N);
+    if (ranges_overlap(dprob, T * 4, A, T * K * 2) || ranges_overlap(dprob, T * 4, B, E * K * N * 2) ||
+        ranges_overlap(dprob, T * 4, dY, T * N * 2) || ranges_overlap(dprob, T * 4, d_offs, (E + 1) * 8))
+        return DGR_ERR_ALIAS;
+    if (T > 0) {
+        if (!ws) return DGR_ERR_INVALID_ARG;
+        if (ws_bytes < need) return DGR_ERR_WORKSPACE_TOO_SMALL;
+        if (!aligned(ws, kAlign)) return DGR_ERR_MISALIGNED;
+        if (ranges_overlap(dprob, T * 4, ws, need)) return DGR_ERR_ALIAS;
+    }
+    dgr_status st = check_device();
+    if (st != DGR_OK) return st;
+    if (T == 0) return DGR_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    CUtensorMap mA, mB;
+    if ((st = make_map(&mA, A, T, K, BM)) != DGR_OK) return st;
+    if ((st = make_map(&mB, B, static_cast<int64_t>(E) * K, N, 64)) != DGR_OK) return st;
+    DsParams p{};
+    p.offs = d_offs;
+    p.E = E;
+    p.T = static_cast<int32_t>(T);
+    p.K = static_cast<int32_t>(K);
+    p.N = static_cast<int32_t>(N);
+    p.nbs = static_cast<int32_t>(N / BN);
+    p.dY = static_cast<const uint16_t *>(dY);
+    p.dprob = dprob;
+    p.accumulate = accumulate ? 1 : 0;
+    p.hdr = static_cast<WsHeader *>(ws);
+    p.slots = reinterpret_cast<float *>(static_cast<char *>(ws) + sizeof(WsHeader));
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaFuncSetAttribute(dsrelu_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes)) !=
+            cudaSuccess)
+        return DGR_ERR_CUDA;
+    const int64_t tiles_max = ((T + BM - 1) / BM + E) * (N / BN);
+    const int grid = static_cast<int>(tiles_max < sms ? tiles_max : sms);
+    dsrelu_gemm<<<grid, kThreads, kSmemBytes, s>>>(mA, mB, p);
+    if (cudaGetLastError() != cudaSuccess) return DGR_ERR_CUDA;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>((T + 255) / 256));
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, dsrelu_fold, p) == cudaSuccess ? DGR_OK : DGR_ERR_CUDA;
+}

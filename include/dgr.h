@@ -305,6 +305,37 @@ size_t dgr_aux_loss_workspace_bytes(int64_t N);
 dgr_status dgr_aux_loss(const float *probs, int64_t N, int32_t E, int64_t ld, const int32_t *d_tokens_per_expert,
                         float scale, float *d_out, void *ws, size_t ws_bytes, void *stream);
 
+/* ------------------------------------------------------------------------ */
+/* 8. dprob fused into its grouped dsReLU GEMM                               */
+/* ------------------------------------------------------------------------ */
+/*
+ * cuDNN-frontend PR #521 ("grouped gemm dsrelu deterministic dprob"): the
+ * backward kernel recomputes the grouped GEMM, reuses relu(C)^2 for dprob,
+ * and makes dprob deterministic with one partial per (token, N-tile), a single
+ * writer each, reduced in a fixed order and accumulated into dprob. For the
+ * tokens of expert e (rows d_offs[e] .. d_offs[e+1]-1):
+ *
+ *   C[m][n] = sum_k A[m][k] B[e][k][n] on the tensor cores (K16 steps over k
+ *             ascending, from a fresh accumulator; fp32);
+ *   leaf    = RN(fp32(dY[m][n]) * RN(r * r)), r = max(C[m][n], 0);
+ *   dprob[m] = fold over N-tiles of 128 of pw_128(leaves), written
+ *             (accumulate = 0) or added with one rounding.
+ *
+ * C is never written. A: [T, K] bf16 row-major; B: [E, K, N] bf16 row-major;
+ * dY: [T, N] bf16 row-major; dprob: [T] fp32; d_offs: [E+1] int64 DEVICE,
+ * non-decreasing, d_offs[0] = 0, d_offs[E] = T (checked on the device: the call
+ * then writes nothing and records DGR_ERR_INVALID_ARG in the status word).
+ * Limits:   K a multiple of 64, N a multiple of 256, 1 <= E <= 1024, T < 2^31.
+ * Alignment: A, B, dY 16-byte aligned.
+ * ws:       dgr_dsrelu_dprob_workspace_bytes(T, N) bytes, zeroed once (status
+ *           word, one FP32 partial per token and N-tile).
+ * dprob must not overlap A, B, dY, d_offs or ws.
+ */
+size_t dgr_dsrelu_dprob_workspace_bytes(int64_t T, int64_t N);
+dgr_status dgr_dsrelu_dprob(const void *A, const void *B, const int64_t *d_offs, int32_t E, int64_t T, int64_t K,
+                            int64_t N, const void *dY, float *dprob, int32_t accumulate, void *ws, size_t ws_bytes,
+                            void *stream);
+
 #ifdef __cplusplus
 }
 #endif

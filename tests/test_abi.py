@@ -146,3 +146,14 @@ def test_aux_loss_host_checks(L):
     assert L.dgr_aux_loss(pr, 1000, 8, 8, tp, F(1.0), o, ws, 16, None) == 3          # workspace too small
     assert L.dgr_aux_loss(pr, 10, 8, 8, tp, F(1.0), _p(0x100004), ws, 1 << 20, None) == 4  # out inside probs
     assert dgr.aux_loss_workspace_bytes(65536) == 256 + 512 * 4
+
+
+def test_dsrelu_host_checks(L):
+    a, b, o, y, d, ws = (_p(x) for x in (0x1000000, 0x2000000, 0x3000000, 0x4000000, 0x5000000, 0x6000000))
+    assert L.dgr_dsrelu_dprob(a, b, o, 0, 100, 64, 256, y, d, 0, ws, 1 << 30, None) == 1    # E = 0
+    assert L.dgr_dsrelu_dprob(a, b, o, 2, 100, 60, 256, y, d, 0, ws, 1 << 30, None) == 2    # K not a multiple of 64
+    assert L.dgr_dsrelu_dprob(a, b, o, 2, 100, 64, 300, y, d, 0, ws, 1 << 30, None) == 2    # N not a multiple of 256
+    assert L.dgr_dsrelu_dprob(_p(0x1000008), b, o, 2, 100, 64, 256, y, d, 0, ws, 1 << 30, None) == 5  # A misaligned
+    assert L.dgr_dsrelu_dprob(a, b, o, 2, 100, 64, 256, y, d, 0, ws, 64, None) == 3          # workspace too small
+    assert L.dgr_dsrelu_dprob(a, b, o, 2, 100, 64, 256, y, _p(0x4000100), 0, ws, 1 << 30, None) == 4  # dprob in dY
+    assert dgr.dsrelu_dprob_workspace_bytes(16384, 4096) == 256 + 16384 * 32 * 4
