@@ -56,15 +56,17 @@ ALGO = {
     "dbias": 65536 * 2048 * 2 + 8 * 2048 * 4,
     "topk": 65536 * 128 * 4 * 5,
     "aux_loss": 65536 * 128 * 4 + 128 * 4 + 4,
+    "dsrelu_flop": 2 * 16384 * 2048 * 4096,
 }
 LAUNCHES = {"colsum_large": 1, "colsum_small": 1, "dprob": 1, "colsum_strided": 1, "index_add": 4, "wgrad": 1,
-            "dbias": 2, "topk": 1, "aux_loss": 1}
+            "dbias": 2, "topk": 1, "aux_loss": 1, "dsrelu": 2}
 # operations beyond the step (the next rows of the scope), timed on their own after it
-EXTRAS = ["dbias", "topk", "aux_loss"]
+EXTRAS = ["dbias", "topk", "aux_loss", "dsrelu"]
 EXTRA_WORKLOADS = {
     "dbias": "grouped dbias bf16 65536x2048, 8 experts (multinomial rows) -> fp32 [8, 2048]",
     "topk": "canonical compact top-K, 65536 rows x 128 slots (int32 ids, fp32 logits; 10 % padding)",
     "aux_loss": "router aux-loss scalar, fp32 probs 65536 x 128 with top-8 expert counts",
+    "dsrelu": "dprob fused into the grouped dsReLU GEMM, bf16 A 16384x2048, B 8x2048x4096, dY 16384x4096",
 }
 
 WORKLOAD = ("deterministic reduction step: colsum bf16 8388608x64 + colsum bf16 2048x16 + dprob bf16 "
@@ -229,6 +231,15 @@ def make_ops(dev, torch, dgr, with_wgrad, only=None, small=False):
                            dgr.aux_loss(aprobs, atpe, sc, aout, ws=aws))
         host["aux_loss"] = ([ax.probs, ax.tpe], [aprobs, atpe])
         outs["aux_loss"] = aout
+    if want("dsrelu"):
+        dsr = gi.dsrelu_full() if not small else gi.dsrelu_input(8, 4096, 2048, 4096, seed=9)
+        sA, sB, soffs, sdY = dsr.A.to(dev), dsr.B.to(dev), dsr.offs.to(dev), dsr.dY.to(dev)
+        sdp = dsr.dprob.to(dev)
+        sws = dgr.workspace(dgr.dsrelu_dprob_workspace_bytes(*dsr.dY.shape), dev)
+        ops["dsrelu"] = (lambda sA=sA, sB=sB, soffs=soffs, sdY=sdY, sdp=sdp, sws=sws:
+                         dgr.dsrelu_dprob(sA, sB, soffs, sdY, sdp, ws=sws))
+        host["dsrelu"] = ([dsr.A, dsr.B, dsr.offs, dsr.dY], [sA, sB, soffs, sdY])
+        outs["dsrelu"] = sdp
     steps = ["colsum_large", "colsum_small", "dprob", "colsum_strided", "index_add", "wgrad"]
     order = [n for n in steps + (EXTRAS if only in EXTRAS else []) if n in ops]
     return order, ops, host, outs
@@ -380,6 +391,12 @@ def run_ours(args, rank, world, local_rank):
                         "launches": LAUNCHES[n], "dram_traffic": traffic.get(n)}
     next_rows = {}
     for n, ms in extra_ms.items():
+        if n == "dsrelu":
+            tf = ALGO["dsrelu_flop"] / (ms * 1e-3) / 1e12
+            next_rows[n] = {"us": round(ms * 1e3, 2), "tflops": round(tf, 1),
+                            "frac_bf16_sustained": round(tf / peaks["bf16_sus"], 4), "launches": LAUNCHES[n],
+                            "workload": EXTRA_WORKLOADS[n], "timed_as": extra_how[n]}
+            continue
         gbs = ALGO[n] / (ms * 1e-3) / 1e9
         next_rows[n] = {"us": round(ms * 1e3, 2), "gbs": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm"], 4),
                         "launches": LAUNCHES[n], "dram_traffic": traffic.get(n), "workload": EXTRA_WORKLOADS[n],
@@ -532,7 +549,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["colsum_large", "colsum_small", "dprob", "colsum_strided", "index_add",
-                                       "wgrad", "dbias", "topk", "aux_loss"],
+                                       "wgrad", "dbias", "topk", "aux_loss", "dsrelu"],
                     help="profiling: run one operation only (no JSON bench line)")
     ap.add_argument("--small", action="store_true",
                     help="profiling: colsum 2097152x64, dprob 16384x4096, wgrad T=8192 (same widths)")
