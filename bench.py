@@ -245,6 +245,19 @@ def make_ops(dev, torch, dgr, with_wgrad, only=None, small=False):
     return order, ops, host, outs
 
 
+def max_over_ranks(vals: list, device=None) -> list:
+    """Element-wise maximum of `vals` over the ranks of the process group (the
+    slowest rank's time); the values themselves with one process."""
+    import torch
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return list(vals)
+    if torch.distributed.get_world_size() == 1:
+        return list(vals)
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
 def wgrad_available(dgr) -> bool:
     try:
         import torch
@@ -320,10 +333,9 @@ def run_ours(args, rank, world, local_rank):
 
     # max over ranks
     if world > 1:
-        t = torch.tensor([total_ms] + [per_ms[n] for n in order], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t[0])
-        per_ms = {n: float(t[i + 1]) for i, n in enumerate(order)}
+        m = max_over_ranks([total_ms] + [per_ms[n] for n in order], dev)
+        total_ms = m[0]
+        per_ms = {n: m[i + 1] for i, n in enumerate(order)}
 
     # end to end through host buffers: pinned host inputs copied in, outputs read back, every step
     # the next rows of the scope, each timed on its own after the step (not in
@@ -365,9 +377,7 @@ def run_ours(args, rank, world, local_rank):
         extra_ms[n] = sum(a.elapsed_time(b) for a, b in evx) / calls
         extra_how[n] = f"CUDA graph of {reps} calls, {n_rep} replays" if graph is not None else "plain launches"
         if world > 1:
-            t = torch.tensor([extra_ms[n]], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            extra_ms[n] = float(t[0])
+            extra_ms[n] = max_over_ranks([extra_ms[n]], dev)[0]
 
     e2e = run_e2e(args, torch, order, ops, host, outs, stream, world, dev)
 
@@ -449,9 +459,8 @@ def run_e2e(args, torch, order, ops, host, outs, stream, world, dev):
     torch.cuda.synchronize()
     per = {n: sum(a.elapsed_time(b) for a, b in ev[n]) / K for n in order}
     if world > 1:
-        t = torch.tensor([per[n] for n in order], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        per = {n: float(t[i]) for i, n in enumerate(order)}
+        m = max_over_ranks([per[n] for n in order], dev)
+        per = {n: m[i] for i, n in enumerate(order)}
     red_ms = sum(per[n] for n in REDUCTIONS)
     val = world * sum(ALGO[n] for n in REDUCTIONS) / (red_ms * 1e-3) / 1e9
     out = {"value": round(val, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
