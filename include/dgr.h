@@ -61,7 +61,8 @@ typedef int32_t dgr_status;
 /* Human-readable name of a status code (static storage). */
 const char *dgr_status_string(dgr_status s);
 
-/* Library ABI version (major * 100 + minor). */
+/* Library ABI version (major * 100 + minor). 1.01 added sections 5-8 (grouped
+ * dbias, canonical top-K, aux-loss scalar, dsReLU dprob); 1.00 entries unchanged. */
 int32_t dgr_version(void);
 
 /* DGR_OK when `device` is a compute capability 10.3 GPU, else DGR_ERR_UNSUPPORTED. */

@@ -55,7 +55,7 @@ def test_library_is_built_for_sm_103a_only():
 
 
 def test_status_strings_and_version(L):
-    assert L.dgr_version() >= 100
+    assert L.dgr_version() >= 101
     for code, name in dgr.STATUS.items():
         assert L.dgr_status_string(code).decode() == name
     assert L.dgr_status_string(99).decode() == "DGR_ERR_UNKNOWN"
