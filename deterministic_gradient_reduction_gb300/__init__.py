@@ -66,6 +66,7 @@ def lib() -> ctypes.CDLL:
             "dgr_aux_loss": ([P, I64, I32, I64, P, ctypes.c_float, P, P, SZ, P], I32),
             "dgr_dsrelu_dprob_workspace_bytes": ([I64, I64], SZ),
             "dgr_dsrelu_dprob": ([P, P, P, I32, I64, I64, I64, P, P, I32, P, SZ, P], I32),
+            "dgr_diag_wait_timeout": ([I32, I32, P, SZ, P], I32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)

@@ -38,8 +38,8 @@ __device__ __forceinline__ void record_error(WsHeader *h, int32_t code, int32_t 
     if (atomicCAS(&h->status, 0, code) == 0) atomicExch(&h->where, where);
 }
 
-// Spin until *p >= target (acquire), at most kWaitLimitNs. Returns false on timeout.
-__device__ __forceinline__ bool wait_counter_geq(const int32_t *p, int32_t target) {
+// Spin until *p >= target (acquire), at most limit_ns. Returns false on timeout.
+__device__ __forceinline__ bool wait_counter_geq(const int32_t *p, int32_t target, uint64_t limit_ns = kWaitLimitNs) {
     if (ld_acquire_gpu(p) >= target) return true;
     const uint64_t t0 = globaltimer_ns();
     unsigned ns = 32;
@@ -47,7 +47,7 @@ __device__ __forceinline__ bool wait_counter_geq(const int32_t *p, int32_t targe
         __nanosleep(ns);
         if (ld_acquire_gpu(p) >= target) return true;
         if (ns < 1024) ns <<= 1;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
 

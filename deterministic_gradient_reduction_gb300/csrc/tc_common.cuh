@@ -46,15 +46,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 
 // Bounded wait for the phase with the given parity to complete. Gives up
 // (recording DGR_ERR_TIMEOUT and raising the CTA's abort flag) after
-// kWaitLimitNs, or returns false at once when another warp has aborted.
+// limit_ns, or returns false at once when another warp has aborted.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                          WsHeader *hdr, int where) {
+                                          WsHeader *hdr, int where, uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             if (hdr) record_error(hdr, DGR_ERR_TIMEOUT, where);
             *abort_flag = 1;
             return false;

@@ -37,6 +37,19 @@ extern "C" {
 dgr_status dgr_tc_probe_k16(const uint16_t *A, const uint16_t *B, const float *C, float *D, int32_t n_prob,
                             int32_t accumulate, void *ws, size_t ws_bytes, void *stream);
 
+/*
+ * A bounded wait that runs out, on purpose: one kernel waits, through the
+ * library's own wait helper, for something that nothing will ever complete,
+ * and gives up after limit_us microseconds instead of the path's 2 s. which =
+ * 0: the integer-counter wait of the column-sum folders and index_add fold
+ * blocks (on a workspace word nobody increments); which = 1: the mbarrier wait
+ * of the tensor-core pipelines (on a fresh barrier nobody arrives at). The
+ * kernel records DGR_ERR_TIMEOUT in the workspace status word (where = 90 + which)
+ * and returns; the context stays usable. No GPU fault or hang is involved.
+ * ws: at least 256 bytes, zeroed. limit_us: 1 .. 1,000,000.
+ */
+dgr_status dgr_diag_wait_timeout(int32_t which, int32_t limit_us, void *ws, size_t ws_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

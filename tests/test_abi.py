@@ -29,10 +29,11 @@ def L():
     return dgr.lib()
 
 
-def test_header_declares_the_four_operations():
+def test_header_declares_every_operation():
     names = declared_functions()
     for op in ("dgr_ordered_colsum", "dgr_ordered_rowdot_dprob", "dgr_det_index_add",
-               "dgr_grouped_wgrad_accumulate"):
+               "dgr_grouped_wgrad_accumulate", "dgr_grouped_dbias", "dgr_topk_canonicalize", "dgr_aux_loss",
+               "dgr_dsrelu_dprob", "dgr_ordered_colsum_noalloc", "dgr_tc_probe_k16", "dgr_diag_wait_timeout"):
         assert op in names
 
 
@@ -157,3 +158,11 @@ def test_dsrelu_host_checks(L):
     assert L.dgr_dsrelu_dprob(a, b, o, 2, 100, 64, 256, y, d, 0, ws, 64, None) == 3          # workspace too small
     assert L.dgr_dsrelu_dprob(a, b, o, 2, 100, 64, 256, y, _p(0x4000100), 0, ws, 1 << 30, None) == 4  # dprob in dY
     assert dgr.dsrelu_dprob_workspace_bytes(16384, 4096) == 256 + 16384 * 32 * 4
+
+
+def test_wait_timeout_diag_host_checks(L):
+    ws = _p(0x100000)
+    assert L.dgr_diag_wait_timeout(2, 1000, ws, 256, None) == 1       # unknown wait
+    assert L.dgr_diag_wait_timeout(0, 0, ws, 256, None) == 1          # no time at all
+    assert L.dgr_diag_wait_timeout(0, 1000, ws, 64, None) == 3        # workspace below the header
+    assert L.dgr_diag_wait_timeout(0, 1000, _p(0x100008), 256, None) == 5
