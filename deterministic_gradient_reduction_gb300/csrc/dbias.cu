@@ -12,7 +12,7 @@
 //             block of V 16-byte column vectors) and belongs to one warp:
 //             lane = (row group, vector), 32 / V row groups of consecutive
 //             rows. A lane sums its rows by the tile tree's lower levels in
-//             registers, 8 rows' loads in flight at a time (batches are
+//             registers, 16 rows' loads in flight at a time (batches are
 //             aligned subtrees, combined through a binary-counter stack); the
 //             upper levels are xor-shuffles between row groups; row group 0
 //             stores the item's partials. No barrier, no fence, no atomic.
@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(kProdThreads, 1) dbias_produce(const DbiasPara
     constexpr int RGW = 32 / V;                  // row groups
     constexpr int RPL = W / RGW;                 // rows a lane
     static_assert(RPL >= 1, "a row a lane at least");
-    constexpr int BATCH = RPL < 8 ? RPL : 8;     // rows in flight a lane
+    constexpr int BATCH = RPL < 16 ? RPL : 16;   // rows in flight a lane
     constexpr int NB = RPL / BATCH;              // batches, a power of two <= 16
     constexpr int LV = NB >= 16 ? 4 : NB >= 8 ? 3 : NB >= 4 ? 2 : NB >= 2 ? 1 : 0;
     __shared__ int32_t tbase[kMaxExperts + 1];
