@@ -13,8 +13,8 @@
 //   gemm - persistent, one CTA per SM, 12 warps. Tiles are (expert, 128-row
 //          block counted from the expert's first row, 256-column block),
 //          expert by expert. Warp 0 loads 64-deep k stages by TMA (A [T, K]
-//          K-major: one 128 x 64 box; B_e [K, N] N-major: four 64 x 64 boxes;
-//          128-byte swizzle, 4 stages); warp 1 issues tcgen05.mma (M 128,
+//          K-major: one 128 x 64 atom; B_e [K, N] N-major: four 64 x 64
+//          atoms in one copy; 128-byte swizzle, 4 stages); warp 1 issues tcgen05.mma (M 128,
 //          N 256, K 16, bf16 in, fp32 in TMEM) over all of K into one of two
 //          TMEM accumulators; warps 4-11 (lane quarter q, column half h) read
 //          their row's 128 columns, form the leaves with the row of dY (its
@@ -37,7 +37,7 @@ using namespace tc;
 
 constexpr int BM = 128;  // rows of a tile (TMEM lanes)
 constexpr int BN = 256;  // columns of a tile (TMEM columns per accumulator)
-constexpr int BK = 64;   // k per stage
+constexpr int BK = 64;   // k per stage (one 64-column block of A)
 constexpr int kStages = 4;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = (4 + kEpiWarps) * 32;
@@ -46,7 +46,8 @@ constexpr int kRegsLow = 56;
 constexpr int kRegsHigh = 224;
 static_assert(128 * kRegsLow + 256 * kRegsHigh <= 384 * 168, "register split exceeds the launch's registers");
 constexpr uint32_t kBoxA = BM * 128;            // 128 rows x 64 k (128 bytes a row)
-constexpr uint32_t kBoxB = 64 * 128;            // 64 k rows x 64 n
+constexpr uint32_t kBoxB = 64 * 128;            // one atom of B: 64 k rows x 64 n
+static_assert(BK == 64, "a stage of A is one 64-column block of the map");
 constexpr uint32_t kStageA = kBoxA;
 constexpr uint32_t kStageB = 4 * kBoxB;         // 64 k x 256 n
 constexpr uint32_t kStageBytes = kStageA + kStageB;
@@ -197,10 +198,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(&ctl->full[stage], kStageBytes);
                     armed[stage] = true;
                     armed_phase[stage] = phase;
-                    tma_load_2d(sA, &tmA, &ctl->full[stage], kb * BK, row0);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        tma_load_2d(sB + q * kBoxB, &tmB, &ctl->full[stage], nb * BN + 64 * q, e * p.K + kb * BK);
+                    // A: one 64-column block of 128 rows; B: 4 blocks of 64 rows
+                    tma_load_3d(sA, &tmA, &ctl->full[stage], 0, row0, kb);
+                    tma_load_3d(sB, &tmB, &ctl->full[stage], 0, e * p.K + kb * BK, nb * (BN / 64));
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1;
@@ -356,17 +356,20 @@ dgr_status encode_fn(PFN_cuTensorMapEncodeTiled_v12000 *fn) {
     return DGR_OK;
 }
 
-// 2-D map over a row-major bf16 [rows, cols] matrix, box {64 columns, box_rows},
-// 128-byte swizzle, zero fill past the end.
-dgr_status make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, uint32_t box_rows) {
+// Map over a row-major bf16 [rows, cols] matrix (cols a multiple of 64) viewed
+// as {64 columns, rows, cols / 64 blocks}: a box {64, box_rows, blocks} lands as
+// `blocks` consecutive {64, box_rows} atoms, 128-byte swizzle, zero fill past
+// the last row.
+dgr_status make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, uint32_t box_rows,
+                    uint32_t blocks) {
     PFN_cuTensorMapEncodeTiled_v12000 enc;
     dgr_status st = encode_fn(&enc);
     if (st != DGR_OK) return st;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
-    const cuuint32_t box[2] = {64, box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+    const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(cols / 64)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols * 2), 128};
+    const cuuint32_t box[3] = {64, box_rows, blocks};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? DGR_OK : DGR_ERR_CUDA;
@@ -408,8 +411,8 @@ extern "C" dgr_status dgr_dsrelu_dprob(const void *A, const void *B, const int64
     if (T == 0) return DGR_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     CUtensorMap mA, mB;
-    if ((st = make_map(&mA, A, T, K, BM)) != DGR_OK) return st;
-    if ((st = make_map(&mB, B, static_cast<int64_t>(E) * K, N, 64)) != DGR_OK) return st;
+    if ((st = make_map(&mA, A, T, K, BM, 1)) != DGR_OK) return st;
+    if ((st = make_map(&mB, B, static_cast<int64_t>(E) * K, N, 64, BN / 64)) != DGR_OK) return st;
     DsParams p{};
     p.offs = d_offs;
     p.E = E;

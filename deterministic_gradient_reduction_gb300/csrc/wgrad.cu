@@ -47,7 +47,7 @@ constexpr int kThreadsW = (4 + kEpiWarps) * 32;  // warpgroup 0: TMA, MMA, 2 idl
 constexpr int kRegsLow = 56;
 constexpr int kRegsHigh = 224;
 static_assert(128 * kRegsLow + 256 * kRegsHigh <= 384 * 168, "register split exceeds the launch's registers");
-constexpr uint32_t kBoxBytes = 64 * 128;                  // one 64 x 64 bf16 TMA box
+constexpr uint32_t kBoxBytes = 64 * 128;                  // one 64 x 64 bf16 atom (128-byte swizzle)
 constexpr uint32_t kStageA = 2 * kBoxBytes;               // 128 n x 64 tokens
 constexpr uint32_t kStageB = 4 * kBoxBytes;               // 256 k x 64 tokens
 constexpr uint32_t kStageBytes = kStageA + kStageB;
@@ -159,11 +159,9 @@ __global__ void __launch_bounds__(kThreadsW, 1)
                         mbar_arrive_expect_tx(&ctl->full[stage], kStageBytes);
                         armed[stage] = true;
                         armed_phase[stage] = phase;
-                        tma_load_2d(sA, &tmG, &ctl->full[stage], nb * BM, t);
-                        tma_load_2d(sA + kBoxBytes, &tmG, &ctl->full[stage], nb * BM + 64, t);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            tma_load_2d(sB + q * kBoxBytes, &tmX, &ctl->full[stage], kb * BN + 64 * q, t);
+                        // G: 2 column blocks of 64, X: 4, one copy each
+                        tma_load_3d(sA, &tmG, &ctl->full[stage], 0, t, nb * (BM / 64));
+                        tma_load_3d(sB, &tmX, &ctl->full[stage], 0, t, kb * (BN / 64));
                         if (++stage == kStages) {
                             stage = 0;
                             phase ^= 1;
@@ -432,17 +430,19 @@ dgr_status encode_fn(PFN_cuTensorMapEncodeTiled_v12000 *fn) {
     return DGR_OK;
 }
 
-// 2-D tensor map over a row-major bf16 [rows, cols] matrix, 64 x 64 boxes,
-// 128-byte swizzle, zero fill past the end.
-dgr_status make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols) {
+// Tensor map over a row-major bf16 [rows, cols] matrix (cols a multiple of 64)
+// viewed as {64 columns, rows, cols / 64 blocks}: a box of 64 rows and
+// `blocks` column blocks lands as `blocks` consecutive 64 x 64 atoms (8 KB
+// each), 128-byte swizzle, zero fill past the last row.
+dgr_status make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, uint32_t blocks) {
     PFN_cuTensorMapEncodeTiled_v12000 enc;
     dgr_status st = encode_fn(&enc);
     if (st != DGR_OK) return st;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
-    const cuuint32_t box[2] = {64, 64};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+    const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(cols / 64)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols * 2), 128};
+    const cuuint32_t box[3] = {64, 64, blocks};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? DGR_OK : DGR_ERR_CUDA;
@@ -499,8 +499,8 @@ extern "C" dgr_status dgr_grouped_wgrad_accumulate(const void *G, const void *X,
     st = set_smem_attrs();
     if (st != DGR_OK) return st;
     CUtensorMap mG, mX;
-    if ((st = make_map(&mG, G, T_total, N)) != DGR_OK) return st;
-    if ((st = make_map(&mX, X, T_total, K)) != DGR_OK) return st;
+    if ((st = make_map(&mG, G, T_total, N, BM / 64)) != DGR_OK) return st;
+    if ((st = make_map(&mX, X, T_total, K, BN / 64)) != DGR_OK) return st;
     WgradParams p{};
     p.offs = d_offs;
     p.E = E;
