@@ -452,6 +452,8 @@ def run_ours(args, rank, world, local_rank):
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
+        if "wgrad" in host:
+            line["cpu_baseline"]["wgrad"] = wgrad_oracle_sample(host["wgrad"][0])
     print(json.dumps(line), flush=True)
 
 
@@ -536,6 +538,38 @@ def cpu_baseline(budget_s: float = 15.0) -> dict:
     return {"value": round(nbytes / t / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"single-threaded C oracle on {frac:.3f} of each reduction workload "
                       f"(colsum 1 GiB / dprob 1 GiB / index_add prefixes; small ones whole), {t:.1f} s"}
+
+
+def wgrad_oracle_sample(wgrad_host, budget_s: float = 3.0, seed: int = 5) -> dict:
+    """The wgrad oracle on a seeded sample of output elements of the full
+    workload (each element: every 512-token chunk of its expert through the
+    tensor-core step model, the chunks folded, added to its main_grad value),
+    timed and extrapolated to all E*N*K elements."""
+    import oracle
+    G, X, offs, mg = wgrad_host
+    Gb, Xb = gi.bits(G), gi.bits(X)
+    o = offs.numpy().astype(np.int64)
+    E, N, K = mg.shape
+    mgf = mg.numpy().reshape(-1)
+    rng = np.random.default_rng(seed)
+
+    def run(n):
+        e = rng.integers(0, E, n)
+        nn = rng.integers(0, N, n)
+        kk = rng.integers(0, K, n)
+        old = mgf[(e * N + nn) * K + kk]
+        t = time.perf_counter()
+        oracle.wgrad_elements(Gb, Xb, o, N, K, e, nn, kk, old)
+        return time.perf_counter() - t
+
+    t16 = max(run(16), 1e-6)
+    n = int(min(200000, max(16, budget_s / (t16 / 16))))
+    t = run(n)
+    full_s = t / n * E * N * K
+    return {"tflops_extrapolated": round(2.0 * N * K * int(o[-1]) / full_s / 1e12, 9), "elements_timed": n,
+            "seconds": round(t, 2), "full_seconds_extrapolated": round(full_s, 1),
+            "sample": f"{n} seeded output elements of the full E{E} N{N} K{K} workload, extrapolated to all "
+                      f"{E * N * K} (single thread)"}
 
 
 def run_reference(args, rank, world):

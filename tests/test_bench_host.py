@@ -1,0 +1,30 @@
+"""Host-side pieces of bench.py that need no GPU: the sampled, extrapolated
+timing of the wgrad oracle, and the rotation of the next rows whose inputs fit
+in L2."""
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+import dgr_inputs as gi  # noqa: E402
+
+L2_BYTES = 129e6
+
+
+def test_wgrad_oracle_sample_extrapolates():
+    wi = gi.wgrad_input(2, 300, 128, 256, seed=3)
+    r = bench.wgrad_oracle_sample([wi.G, wi.X, wi.offs, wi.main_grad], budget_s=0.2)
+    assert r["elements_timed"] >= 16
+    assert r["tflops_extrapolated"] > 0
+    assert r["full_seconds_extrapolated"] > 0
+    assert "E2 N128 K256" in r["sample"]
+
+
+def test_rotated_next_rows_stream_more_than_twice_l2_between_uses():
+    # between two uses of one input copy, the other copies' calls stream their
+    # algorithmic bytes: that must exceed twice L2 so no timed call hits in L2
+    for name, copies in bench.ROTATE.items():
+        assert name in bench.EXTRAS
+        assert (copies - 1) * bench.ALGO[name] > 2 * L2_BYTES, name
