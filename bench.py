@@ -140,13 +140,21 @@ class ClockSampler:
             self.t1 = time.time()
 
     def stop(self) -> dict:
+        """End sampling; the clocks of the window between the two marks."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         time.sleep(0.25)
         self.proc.terminate()
         self.proc.wait()
-        inside = [s for t, s in self.samples if self.t0 is None or (self.t0 <= t <= (self.t1 or t) + 0.15)]
-        if not inside:
+        return self.window(self.t0, self.t1, fallback=True)
+
+    def window(self, t0, t1, fallback: bool = False) -> dict:
+        """Median SM clock, maximum clock and throttle reasons of the samples taken in [t0, t1]
+        (with `fallback`, of all samples when none falls inside)."""
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        inside = [s for t, s in self.samples if t0 is None or (t0 <= t <= (t1 or t) + 0.15)]
+        if not inside and fallback:
             inside = [s for _, s in self.samples]
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -342,7 +350,6 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     sampler.mark(False)
     barrier()
-    clocks = sampler.stop()
     total_ms = step0.elapsed_time(step1)
     per_ms = {n: sum(a.elapsed_time(b) for a, b in ev[n]) / K for n in order}
 
@@ -359,7 +366,7 @@ def run_ours(args, rank, world, local_rank):
     # call is not hidden behind the host's per-call work (the library holds no
     # host state and synchronises nothing, so its calls capture as they run);
     # plain launches if capture is refused.
-    extra_ms, extra_how = {}, {}
+    extra_ms, extra_how, extra_win = {}, {}, {}
     for n in [x for x in EXTRAS if x in ops]:
         for _ in range(args.warmup):
             ops[n]()
@@ -378,9 +385,17 @@ def run_ours(args, rank, world, local_rank):
             graph = None
             torch.cuda.synchronize()
         n_rep = max(1, K // reps) if graph is not None else K
+        if graph is not None:  # run each next row for at least ~0.4 s so its clocks are sampled
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            n_rep = min(5000, max(n_rep, int(400.0 / max(e0.elapsed_time(e1), 1e-3)) + 1))
         evx = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_rep)]
         barrier()
         torch.cuda.synchronize()
+        tx0 = time.time()
         for a, b in evx:
             a.record(stream)
             if graph is not None:
@@ -389,11 +404,15 @@ def run_ours(args, rank, world, local_rank):
                 ops[n]()
             b.record(stream)
         torch.cuda.synchronize()
+        extra_win[n] = (tx0, time.time())
         calls = n_rep * (reps if graph is not None else 1)
         extra_ms[n] = sum(a.elapsed_time(b) for a, b in evx) / calls
         extra_how[n] = f"CUDA graph of {reps} calls, {n_rep} replays" if graph is not None else "plain launches"
         if world > 1:
             extra_ms[n] = max_over_ranks([extra_ms[n]], dev)[0]
+
+    clocks = sampler.stop()  # the step's window
+    extra_clocks = {n: sampler.window(*w) for n, w in extra_win.items()}
 
     e2e = run_e2e(args, torch, order, ops, host, outs, stream, world, dev)
 
@@ -421,12 +440,12 @@ def run_ours(args, rank, world, local_rank):
             tf = ALGO["dsrelu_flop"] / (ms * 1e-3) / 1e12
             next_rows[n] = {"us": round(ms * 1e3, 2), "tflops": round(tf, 1),
                             "frac_bf16_sustained": round(tf / peaks["bf16_sus"], 4), "launches": LAUNCHES[n],
-                            "workload": EXTRA_WORKLOADS[n], "timed_as": extra_how[n]}
+                            "workload": EXTRA_WORKLOADS[n], "timed_as": extra_how[n], "clocks": extra_clocks.get(n)}
             continue
         gbs = ALGO[n] / (ms * 1e-3) / 1e9
         next_rows[n] = {"us": round(ms * 1e3, 2), "gbs": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm"], 4),
                         "launches": LAUNCHES[n], "dram_traffic": traffic.get(n), "workload": EXTRA_WORKLOADS[n],
-                        "timed_as": extra_how[n]}
+                        "timed_as": extra_how[n], "clocks": extra_clocks.get(n)}
     dom = max(order, key=lambda n: per_ms[n])
     if dom == "wgrad":
         ach = ALGO["wgrad_flop"] / (per_ms[dom] * 1e-3) / 1e12

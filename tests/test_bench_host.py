@@ -28,3 +28,18 @@ def test_rotated_next_rows_stream_more_than_twice_l2_between_uses():
     for name, copies in bench.ROTATE.items():
         assert name in bench.EXTRAS
         assert (copies - 1) * bench.ALGO[name] > 2 * L2_BYTES, name
+
+
+def test_clock_window_reports_each_window_and_its_reasons():
+    c = bench.ClockSampler(0)
+    c.proc = object()  # samples are injected; no nvidia-smi here
+    t = 1000.0
+    c.samples = [(t, "2070, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, Not Active"),
+                 (t + 1, "1800, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active")]
+    step = c.window(t - 0.1, t + 0.05)
+    assert step["sm_mhz"] == 2070.0 and step["reasons"] == [] and step["samples"] == 1
+    extra = c.window(t + 0.5, t + 1.2)
+    assert extra["sm_mhz"] == 1800.0 and extra["reasons"] == ["sw_power_cap"]
+    empty = c.window(t + 5, t + 6)
+    assert empty["sm_mhz"] is None and empty["samples"] == 0
+    assert c.window(t + 5, t + 6, fallback=True)["samples"] == 2
