@@ -385,13 +385,13 @@ def run_ours(args, rank, world, local_rank):
             graph = None
             torch.cuda.synchronize()
         n_rep = max(1, K // reps) if graph is not None else K
-        if graph is not None:  # run each next row for at least ~0.4 s so its clocks are sampled
+        if graph is not None and args.next_min_s > 0:  # long enough for its clocks to be sampled
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             graph.replay()
             e1.record(stream)
             torch.cuda.synchronize()
-            n_rep = min(5000, max(n_rep, int(400.0 / max(e0.elapsed_time(e1), 1e-3)) + 1))
+            n_rep = min(5000, max(n_rep, int(1000.0 * args.next_min_s / max(e0.elapsed_time(e1), 1e-3)) + 1))
         evx = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_rep)]
         barrier()
         torch.cuda.synchronize()
@@ -627,6 +627,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--next-min-s", type=float, default=0.4,
+                    help="time each next row for at least this long (its clocks are sampled over it); "
+                         "0 for short profiling runs")
     ap.add_argument("--only", choices=["colsum_large", "colsum_small", "dprob", "colsum_strided", "index_add",
                                        "wgrad", "dbias", "topk", "aux_loss", "dsrelu"],
                     help="profiling: run one operation only (no JSON bench line)")
