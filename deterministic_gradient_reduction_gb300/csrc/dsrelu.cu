@@ -20,8 +20,10 @@
 //          their row's 128 columns, form the leaves with the row of dY (its
 //          loads issued before the accumulator is ready), sum them by the tile
 //          tree in registers and store one partial per (row, N-tile).
-//   fold - one thread per token (programmatic dependent launch): its N-tile
-//          partials folded in order into dprob.
+//   fold - one thread per token, in plain stream order after the GEMM: its
+//          N-tile partials folded in order into dprob. (Launched as a
+//          programmatic dependent of the GEMM, with the GEMM releasing it at
+//          its start, the pair took 266 us a call against 215 us this way.)
 // Every wait is bounded; no floating-point value depends on timing.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -80,8 +82,6 @@ struct DsParams {
     WsHeader *hdr;
 };
 
-__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // mb_base[e] = first m-block of expert e (mb_base[E] = all m-blocks), by the
 // whole block; false when the offsets break the contract.
@@ -143,7 +143,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     volatile int *abort_flag = &ctl->abort;
-    launch_dependents();  // the fold may start its blocks; it waits for this grid
 
     if (!mblock_bases(p, mb_base, wsum, &bad)) {
         if (blockIdx.x == 0 && threadIdx.x == 0) record_error(p.hdr, DGR_ERR_INVALID_ARG, 30);
@@ -326,7 +325,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 __global__ void __launch_bounds__(256) dsrelu_fold(const DsParams p) {
-    grid_dep_wait();  // the GEMM grid has completed; its partials are visible
     if (p.hdr->status != 0) return;  // the GEMM gave up (offsets or a bounded wait): dprob untouched
     const int64_t m = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
     if (m >= p.T) return;
@@ -435,14 +433,6 @@ extern "C" dgr_status dgr_dsrelu_dprob(const void *A, const void *B, const int64
     const int grid = static_cast<int>(tiles_max < sms ? tiles_max : sms);
     dsrelu_gemm<<<grid, kThreads, kSmemBytes, s>>>(mA, mB, p);
     if (cudaGetLastError() != cudaSuccess) return DGR_ERR_CUDA;
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(static_cast<unsigned>((T + 255) / 256));
-    cfg.blockDim = dim3(256);
-    cfg.stream = s;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    at[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, dsrelu_fold, p) == cudaSuccess ? DGR_OK : DGR_ERR_CUDA;
+    dsrelu_fold<<<static_cast<unsigned>((T + 255) / 256), 256, 0, s>>>(p);
+    return cudaGetLastError() == cudaSuccess ? DGR_OK : DGR_ERR_CUDA;
 }
