@@ -51,6 +51,7 @@ def lib() -> ctypes.CDLL:
             "dgr_version": ([], I32),
             "dgr_device_supported": ([I32], I32),
             "dgr_read_device_status": ([P, I32, P, P], I32),
+            "dgr_query_device_status": ([P, P], I32),
             "dgr_colsum_workspace_bytes": ([I64, I64, I32], SZ),
             "dgr_ordered_colsum": ([P, I32, I64, I64, I64, I64, I64, P, I32, I32, P, SZ, P], I32),
             "dgr_rowdot_workspace_bytes": ([I64, I64, I32], SZ),
@@ -108,6 +109,12 @@ def read_device_status(ws: torch.Tensor, clear: bool = False, stream=None) -> in
     _check("dgr_read_device_status", lib().dgr_read_device_status(ws.data_ptr(), int(clear),
                                                                   ctypes.byref(st), _stream(stream)))
     return st.value
+
+
+def query_device_status(ws: torch.Tensor, stream=None) -> int:
+    """The status recorded in the workspace (0 when none; a code of STATUS), after synchronising
+    the stream; the word is left as it is."""
+    return int(lib().dgr_query_device_status(ws.data_ptr(), _stream(stream)))
 
 
 def colsum_workspace_bytes(T: int, H: int, tile_rows: int = 128) -> int:

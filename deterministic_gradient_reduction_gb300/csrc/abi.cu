@@ -25,7 +25,7 @@ extern "C" const char *dgr_status_string(dgr_status s) {
     }
 }
 
-extern "C" int32_t dgr_version(void) { return 101; }
+extern "C" int32_t dgr_version(void) { return 102; }
 
 extern "C" dgr_status dgr_device_supported(int32_t device) {
     int major = 0, minor = 0;
@@ -49,4 +49,10 @@ extern "C" dgr_status dgr_read_device_status(const void *ws, int32_t clear, int3
             return DGR_ERR_CUDA;
     }
     return DGR_OK;
+}
+
+extern "C" dgr_status dgr_query_device_status(const void *ws, void *stream) {
+    int32_t v = 0;
+    const dgr_status r = dgr_read_device_status(ws, 0, &v, stream);
+    return r != DGR_OK ? r : static_cast<dgr_status>(v);
 }

@@ -62,7 +62,8 @@ typedef int32_t dgr_status;
 const char *dgr_status_string(dgr_status s);
 
 /* Library ABI version (major * 100 + minor). 1.01 added sections 5-8 (grouped
- * dbias, canonical top-K, aux-loss scalar, dsReLU dprob); 1.00 entries unchanged. */
+ * dbias, canonical top-K, aux-loss scalar, dsReLU dprob); 1.02 added
+ * dgr_query_device_status; earlier entries unchanged. */
 int32_t dgr_version(void);
 
 /* DGR_OK when `device` is a compute capability 10.3 GPU, else DGR_ERR_UNSUPPORTED. */
@@ -74,6 +75,15 @@ dgr_status dgr_device_supported(int32_t device);
  * DGR_OK in *status means no device-side error was recorded.
  */
 dgr_status dgr_read_device_status(const void *ws, int32_t clear, int32_t *status, void *stream);
+
+/*
+ * The same read as a return value: synchronises `stream` and returns the
+ * status recorded in the workspace's status word (DGR_OK when none was, e.g.
+ * DGR_ERR_TIMEOUT after a bounded wait ran out), or the error of the read
+ * itself (DGR_ERR_INVALID_ARG for a null ws, DGR_ERR_CUDA). The word is left
+ * as it is: clear it with dgr_read_device_status(ws, 1, ...).
+ */
+dgr_status dgr_query_device_status(const void *ws, void *stream);
 
 /* ------------------------------------------------------------------------ */
 /* 1. Ordered column sum                                                     */

@@ -56,10 +56,17 @@ def test_library_is_built_for_sm_103a_only():
 
 
 def test_status_strings_and_version(L):
-    assert L.dgr_version() >= 101
+    assert L.dgr_version() >= 102
     for code, name in dgr.STATUS.items():
         assert L.dgr_status_string(code).decode() == name
     assert L.dgr_status_string(99).decode() == "DGR_ERR_UNKNOWN"
+
+
+def test_status_reads_refuse_a_null_workspace(L):
+    # checked before any CUDA call
+    st = ctypes.c_int32(-1)
+    assert L.dgr_read_device_status(None, 0, ctypes.byref(st), None) == 1  # DGR_ERR_INVALID_ARG
+    assert L.dgr_query_device_status(None, None) == 1
 
 
 def test_workspace_sizes(L):

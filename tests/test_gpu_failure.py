@@ -34,9 +34,11 @@ def test_wait_runs_out_and_the_context_stays_usable(which):
     elapsed = time.perf_counter() - t0
     assert 0.015 <= elapsed < 2.0  # it waited about its 20 ms, and no longer than the path's limit
     assert dgr.read_device_status(ws) == 7  # DGR_ERR_TIMEOUT
+    assert dgr.query_device_status(ws) == 7  # the same word as a return value, left as it is
     where = int(ws[4:8].view(torch.int32).item())
     assert where == 90 + which
     assert dgr.read_device_status(ws, clear=True) == 7 and dgr.read_device_status(ws) == 0
+    assert dgr.query_device_status(ws) == 0
     # the context is still usable: a column sum, bit-exact
     ci = gi.colsum_input(1, 3000, 64, seed=5)
     want = np.zeros(64, np.float32)
