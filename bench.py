@@ -549,12 +549,36 @@ class OracleWork:
         return time.perf_counter() - t, nbytes
 
 
+def host_cpu() -> dict:
+    """The host's CPU model (lscpu, else /proc/cpuinfo, else the machine type) and its core count."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() == "Model name":
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:  # noqa: BLE001
+        model = None
+    if not model:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith("model name"):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            model = None
+    import platform
+    return {"cpu_model": model or platform.machine() or "unknown", "host_cores": os.cpu_count()}
+
+
 def cpu_baseline(budget_s: float = 15.0) -> dict:
     w = OracleWork()
     t_small, _ = w.run(1 / 256)
     frac = min(1.0, max(1 / 256, budget_s / max(t_small * 256, 1e-3)))
     t, nbytes = w.run(frac)
-    return {"value": round(nbytes / t / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+    return {"value": round(nbytes / t / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle", **host_cpu(),
             "sample": f"single-threaded C oracle on {frac:.3f} of each reduction workload "
                       f"(colsum 1 GiB / dprob 1 GiB / index_add prefixes; small ones whole), {t:.1f} s"}
 
@@ -612,7 +636,7 @@ def run_reference(args, rank, world):
             "data": "synthetic",
             "config": {"workload": WORKLOAD, "l2": "n/a (CPU)", "parallelism": "single host thread",
                        "wgrad": "not in the oracle rate"},
-            "cpu_baseline": {"value": round(val, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": round(val, 3), "unit": "GB/s", "cores": 1, "kind": "oracle", **host_cpu(),
                              "sample": f"{frac:.5f} of each reduction workload per step"},
             "e2e": {"value": round(val, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)

@@ -43,3 +43,9 @@ def test_clock_window_reports_each_window_and_its_reasons():
     empty = c.window(t + 5, t + 6)
     assert empty["sm_mhz"] is None and empty["samples"] == 0
     assert c.window(t + 5, t + 6, fallback=True)["samples"] == 2
+
+
+def test_host_cpu_names_a_model_and_counts_cores():
+    h = bench.host_cpu()
+    assert isinstance(h["cpu_model"], str) and h["cpu_model"]
+    assert h["host_cores"] >= 1
