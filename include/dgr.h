@@ -12,9 +12,12 @@
  * Conventions for every entry point:
  *   - Pointers are DEVICE pointers unless stated otherwise; the caller owns
  *     every buffer (inputs, outputs, workspace). The library allocates no
- *     memory and keeps no state between calls.
+ *     memory and keeps no state between calls (the one exception,
+ *     dgr_ordered_colsum_noalloc, uses a static device scratch; see there).
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
- *     stream). All work is enqueued on it; nothing synchronises the host.
+ *     stream). All work is enqueued on it; no operation synchronises the host
+ *     (the status reads, dgr_read_device_status and dgr_query_device_status,
+ *     synchronise their stream to return the word).
  *   - Arguments are checked on the host before anything is launched; a bad
  *     argument returns an error code and launches nothing.
  *   - Workspaces: query the size with the matching *_workspace_bytes() call,
