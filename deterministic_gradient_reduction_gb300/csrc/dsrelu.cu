@@ -24,7 +24,9 @@
 //          N-tile partials folded in order into dprob. (Launched as a
 //          programmatic dependent of the GEMM, with the GEMM releasing it at
 //          its start, the pair took 266 us a call against 215 us this way.)
-// Every wait is bounded; no floating-point value depends on timing.
+// Every wait is bounded; no floating-point value depends on timing. A timeout
+// aborts the CTA, which then waits (bounded again) for its own TMA copies in
+// flight and for the completion of the MMAs it issued before it frees TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -206,16 +208,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (!ok) {  // aborted: let our copies in flight land before the CTA exits
+            if (!ok) {  // aborted: let our copies in flight land (bounded) before the CTA exits
                 int dummy = 0;
                 for (int s = 0; s < kStages; ++s)
-                    if (armed[s]) mbar_wait(&ctl->full[s], armed_phase[s], &dummy, nullptr, 0);
+                    if (armed[s]) mbar_wait(&ctl->full[s], armed_phase[s], &dummy, nullptr, kWaitLimitNs);
             }
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         uint32_t stage = 0, phase = 0, g = 0;
-        bool ok = true;
+        uint32_t last_stage = 0, last_phase = 0;  // the latest stage-release commit
+        bool committed = false, ok = true;
         for (int64_t tau = blockIdx.x; ok && tau < n_tiles; tau += gridDim.x, ++g) {
             const uint32_t buf = g & 1, tph = (g >> 1) & 1;
             if (!mbar_wait(&ctl->tempty[buf], tph ^ 1, abort_flag, p.hdr, 32)) {
@@ -246,6 +249,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_commit(&ctl->empty[stage]);
                 }
                 __syncwarp();
+                committed = true;
+                last_stage = stage;
+                last_phase = phase;
                 if (++stage == kStages) {
                     stage = 0;
                     phase ^= 1;
@@ -254,6 +260,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             if (lane == 0) mma_commit(&ctl->tfull[buf]);
             __syncwarp();
+        }
+        if (!ok && committed) {
+            // aborted: wait (bounded) until the MMAs issued here are done, as
+            // their latest commit says, before the CTA frees its TMEM and exits
+            int dummy = 0;
+            mbar_wait(&ctl->empty[last_stage], last_phase, &dummy, nullptr, kWaitLimitNs);
         }
     } else if (warp >= 4) {
         // ---------------- epilogue: leaves, tile trees, partials ----------------

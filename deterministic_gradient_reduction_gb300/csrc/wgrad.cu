@@ -20,8 +20,9 @@
 // they take most of the registers; warps 2-3 idle).
 // Rows of a stage past the expert's end are zeroed in shared memory before
 // the MMA reads them (TMA fills rows past the tensor's end with zeros).
-// Every wait is bounded; a timeout records DGR_ERR_TIMEOUT, aborts the CTA,
-// waits for its own TMA copies and frees its TMEM.
+// Every wait is bounded; a timeout records DGR_ERR_TIMEOUT and aborts the
+// CTA, which then waits (bounded again) for its own TMA copies in flight and
+// for the completion of the MMAs it issued before it frees its TMEM.
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -169,16 +170,17 @@ __global__ void __launch_bounds__(kThreadsW, 1)
                     }
                 }
             }
-            if (!ok) {  // aborted: let our copies in flight land before the CTA exits
+            if (!ok) {  // aborted: let our copies in flight land (bounded) before the CTA exits
                 int dummy = 0;
                 for (int s = 0; s < kStages; ++s)
-                    if (armed[s]) mbar_wait(&ctl->full[s], armed_phase[s], &dummy, nullptr, 0);
+                    if (armed[s]) mbar_wait(&ctl->full[s], armed_phase[s], &dummy, nullptr, kWaitLimitNs);
             }
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         uint32_t stage = 0, phase = 0, g = 0;
-        bool ok = true;
+        uint32_t last_stage = 0, last_phase = 0;  // the latest stage-release commit
+        bool committed = false, ok = true;
         for (int tau = blockIdx.x; ok && tau < p.n_tiles; tau += gridDim.x) {
             int e, nb, kb;
             tile_coords(p, tau, e, nb, kb);
@@ -245,6 +247,9 @@ __global__ void __launch_bounds__(kThreadsW, 1)
                         mma_commit(&ctl->empty[stage]);
                     }
                     __syncwarp();
+                    committed = true;
+                    last_stage = stage;
+                    last_phase = phase;
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1;
@@ -254,6 +259,13 @@ __global__ void __launch_bounds__(kThreadsW, 1)
                 if (lane == 0) mma_commit(&ctl->tfull[buf]);
                 __syncwarp();
             }
+        }
+        if (!ok && committed) {
+            // aborted: the tensor pipe may still be running MMAs issued here;
+            // the latest commit completes once all of them are done (bounded),
+            // and only then may the CTA free its TMEM and exit
+            int dummy = 0;
+            mbar_wait(&ctl->empty[last_stage], last_phase, &dummy, nullptr, kWaitLimitNs);
         }
     } else if (warp >= 4) {
         // ---------------- epilogue: fold chunks, add into main_grad ----------------
