@@ -21,6 +21,7 @@ __all__ = [
     "DgrError", "lib", "build", "ordered_colsum", "ordered_rowdot_dprob", "det_index_add",
     "grouped_wgrad_accumulate", "colsum_workspace_bytes", "rowdot_workspace_bytes",
     "index_add_workspace_bytes", "wgrad_workspace_bytes", "workspace", "read_device_status",
+    "ordered_colsum_noalloc", "colsum_noalloc_read_status",
 ]
 
 DTYPE_F32, DTYPE_BF16 = 0, 1
@@ -68,6 +69,9 @@ def lib() -> ctypes.CDLL:
             "dgr_dsrelu_dprob_workspace_bytes": ([I64, I64], SZ),
             "dgr_dsrelu_dprob": ([P, P, P, I32, I64, I64, I64, P, P, I32, P, SZ, P], I32),
             "dgr_diag_wait_timeout": ([I32, I32, P, SZ, P], I32),
+            "dgr_ordered_colsum_noalloc": ([P, I32, I64, I64, I64, I64, I64, P, I32, I32, P], I32),
+            "dgr_colsum_noalloc_read_status": ([I32, P, P], I32),
+            "dgr_diag_noalloc_wait_timeout": ([I32, I32, P], I32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -139,6 +143,29 @@ def ordered_colsum(x: torch.Tensor, out: torch.Tensor, *, accumulate: bool = Fal
         _ptr(x), _dtype(x), B, S, H, x.stride(0), x.stride(1), _ptr(out), int(accumulate), tile_rows,
         _ptr(ws), ws.numel(), _stream(stream)))
     return out
+
+
+def ordered_colsum_noalloc(x: torch.Tensor, out: torch.Tensor, *, accumulate: bool = False, tile_rows: int = 128,
+                           stream=None) -> torch.Tensor:
+    """ordered_colsum without a workspace: the library's static scratch array serves as one (calls
+    needing more than it holds are refused; calls that overlap on the GPU race on it)."""
+    if x.dim() == 2:
+        x = x.unsqueeze(0)
+    B, S, H = x.shape
+    if H > 0 and x.stride(2) != 1:
+        raise ValueError("the last dimension of x must be contiguous")
+    _check("dgr_ordered_colsum_noalloc", lib().dgr_ordered_colsum_noalloc(
+        _ptr(x), _dtype(x), B, S, H, x.stride(0), x.stride(1), _ptr(out), int(accumulate), tile_rows,
+        _stream(stream)))
+    return out
+
+
+def colsum_noalloc_read_status(clear: bool = False, stream=None) -> int:
+    """The status word of the no-alloc column sum's scratch (0 when no device-side error was recorded)."""
+    st = ctypes.c_int32(0)
+    _check("dgr_colsum_noalloc_read_status", lib().dgr_colsum_noalloc_read_status(int(clear), ctypes.byref(st),
+                                                                                  _stream(stream)))
+    return st.value
 
 
 def rowdot_workspace_bytes(M: int, N: int, tile_n: int = 128) -> int:

@@ -25,7 +25,7 @@ extern "C" const char *dgr_status_string(dgr_status s) {
     }
 }
 
-extern "C" int32_t dgr_version(void) { return 102; }
+extern "C" int32_t dgr_version(void) { return 103; }
 
 extern "C" dgr_status dgr_device_supported(int32_t device) {
     int major = 0, minor = 0;

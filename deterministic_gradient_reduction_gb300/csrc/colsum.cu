@@ -693,31 +693,46 @@ extern "C" size_t dgr_colsum_workspace_bytes(int64_t T, int64_t H, int32_t tile_
     return colsum_layout(T, H, tile_rows).total;
 }
 
-extern "C" dgr_status dgr_ordered_colsum(const void *x, int32_t dtype, int64_t B, int64_t S, int64_t H,
-                                         int64_t stride_b, int64_t stride_s, float *out,
-                                         int32_t accumulate, int32_t tile_rows, void *ws, size_t ws_bytes,
-                                         void *stream) {
+namespace dgr {
+namespace {
+
+// Argument checks shared by both entry points (the workspace's own checks are
+// the caller's). `nothing` is set when H = 0: there is nothing to do.
+dgr_status colsum_args(const void *x, int32_t dtype, int64_t B, int64_t S, int64_t H, int64_t stride_b,
+                       int64_t stride_s, const float *out, int32_t tile_rows, bool &nothing) {
+    nothing = false;
     if (dtype != DGR_DTYPE_BF16 && dtype != DGR_DTYPE_F32) return DGR_ERR_INVALID_ARG;
     if (B < 0 || S < 0 || H < 0 || stride_b < 0 || stride_s < 0) return DGR_ERR_INVALID_ARG;
     if (!is_pow2(tile_rows) || tile_rows > 4096) return DGR_ERR_INVALID_ARG;
     if (H > 4096 || (S > 0 && B > INT32_MAX / S)) return DGR_ERR_UNSUPPORTED;
-    const int64_t T = B * S;
-    if (H == 0) return DGR_OK;
-    if (!out || (T > 0 && !x)) return DGR_ERR_INVALID_ARG;
-    if (!aligned(out, 4)) return DGR_ERR_MISALIGNED;
-    const Layout L = colsum_layout(T, H, tile_rows);
-    if (T > 0) {
-        if (!ws) return DGR_ERR_INVALID_ARG;
-        if (ws_bytes < L.total) return DGR_ERR_WORKSPACE_TOO_SMALL;
-        if (!aligned(ws, kAlign)) return DGR_ERR_MISALIGNED;
+    if (H == 0) {
+        nothing = true;
+        return DGR_OK;
     }
+    if (!out || (B * S > 0 && !x)) return DGR_ERR_INVALID_ARG;
+    if (!aligned(out, 4)) return DGR_ERR_MISALIGNED;
+    return DGR_OK;
+}
+
+// The input's alignment and its overlap with out.
+dgr_status colsum_input_checks(const void *x, int32_t dtype, int64_t B, int64_t S, int64_t H, int64_t stride_b,
+                               int64_t stride_s, const float *out) {
     const int esize = dtype == DGR_DTYPE_BF16 ? 2 : 4;
+    const int64_t T = B * S;
     if (x && !aligned(x, esize)) return DGR_ERR_MISALIGNED;
     const int64_t x_extent = T > 0 ? ((B - 1) * stride_b + (S - 1) * stride_s + H) * esize : 0;
     if (ranges_overlap(out, H * 4, x, x_extent)) return DGR_ERR_ALIAS;
-    if (T > 0 && ranges_overlap(out, H * 4, ws, L.total)) return DGR_ERR_ALIAS;
-    dgr_status st = check_device();
-    if (st != DGR_OK) return st;
+    return DGR_OK;
+}
+
+// Enqueues the call on `stream` once every argument has been checked; ws holds
+// at least colsum_layout(B*S, H, tile_rows).total zeroed bytes.
+dgr_status colsum_enqueue(const void *x, int32_t dtype, int64_t B, int64_t S, int64_t H, int64_t stride_b,
+                          int64_t stride_s, float *out, int32_t accumulate, int32_t tile_rows, void *ws,
+                          void *stream) {
+    const int64_t T = B * S;
+    const Layout L = colsum_layout(T, H, tile_rows);
+    const int esize = dtype == DGR_DTYPE_BF16 ? 2 : 4;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (T == 0) {
         if (accumulate) return DGR_OK;
@@ -808,6 +823,29 @@ extern "C" dgr_status dgr_ordered_colsum(const void *x, int32_t dtype, int64_t B
                    : launch_rpt<DGR_DTYPE_F32, 1>(p, rpt, static_cast<int>(grid), smem_bytes, s);
 }
 
+}  // namespace
+}  // namespace dgr
+
+extern "C" dgr_status dgr_ordered_colsum(const void *x, int32_t dtype, int64_t B, int64_t S, int64_t H,
+                                         int64_t stride_b, int64_t stride_s, float *out,
+                                         int32_t accumulate, int32_t tile_rows, void *ws, size_t ws_bytes,
+                                         void *stream) {
+    bool nothing = false;
+    dgr_status st = colsum_args(x, dtype, B, S, H, stride_b, stride_s, out, tile_rows, nothing);
+    if (st != DGR_OK || nothing) return st;
+    const int64_t T = B * S;
+    const Layout L = colsum_layout(T, H, tile_rows);
+    if (T > 0) {
+        if (!ws) return DGR_ERR_INVALID_ARG;
+        if (ws_bytes < L.total) return DGR_ERR_WORKSPACE_TOO_SMALL;
+        if (!aligned(ws, kAlign)) return DGR_ERR_MISALIGNED;
+    }
+    if ((st = colsum_input_checks(x, dtype, B, S, H, stride_b, stride_s, out)) != DGR_OK) return st;
+    if (T > 0 && ranges_overlap(out, H * 4, ws, L.total)) return DGR_ERR_ALIAS;
+    if ((st = check_device()) != DGR_OK) return st;
+    return colsum_enqueue(x, dtype, B, S, H, stride_b, stride_s, out, accumulate, tile_rows, ws, stream);
+}
+
 // ---------------------------------------------------------------------------
 // Column sum without a caller workspace.
 //
@@ -819,8 +857,11 @@ extern "C" dgr_status dgr_ordered_colsum(const void *x, int32_t dtype, int64_t B
 // GPU that loads the library until the process exits). The host cannot use
 // the array's name as a device address (it is a host-side stand-in), so the
 // first call on each device looks the address up with cudaGetSymbolAddress
-// while that device is current and keeps it.
+// while that device is current and keeps it (only a lookup that succeeded is
+// kept). A device-side error of a call is recorded in the array's first word,
+// which dgr_colsum_noalloc_read_status() reads.
 // ---------------------------------------------------------------------------
+#include <atomic>
 #include <mutex>
 
 namespace dgr {
@@ -831,43 +872,62 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_colsum_scratch[kStaticScratchBytes];
 
-std::once_flag g_scratch_once[kMaxDevices];
-void *g_scratch_ptr[kMaxDevices];
-cudaError_t g_scratch_err[kMaxDevices];
+// Device addresses of the array, one per device, set only by a lookup that
+// succeeded (a failed one, e.g. during a stream capture, is tried again).
+std::atomic<void *> g_scratch_ptr[kMaxDevices];
+std::mutex g_scratch_mu;
 
-dgr_status static_scratch(void **ptr) {
+}  // namespace
+
+dgr_status noalloc_scratch(void **ptr) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return DGR_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return DGR_ERR_UNSUPPORTED;
-    std::call_once(g_scratch_once[dev], [dev] {
-        void *p = nullptr;
-        g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_colsum_scratch);
-        g_scratch_ptr[dev] = p;
-    });
-    if (g_scratch_err[dev] != cudaSuccess || !g_scratch_ptr[dev]) return DGR_ERR_CUDA;
-    *ptr = g_scratch_ptr[dev];
+    void *p = g_scratch_ptr[dev].load(std::memory_order_acquire);
+    if (!p) {
+        std::lock_guard<std::mutex> lock(g_scratch_mu);
+        p = g_scratch_ptr[dev].load(std::memory_order_relaxed);
+        if (!p) {
+            if (cudaGetSymbolAddress(&p, g_colsum_scratch) != cudaSuccess || !p) {
+                cudaGetLastError();
+                return DGR_ERR_CUDA;
+            }
+            g_scratch_ptr[dev].store(p, std::memory_order_release);
+        }
+    }
+    *ptr = p;
     return DGR_OK;
 }
 
-}  // namespace
 }  // namespace dgr
 
 extern "C" dgr_status dgr_ordered_colsum_noalloc(const void *x, int32_t dtype, int64_t B, int64_t S, int64_t H,
                                                  int64_t stride_b, int64_t stride_s, float *out,
                                                  int32_t accumulate, int32_t tile_rows, void *stream) {
-    if (B < 0 || S < 0 || H < 0 || H > 4096 || !is_pow2(tile_rows) || tile_rows > 4096 ||
-        (S > 0 && B > INT32_MAX / S))
-        return dgr_ordered_colsum(x, dtype, B, S, H, stride_b, stride_s, out, accumulate, tile_rows, nullptr, 0,
-                                  stream);  // the same argument errors as the workspace form
-    const Layout L = colsum_layout(B * S, H, tile_rows);
+    // every argument is checked before the shared array is touched: a refused
+    // call enqueues nothing
+    bool nothing = false;
+    dgr_status st = colsum_args(x, dtype, B, S, H, stride_b, stride_s, out, tile_rows, nothing);
+    if (st != DGR_OK || nothing) return st;
+    const int64_t T = B * S;
+    const Layout L = colsum_layout(T, H, tile_rows);
     if (L.total > kStaticScratchBytes) return DGR_ERR_WORKSPACE_TOO_SMALL;
+    if ((st = colsum_input_checks(x, dtype, B, S, H, stride_b, stride_s, out)) != DGR_OK) return st;
+    if ((st = check_device()) != DGR_OK) return st;
     void *ws = nullptr;
-    dgr_status st = static_scratch(&ws);
-    if (st != DGR_OK) return st;
+    if ((st = noalloc_scratch(&ws)) != DGR_OK) return st;
     // The array keeps whatever the previous call (of any shape, or one that
-    // ended in an error) left; the call's region must start at zero.
-    if (B * S > 0 && H > 0 && cudaMemsetAsync(ws, 0, L.total, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    // ended in an error) left; the call's whole region starts at zero.
+    if (T > 0 && cudaMemsetAsync(ws, 0, L.total, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return DGR_ERR_CUDA;
-    return dgr_ordered_colsum(x, dtype, B, S, H, stride_b, stride_s, out, accumulate, tile_rows, ws,
-                              kStaticScratchBytes, stream);
+    return colsum_enqueue(x, dtype, B, S, H, stride_b, stride_s, out, accumulate, tile_rows, ws, stream);
+}
+
+extern "C" dgr_status dgr_colsum_noalloc_read_status(int32_t clear, int32_t *status, void *stream) {
+    if (!status) return DGR_ERR_INVALID_ARG;
+    dgr_status st = check_device();
+    if (st != DGR_OK) return st;
+    void *ws = nullptr;
+    if ((st = noalloc_scratch(&ws)) != DGR_OK) return st;
+    return dgr_read_device_status(ws, clear, status, stream);
 }

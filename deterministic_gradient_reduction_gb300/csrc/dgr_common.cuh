@@ -126,6 +126,10 @@ inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_
 // Checks the current device is compute capability 10.3.
 dgr_status check_device();
 
+// Device address, on the current device, of the column sum's static scratch
+// array (the no-alloc entry's scratch); looked up once per device.
+dgr_status noalloc_scratch(void **ptr);
+
 inline dgr_status launch_status() {
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? DGR_OK : DGR_ERR_CUDA;

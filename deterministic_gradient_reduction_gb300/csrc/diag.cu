@@ -38,3 +38,16 @@ extern "C" dgr_status dgr_diag_wait_timeout(int32_t which, int32_t limit_us, voi
         which, static_cast<uint64_t>(limit_us) * 1000ull, static_cast<WsHeader *>(ws));
     return launch_status();
 }
+
+extern "C" dgr_status dgr_diag_noalloc_wait_timeout(int32_t which, int32_t limit_us, void *stream) {
+    if ((which != 0 && which != 1) || limit_us < 1 || limit_us > 1000000) return DGR_ERR_INVALID_ARG;
+    dgr_status st = check_device();
+    if (st != DGR_OK) return st;
+    void *ws = nullptr;
+    if ((st = noalloc_scratch(&ws)) != DGR_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(ws, 0, sizeof(WsHeader), s) != cudaSuccess) return DGR_ERR_CUDA;
+    wait_timeout_kernel<<<1, 32, 0, s>>>(which, static_cast<uint64_t>(limit_us) * 1000ull,
+                                         static_cast<WsHeader *>(ws));
+    return launch_status();
+}

@@ -67,9 +67,29 @@ struct IdxParams {
     int32_t *cnt;                // [2][nb][256] per-tile digit counts of the two passes
     int32_t *incl;               // [2][nb][256] published inclusive counts (bit 31: published)
     int32_t *heavy_rows;         // split rows longer than kWarpFoldTiles tiles (fold-block work)
+    int32_t max_fold_rows;       // capacity of heavy_rows
     float *slots;
-    WsHeader *hdr;  // pad[2]: bad-index total, pad[3]: fold-row count
+    WsHeader *hdr;  // pad[2]: bad-index total, pad[3]: fold-row count, pad[8..10]: layout tag
 };
+
+// Layout tag (header words 8-10): N, R + 1 and a constant, all non-zero,
+// written by the first call on a zeroed workspace. The regions of the
+// workspace move with N and R, and the arrays one call leaves behind (keys,
+// permutation) would be read as counters by a call of other sizes, so every
+// call checks the tag before it writes anything. hist accepts words that are
+// still zero (a fresh workspace whose tag block 0 is writing); the later
+// launches, which start after hist has completed, want the exact tag.
+constexpr int32_t kTagMagic = 0x31584449;
+constexpr int kTagWord = 8;
+
+__device__ __forceinline__ bool tag_word_ok(int32_t have, int32_t want) { return have == 0 || have == want; }
+
+__device__ __forceinline__ bool tag_exact(const IdxParams &p) {
+    const volatile int32_t *t = p.hdr->pad + kTagWord;
+    return t[0] == p.N && t[1] == p.R + 1 && t[2] == kTagMagic;
+}
+
+__device__ __forceinline__ int32_t clampi(int32_t v, int32_t lo, int32_t hi) { return min(max(v, lo), hi); }
 
 __device__ __forceinline__ int32_t map_key(int32_t v, int32_t R, bool &bad) {
     if (v >= 0 && v < R) return v;
@@ -95,17 +115,11 @@ __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.w
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kSortThreads) hist_kernel(const IdxParams p) {
     __shared__ int32_t h[2][kDigits];
-    __shared__ int32_t bad_block, pad_block;
+    __shared__ int32_t bad_block, pad_block, tag_ok;
     const int tid = threadIdx.x;
     launch_dependents();
     h[0][tid] = 0;
     h[1][tid] = 0;
-    if (tid == 0) {
-        bad_block = 0;
-        pad_block = 0;
-    }
-    if (blockIdx.x == 0 && tid == 0) p.hdr->pad[3] = 0;  // fold-row list of this call starts empty
-    __syncthreads();
     int32_t v[kSortItems];
 #pragma unroll
     for (int r = 0; r < kSortItems; ++r) {
@@ -113,6 +127,25 @@ __global__ void __launch_bounds__(kSortThreads) hist_kernel(const IdxParams p) {
         v[r] = 0;
         ldg_nc_b32_if(v[r], p.idx + e, e < p.N);
     }
+    if (tid == 0) {
+        bad_block = 0;
+        pad_block = 0;
+        const volatile int32_t *t = p.hdr->pad + kTagWord;
+        const int32_t t0 = t[0], t1 = t[1], t2 = t[2];
+        tag_ok = tag_word_ok(t0, p.N) && tag_word_ok(t1, p.R + 1) && tag_word_ok(t2, kTagMagic);
+        if (blockIdx.x == 0) {
+            if (tag_ok) {
+                p.hdr->pad[3] = 0;  // fold-row list of this call starts empty
+                p.hdr->pad[kTagWord] = p.N;
+                p.hdr->pad[kTagWord + 1] = p.R + 1;
+                p.hdr->pad[kTagWord + 2] = kTagMagic;
+            } else {
+                record_error(p.hdr, DGR_ERR_INVALID_ARG, 40);
+            }
+        }
+    }
+    __syncthreads();
+    if (!tag_ok) return;  // a workspace laid out for other sizes: nothing is written
     int my_bad = 0;
 #pragma unroll
     for (int r = 0; r < kSortItems; ++r) {
@@ -269,6 +302,7 @@ __global__ void __launch_bounds__(kPassThreads) pass_kernel(const IdxParams p) {
     for (int q = tid; q < kSortWarps * kDigits; q += kPassThreads) (&cnt[0][0])[q] = 0;
     launch_dependents();
     grid_dep_wait();
+    if (!tag_exact(p)) return;  // hist refused the workspace (the same answer in every thread)
     __syncthreads();
     int32_t key[kSortItems], val[kSortItems], rank[kSortItems];
     int32_t gx = 0, my_count = 0;
@@ -298,6 +332,8 @@ __global__ void __launch_bounds__(kPassThreads) pass_kernel(const IdxParams p) {
             } else if (PASS == 0) {
                 bool bad = false;
                 key[r] = map_key(key[r], p.R, bad);
+            } else {
+                key[r] = clampi(key[r], 0, p.R);  // a key read back from the workspace stays a key
             }
         }
 #pragma unroll
@@ -380,7 +416,9 @@ __global__ void __launch_bounds__(kPassThreads) pass_kernel(const IdxParams p) {
         for (int r = 0; r < kSortItems; ++r) {
             if (key[r] < 0) continue;
             const int d = pass_digit<PASS>(key[r]);
-            const int32_t lp = lbase[d] + cnt[w][d] + rank[r];
+            // the local bases come from counts in the workspace: keep the
+            // position inside the tile whatever they hold
+            const int32_t lp = clampi(lbase[d] + cnt[w][d] + rank[r], 0, kSortTile - 1);
             sk[lp] = key[r];
             sv[lp] = val[r];
         }
@@ -390,10 +428,12 @@ __global__ void __launch_bounds__(kPassThreads) pass_kernel(const IdxParams p) {
         // (in any order: each row is folded by one block, the same way)
         const int32_t k = b * kDigits + (tid - kSortThreads);
         if (k <= p.R) {
-            p.seg_start[k] = dbase_s[b] + kx;
+            p.seg_start[k] = clampi(dbase_s[b] + kx, 0, p.N);
             if (k == p.R) p.seg_start[p.R + 1] = p.N;
-            if (p.seg_tile == kSegTile && kc > kWarpFoldTiles * kSegTile)
-                p.heavy_rows[atomicAdd(&p.hdr->pad[3], 1)] = k;
+            if (p.seg_tile == kSegTile && kc > kWarpFoldTiles * kSegTile) {
+                const int32_t at = atomicAdd(&p.hdr->pad[3], 1);
+                if (at < p.max_fold_rows) p.heavy_rows[at] = k;
+            }
             p.count[k] = 0;  // read no more: cleared for the next call
         }
         if (b == 0 && tid == kSortThreads) {  // every hist block has counted by now
@@ -410,9 +450,10 @@ __global__ void __launch_bounds__(kPassThreads) pass_kernel(const IdxParams p) {
     for (int r = 0; r < kSortTile / kPassThreads; ++r) {
         const int i = r * kPassThreads + tid;
         if (i >= n_here) continue;
-        const int32_t k = sk[i];
+        const int32_t k = clampi(sk[i], 0, p.R);
         const int d = pass_digit<PASS>(k);
-        const int32_t pos = gbase[d] + (i - lbase[d]);
+        // digit bases come from counts in the workspace: the write stays in [0, N)
+        const int32_t pos = clampi(gbase[d] + (i - lbase[d]), 0, p.N - 1);
         if (PASS == 0) {
             p.keys_a[pos] = k;
             p.vals_a[pos] = sv[i];
@@ -513,6 +554,9 @@ __device__ __forceinline__ void load_seg(const IdxParams &p, int32_t kc, int32_t
     st = en = 0;
     ldg_nc_b32_if(st, &p.seg_start[k], lane < k_end - kc);
     ldg_nc_b32_if(en, &p.seg_start[k + 1], lane < k_end - kc);
+    // segment starts are workspace words: every row stays inside [0, N)
+    st = clampi(st, 0, p.N);
+    en = clampi(en, st, p.N);
 }
 
 __device__ __forceinline__ KeyRows key_rows(int32_t kc, int32_t k_end, int32_t st, int32_t en, int gs, bool split_on,
@@ -717,7 +761,7 @@ __device__ __forceinline__ void issue_group(const IdxParams &p, float4 *slot, in
     const int nv = gd_nv(gd);
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-        const int32_t row = __shfl_sync(full, Q.pq, j * 8 + u);
+        const int32_t row = clampi(__shfl_sync(full, Q.pq, j * 8 + u), 0, p.N - 1);  // a perm entry is a row of src
         cp_async16_if(slot + u * 32 + lane, p.src + static_cast<int64_t>(row) * p.ld_src + col, u < nv && act);
     }
     cp_async16_if(slot + 8 * 32 + lane, p.out + static_cast<int64_t>(gd_key(gd)) * p.ld_out + col,
@@ -778,8 +822,8 @@ __device__ __forceinline__ void consume_group(const IdxParams &p, const float4 *
 // kStages - 1 groups ahead of the sums.
 __device__ void walk(const IdxParams &p, int32_t P0, int32_t P1, int lane, float4 *ring, int32_t *dring) {
     // keys from the one at P0 to the one at P1: key_rows keeps what starts in [P0, P1)
-    const int32_t k_first = p.skey[P0];
-    const int32_t k_end = P1 < p.N ? p.skey[P1] + 1 : p.R + 1;
+    const int32_t k_first = clampi(p.skey[P0], 0, p.R);
+    const int32_t k_end = P1 < p.N ? clampi(p.skey[P1] + 1, k_first, p.R + 1) : p.R + 1;
     const int gs = min(8, p.seg_tile);
     const int gpt = p.seg_tile / gs;
     const bool split_on = p.seg_tile == kSegTile;
@@ -850,8 +894,8 @@ __device__ void fold_rows(const IdxParams &p, int first, int stride, int n_rows,
     __shared__ int timed_out;
     const int tid = threadIdx.x, lane = tid & 31;
     for (int i = first; i < n_rows; i += stride) {
-        const int32_t k = p.heavy_rows[i];
-        const int64_t s0 = p.seg_start[k], e0 = p.seg_start[k + 1];
+        const int32_t k = clampi(p.heavy_rows[i], 0, p.R);
+        const int32_t s0 = clampi(p.seg_start[k], 0, p.N), e0 = clampi(p.seg_start[k + 1], s0, p.N);
         const int32_t T = static_cast<int32_t>((e0 - s0 + kSegTile - 1) / kSegTile);
         if (tid == 0) {
             timed_out = wait_counter_geq(&p.tickets[k], T * ((p.D + 127) / 128)) ? 0 : 1;
@@ -902,6 +946,7 @@ __global__ void __launch_bounds__(kSegThreads, 1) segsum_kernel(const IdxParams 
     extern __shared__ __align__(16) float4 seg_smem[];
     const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
     grid_dep_wait();
+    if (!tag_exact(p)) return;  // hist refused the workspace: nothing is written
     {  // what the sort passes leave behind, cleared for the next call
         const int64_t tiles = static_cast<int64_t>(p.nb) * kDigits;
         const int64_t g = static_cast<int64_t>(blockIdx.x) * kSegThreads + threadIdx.x;
@@ -912,7 +957,7 @@ __global__ void __launch_bounds__(kSegThreads, 1) segsum_kernel(const IdxParams 
         if (g < 2 * kDigits) p.hist[g] = 0;
     }
     if (p.D == 0) return;
-    const int n_fold_rows = p.seg_tile == kSegTile ? p.hdr->pad[3] : 0;
+    const int n_fold_rows = p.seg_tile == kSegTile ? clampi(p.hdr->pad[3], 0, p.max_fold_rows) : 0;
     const int n_fold = min(n_fold_rows, min(kMaxFoldBlocks, static_cast<int>(gridDim.x) - 1));
     if (static_cast<int>(blockIdx.x) < n_fold) {
         fold_rows(p, blockIdx.x, n_fold, n_fold_rows, seg_smem);
@@ -1051,6 +1096,7 @@ extern "C" dgr_status dgr_det_index_add(float *out, int64_t R, int64_t D, int64_
     p.tickets = reinterpret_cast<int32_t *>(w + L.tickets);
     p.slots = reinterpret_cast<float *>(w + L.slots);
     p.heavy_rows = reinterpret_cast<int32_t *>(w + L.heavy);
+    p.max_fold_rows = L.max_fold_rows;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||

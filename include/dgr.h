@@ -66,7 +66,8 @@ const char *dgr_status_string(dgr_status s);
 
 /* Library ABI version (major * 100 + minor). 1.01 added sections 5-8 (grouped
  * dbias, canonical top-K, aux-loss scalar, dsReLU dprob); 1.02 added
- * dgr_query_device_status; earlier entries unchanged. */
+ * dgr_query_device_status; 1.03 added dgr_colsum_noalloc_read_status;
+ * earlier entries unchanged. */
 int32_t dgr_version(void);
 
 /* DGR_OK when `device` is a compute capability 10.3 GPU, else DGR_ERR_UNSUPPORTED. */
@@ -129,16 +130,32 @@ dgr_status dgr_ordered_colsum(const void *x, int32_t dtype, int64_t B, int64_t S
  * that loads it, until the process exits); nothing is allocated. A call whose
  * dgr_colsum_workspace_bytes(B*S, H, tile_rows) exceeds that size returns
  * DGR_ERR_WORKSPACE_TOO_SMALL and launches nothing.
- * The first call on a device looks up the array's device address (with that
- * device current); make that first call before any stream capture. Each call
- * clears the array's counters on `stream` before its kernel. All calls share
- * the one array: calls that can overlap on the GPU (different streams, or
- * different host threads without ordering) race and give wrong results.
+ * Every argument is checked before the array is touched: a refused call
+ * enqueues nothing. The first call on a device looks up the array's device
+ * address (with that device current; a lookup that fails is tried again on
+ * the next call); make that first call before any stream capture. Each call
+ * then zeroes the part of the array it uses, the whole
+ * dgr_colsum_workspace_bytes(B*S, H, tile_rows) bytes (one cudaMemsetAsync on
+ * `stream` before its kernel), so a call never depends on what an earlier
+ * call left there. All calls share the one array: calls that can overlap on
+ * the GPU (different streams, or different host threads without ordering)
+ * race and give wrong results.
  */
 #define DGR_COLSUM_NOALLOC_SCRATCH_BYTES (4u << 20)
 dgr_status dgr_ordered_colsum_noalloc(const void *x, int32_t dtype, int64_t B, int64_t S, int64_t H,
                                       int64_t stride_b, int64_t stride_s, float *out, int32_t accumulate,
                                       int32_t tile_rows, void *stream);
+
+/*
+ * The status word of the no-alloc column sum's array on the current device,
+ * as dgr_read_device_status() reads a workspace's: synchronises `stream`,
+ * copies the word to *status (host pointer; DGR_OK when no device-side error
+ * was recorded, DGR_ERR_TIMEOUT when a bounded wait ran out) and with
+ * clear != 0 then zeroes it. The next dgr_ordered_colsum_noalloc() call
+ * zeroes the word again, so read it after the call of interest and before the
+ * next one (ordered on `stream`). Returns the read's own error, if any.
+ */
+dgr_status dgr_colsum_noalloc_read_status(int32_t clear, int32_t *status, void *stream);
 
 /* ------------------------------------------------------------------------ */
 /* 2. Ordered per-row dprob                                                  */
@@ -192,7 +209,14 @@ dgr_status dgr_ordered_rowdot_dprob(const void *dY, const void *Y, int32_t dtype
  *           need 16-byte alignment (ld_* and D multiples of 4).
  * ws:       dgr_index_add_workspace_bytes(N, R, D) bytes, zeroed once; it
  *           then serves every call with the same N and R and any D' <= D
- *           (D' = 0 included: the call then only counts bad indices).
+ *           (D' = 0 included: the call then only counts bad indices). The
+ *           first call records N and R in the workspace header; a later call
+ *           with another N or R is refused on the device: it records
+ *           DGR_ERR_INVALID_ARG in the status word and writes nothing (out and
+ *           bad_count untouched); zero the workspace before using it for
+ *           other sizes. Offsets read back from the workspace are clamped to
+ *           their arrays, so a workspace left inconsistent (e.g. by a call that
+ *           timed out) gives wrong sums, never an access out of bounds.
  * out must not overlap src, idx, bad_count or ws.
  */
 size_t dgr_index_add_workspace_bytes(int64_t N, int64_t R, int64_t D);

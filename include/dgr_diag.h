@@ -50,6 +50,14 @@ dgr_status dgr_tc_probe_k16(const uint16_t *A, const uint16_t *B, const float *C
  */
 dgr_status dgr_diag_wait_timeout(int32_t which, int32_t limit_us, void *ws, size_t ws_bytes, void *stream);
 
+/*
+ * The same timeout on the status word of the no-alloc column sum's static
+ * array (its 256-byte header is zeroed first, on `stream`): afterwards
+ * dgr_colsum_noalloc_read_status() returns DGR_ERR_TIMEOUT, as it would after
+ * a column-sum folder gave up. Shares the array with every no-alloc call.
+ */
+dgr_status dgr_diag_noalloc_wait_timeout(int32_t which, int32_t limit_us, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

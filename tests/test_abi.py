@@ -33,7 +33,8 @@ def test_header_declares_every_operation():
     names = declared_functions()
     for op in ("dgr_ordered_colsum", "dgr_ordered_rowdot_dprob", "dgr_det_index_add",
                "dgr_grouped_wgrad_accumulate", "dgr_grouped_dbias", "dgr_topk_canonicalize", "dgr_aux_loss",
-               "dgr_dsrelu_dprob", "dgr_ordered_colsum_noalloc", "dgr_tc_probe_k16", "dgr_diag_wait_timeout"):
+               "dgr_dsrelu_dprob", "dgr_ordered_colsum_noalloc", "dgr_colsum_noalloc_read_status",
+               "dgr_tc_probe_k16", "dgr_diag_wait_timeout", "dgr_diag_noalloc_wait_timeout"):
         assert op in names
 
 
@@ -56,7 +57,7 @@ def test_library_is_built_for_sm_103a_only():
 
 
 def test_status_strings_and_version(L):
-    assert L.dgr_version() >= 102
+    assert L.dgr_version() >= 103
     for code, name in dgr.STATUS.items():
         assert L.dgr_status_string(code).decode() == name
     assert L.dgr_status_string(99).decode() == "DGR_ERR_UNKNOWN"
@@ -173,3 +174,18 @@ def test_wait_timeout_diag_host_checks(L):
     assert L.dgr_diag_wait_timeout(0, 0, ws, 256, None) == 1          # no time at all
     assert L.dgr_diag_wait_timeout(0, 1000, ws, 64, None) == 3        # workspace below the header
     assert L.dgr_diag_wait_timeout(0, 1000, _p(0x100008), 256, None) == 5
+
+
+def test_noalloc_host_checks(L):
+    # the no-alloc column sum checks every argument before it touches its
+    # static scratch (no device is needed to see these refusals)
+    fake, out = _p(0x10000), _p(0x20000)
+    assert L.dgr_ordered_colsum_noalloc(fake, 7, 1, 4, 4, 16, 4, out, 0, 128, None) == 1        # bad dtype
+    assert L.dgr_ordered_colsum_noalloc(fake, 1, 1, 4, 4, 16, 4, None, 0, 128, None) == 1       # null out
+    assert L.dgr_ordered_colsum_noalloc(fake, 1, 1, 4, 4, 16, 4, out, 0, 100, None) == 1        # tile not pow2
+    assert L.dgr_ordered_colsum_noalloc(fake, 1, 1, 1 << 20, 512, 512 * (1 << 20), 512, out, 0, 128,
+                                        None) == 3                                               # beyond scratch
+    assert L.dgr_ordered_colsum_noalloc(_p(0x20000), 1, 1, 64, 16, 0, 16, _p(0x20010), 0, 128, None) == 4
+    assert L.dgr_ordered_colsum_noalloc(_p(0x10001), 1, 1, 64, 16, 0, 16, out, 0, 128, None) == 5  # x misaligned
+    assert L.dgr_colsum_noalloc_read_status(0, None, None) == 1
+    assert L.dgr_diag_noalloc_wait_timeout(2, 1000, None) == 1

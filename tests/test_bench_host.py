@@ -49,3 +49,15 @@ def test_host_cpu_names_a_model_and_counts_cores():
     h = bench.host_cpu()
     assert isinstance(h["cpu_model"], str) and h["cpu_model"]
     assert h["host_cores"] >= 1
+
+
+def test_tensor_peak_follows_the_clock_record():
+    peaks = {"bf16": 1916.5, "bf16_sus": 1702.9}
+    # a short window at full clock, no reason active: the burst figure
+    assert bench.tensor_peak(peaks, {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}) == (1916.5,
+                                                                                              "bf16 burst")
+    # the power cap, or clocks held well below maximum: the sustained figure
+    assert bench.tensor_peak(peaks, {"sm_mhz": 1950.0, "sm_max_mhz": 2070.0,
+                                     "reasons": ["sw_power_cap"]})[1] == "bf16 sustained"
+    assert bench.tensor_peak(peaks, {"sm_mhz": 1700.0, "sm_max_mhz": 2070.0, "reasons": []})[0] == 1702.9
+    assert bench.tensor_peak(peaks, None) == (1916.5, "bf16 burst")

@@ -167,3 +167,34 @@ def test_workspace_reused_with_fewer_columns():
             got = _gpu(half, ws=ws)
             assert_bits_equal(got.cpu().numpy(), want_half, f"N={N} D={D // 2} R={R} in a D={D} workspace")
         assert dgr.read_device_status(ws) == 0
+
+
+def test_workspace_of_other_sizes_is_refused():
+    # a workspace records the N and R of its first call; a call with other
+    # sizes would read the first call's sorted keys as its counters, so it is
+    # refused on the device: DGR_ERR_INVALID_ARG in the status word, out and
+    # the bad-index count untouched, the workspace itself unchanged
+    big = gi.index_add_input(70000, 128, 60000, seed=950, out_init="zeros")
+    small = gi.index_add_input(3000, 8, 5000, seed=951, out_init="random")
+    ws = dgr.workspace(dgr.index_add_workspace_bytes(70000, 60000, 128))
+    assert ws.numel() >= dgr.index_add_workspace_bytes(3000, 5000, 8)
+    want_big, _ = _oracle(big)
+    assert_bits_equal(_gpu(big, ws=ws).cpu().numpy(), want_big, "first call")
+    assert dgr.read_device_status(ws) == 0
+    snapshot = ws.clone()
+    badc = torch.full((1,), -7, dtype=torch.int32, device="cuda")
+    out0 = small.out.cuda()
+    got = _gpu(small, dev=(small.src.cuda(), small.idx.cuda(), out0), ws=ws, bad=badc)
+    assert dgr.read_device_status(ws) == 1  # DGR_ERR_INVALID_ARG
+    assert torch.equal(got.view(torch.int32), out0.view(torch.int32))
+    assert int(badc.item()) == -7
+    assert torch.equal(ws[256:], snapshot[256:])  # past the header: nothing written
+    # the status cleared, the workspace still serves its own sizes
+    assert dgr.read_device_status(ws, clear=True) == 1
+    assert_bits_equal(_gpu(big, ws=ws).cpu().numpy(), want_big, "first sizes again")
+    assert dgr.read_device_status(ws) == 0
+    # zeroed, it serves the other sizes
+    ws.zero_()
+    want_small, _ = _oracle(small)
+    assert_bits_equal(_gpu(small, ws=ws).cpu().numpy(), want_small, "other sizes after zeroing")
+    assert dgr.read_device_status(ws) == 0
