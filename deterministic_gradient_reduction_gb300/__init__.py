@@ -12,6 +12,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+from contextlib import nullcontext as _nullcontext
 
 import torch
 
@@ -72,6 +73,10 @@ def lib() -> ctypes.CDLL:
             "dgr_ordered_colsum_noalloc": ([P, I32, I64, I64, I64, I64, I64, P, I32, I32, P], I32),
             "dgr_colsum_noalloc_read_status": ([I32, P, P], I32),
             "dgr_diag_noalloc_wait_timeout": ([I32, I32, P], I32),
+            "dgr_diag_set_schedule": ([I32, ctypes.c_uint32, I32], I32),
+            "dgr_diag_colsum_plan": ([I64, I64, I32, I32, I32, I32, I32, I32, P], I32),
+            "dgr_diag_atomic_colsum": ([P, I64, I32, P, P], I32),
+            "dgr_diag_atomic_rowdot": ([P, P, I64, I32, P, P], I32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -103,9 +108,14 @@ def _dtype(t: torch.Tensor) -> int:
     raise TypeError(f"bf16 or fp32 expected, got {t.dtype}")
 
 
-def workspace(nbytes: int, device=None) -> torch.Tensor:
-    """A zeroed, 256-byte aligned device workspace of at least nbytes."""
-    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+def workspace(nbytes: int, device=None, stream=None) -> torch.Tensor:
+    """A zeroed, 256-byte aligned device workspace of at least nbytes. With a stream, it is
+    allocated and zeroed on that stream (the stream the call that uses it runs on), so the
+    zeroing is ordered before the call whatever torch's current stream is doing."""
+    if stream is None:
+        return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+    with torch.cuda.stream(stream):
+        return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
 
 
 def read_device_status(ws: torch.Tensor, clear: bool = False, stream=None) -> int:
@@ -138,7 +148,7 @@ def ordered_colsum(x: torch.Tensor, out: torch.Tensor, *, accumulate: bool = Fal
     if H > 0 and x.stride(2) != 1:
         raise ValueError("the last dimension of x must be contiguous")
     if ws is None:
-        ws = workspace(colsum_workspace_bytes(B * S, H, tile_rows), x.device)
+        ws = workspace(colsum_workspace_bytes(B * S, H, tile_rows), x.device, stream)
     _check("dgr_ordered_colsum", lib().dgr_ordered_colsum(
         _ptr(x), _dtype(x), B, S, H, x.stride(0), x.stride(1), _ptr(out), int(accumulate), tile_rows,
         _ptr(ws), ws.numel(), _stream(stream)))
@@ -200,7 +210,7 @@ def det_index_add(out: torch.Tensor, src: torch.Tensor, idx: torch.Tensor, *, se
     if out.shape[1] != D or idx.shape != (N,) or idx.dtype != torch.int32:
         raise ValueError("out [R+1, D], src [N, D], idx int32 [N] expected")
     if ws is None:
-        ws = workspace(index_add_workspace_bytes(N, R, D), out.device)
+        ws = workspace(index_add_workspace_bytes(N, R, D), out.device, stream)
     _check("dgr_det_index_add", lib().dgr_det_index_add(
         _ptr(out), R, D, out.stride(0), _ptr(src), src.stride(0), _ptr(idx), N, seg_tile, _ptr(bad_count),
         _ptr(ws), ws.numel(), _stream(stream)))
@@ -219,7 +229,7 @@ def grouped_wgrad_accumulate(G: torch.Tensor, X: torch.Tensor, offs: torch.Tenso
     K = X.shape[1]
     E = offs.numel() - 1
     if ws is None:
-        ws = workspace(wgrad_workspace_bytes(E, N, K), G.device)
+        ws = workspace(wgrad_workspace_bytes(E, N, K), G.device, stream)
     _check("dgr_grouped_wgrad_accumulate", lib().dgr_grouped_wgrad_accumulate(
         _ptr(G), _ptr(X), _ptr(offs), E, T, N, K, _ptr(main_grad), chunk_tokens, _ptr(ws), ws.numel(),
         _stream(stream)))
@@ -239,7 +249,7 @@ def grouped_dbias(dY: torch.Tensor, offs: torch.Tensor, out: torch.Tensor, *, ac
     if out.dim() != 2 or out.shape != (E, H) or out.dtype != torch.float32 or offs.dtype != torch.int64:
         raise ValueError("dY [T, H], offs int64 [E+1], out fp32 [E, H] expected")
     if ws is None:
-        ws = workspace(dbias_workspace_bytes(T, H, E, tile_rows), dY.device)
+        ws = workspace(dbias_workspace_bytes(T, H, E, tile_rows), dY.device, stream)
     _check("dgr_grouped_dbias", lib().dgr_grouped_dbias(
         _ptr(dY), _dtype(dY), T, H, dY.stride(0), _ptr(offs), E, _ptr(out), out.stride(0), int(accumulate),
         tile_rows, _ptr(ws), ws.numel(), _stream(stream)))
@@ -254,9 +264,10 @@ def topk_canonicalize(ids: torch.Tensor, logits: torch.Tensor, out_ids: torch.Te
     if ids.dim() != 2 or ids.dtype != torch.int32 or logits.shape != ids.shape or logits.dtype != torch.float32:
         raise ValueError("ids int32 [R, K] and logits fp32 [R, K] expected")
     R, K = ids.shape
-    out_ids = torch.empty_like(ids) if out_ids is None else out_ids
-    out_logits = torch.empty_like(logits) if out_logits is None else out_logits
-    probs = torch.empty_like(logits) if probs is None else probs
+    with torch.cuda.stream(stream) if stream is not None else _nullcontext():  # outputs live on the call's stream
+        out_ids = torch.empty_like(ids) if out_ids is None else out_ids
+        out_logits = torch.empty_like(logits) if out_logits is None else out_logits
+        probs = torch.empty_like(logits) if probs is None else probs
     ld = out_ids.stride(0)
     if out_logits.stride(0) != ld or probs.stride(0) != ld or any(t.stride(1) != 1 for t in
                                                                   (ids, logits, out_ids, out_logits, probs)):
@@ -280,9 +291,11 @@ def aux_loss(probs: torch.Tensor, tokens_per_expert: torch.Tensor, scale: float,
     N, E = probs.shape
     if tokens_per_expert.shape != (E,) or probs.stride(1) != 1:
         raise ValueError("tokens_per_expert [E] and rows of probs contiguous expected")
-    out = torch.empty(1, dtype=torch.float32, device=probs.device) if out is None else out
+    if out is None:
+        with torch.cuda.stream(stream) if stream is not None else _nullcontext():  # on the call's stream
+            out = torch.empty(1, dtype=torch.float32, device=probs.device)
     if ws is None:
-        ws = workspace(aux_loss_workspace_bytes(N), probs.device)
+        ws = workspace(aux_loss_workspace_bytes(N), probs.device, stream)
     _check("dgr_aux_loss", lib().dgr_aux_loss(
         _ptr(probs), N, E, probs.stride(0), _ptr(tokens_per_expert), float(scale), _ptr(out), _ptr(ws), ws.numel(),
         _stream(stream)))
@@ -305,7 +318,7 @@ def dsrelu_dprob(A: torch.Tensor, B: torch.Tensor, offs: torch.Tensor, dY: torch
     if not (A.is_contiguous() and B.is_contiguous() and dY.is_contiguous()):
         raise ValueError("A, B and dY must be contiguous")
     if ws is None:
-        ws = workspace(dsrelu_dprob_workspace_bytes(T, N), A.device)
+        ws = workspace(dsrelu_dprob_workspace_bytes(T, N), A.device, stream)
     _check("dgr_dsrelu_dprob", lib().dgr_dsrelu_dprob(
         _ptr(A), _ptr(B), _ptr(offs), E, T, K, N, _ptr(dY), _ptr(dprob), int(accumulate), _ptr(ws), ws.numel(),
         _stream(stream)))

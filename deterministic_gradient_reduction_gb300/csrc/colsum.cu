@@ -24,6 +24,7 @@
 // before its write has arrived is read again (bounded). Producers never wait,
 // so the folders' waits always end.
 #include "dgr_common.cuh"
+#include "dgr_diag.h"
 
 namespace dgr {
 namespace {
@@ -56,6 +57,11 @@ struct ColsumParams {
     int64_t col_stride;
     int32_t *counters;           // [n_groups]
     WsHeader *hdr;
+    // folder CTAs of this launch (the first blockIdx values): all of them when
+    // folders and producers share one launch, none in a producers-only launch
+    int32_t fold_ctas;
+    int32_t n_units;             // producer work units (tiles, or tile groups x column blocks)
+    Sched sched;                 // which producer takes which unit
 };
 
 template <int DT>
@@ -520,13 +526,21 @@ __device__ void fold(const ColsumParams &p, int f, float *sm) {
     }
 }
 
+// Folder blocks f of this launch's folder CTAs (a CTA takes several when the
+// launch has fewer folder CTAs than folder blocks).
+__device__ __forceinline__ void fold_all(const ColsumParams &p, float *sm) {
+    for (int f = blockIdx.x; f < p.n_fcb; f += p.fold_ctas) fold(p, f, sm);
+}
+
 template <int DT, int VE, int RPT>
 __global__ void __launch_bounds__(kThreads) colsum_kernel(const ColsumParams p) {
     extern __shared__ __align__(128) float smem[];
-    if (static_cast<int>(blockIdx.x) < p.n_fcb) {
-        fold(p, blockIdx.x, smem);
+    if (static_cast<int>(blockIdx.x) < p.fold_ctas) {
+        fold_all(p, smem);
     } else {
-        produce<DT, VE, RPT>(p, blockIdx.x - p.n_fcb, smem);
+        const int n_prod = static_cast<int>(gridDim.x) - p.fold_ctas;
+        for (int u = blockIdx.x - p.fold_ctas; u < p.n_units; u += n_prod)
+            produce<DT, VE, RPT>(p, static_cast<int>(sched_item(p.sched, static_cast<uint32_t>(u))), smem);
     }
 }
 
@@ -538,16 +552,17 @@ __global__ void __launch_bounds__(kThreads) colsum_kernel(const ColsumParams p) 
 template <int DT, int VE, int RPL>
 __global__ void __launch_bounds__(kWarpThreads, 1) colsum_warp_kernel(const ColsumParams p) {
     extern __shared__ __align__(128) float smem[];
-    if (static_cast<int>(blockIdx.x) < p.n_fcb) {
-        fold(p, blockIdx.x, smem);
+    if (static_cast<int>(blockIdx.x) < p.fold_ctas) {
+        fold_all(p, smem);
     } else {
         const int64_t wpc = kWarpThreads / 32;
-        const int64_t n_warps = static_cast<int64_t>(gridDim.x - p.n_fcb) * wpc;
+        const int64_t n_warps = static_cast<int64_t>(gridDim.x - p.fold_ctas) * wpc;
         int pending = -1;
-        for (int64_t w = static_cast<int64_t>(blockIdx.x - p.n_fcb) * wpc + (threadIdx.x >> 5); w < p.n_tiles;
+        for (int64_t w = static_cast<int64_t>(blockIdx.x - p.fold_ctas) * wpc + (threadIdx.x >> 5); w < p.n_tiles;
              w += n_warps) {
-            produce_warp_tile<DT, VE, RPL>(p, w, pending);
-            pending = static_cast<int>(w);
+            const int tile = static_cast<int>(sched_item(p.sched, static_cast<uint32_t>(w)));
+            produce_warp_tile<DT, VE, RPL>(p, tile, pending);
+            pending = tile;
         }
         if (pending >= 0) publish_tile(p, pending);
     }
@@ -563,15 +578,18 @@ constexpr int kSmallWarps = 4;
 template <int DT, int VE, int RPL>
 __global__ void __launch_bounds__(kSmallWarps * 32) colsum_small_kernel(const ColsumParams p) {
     const int lane = threadIdx.x & 31;
-    const int w = static_cast<int>(blockIdx.x) * kSmallWarps + (threadIdx.x >> 5);
-    if (w >= p.n_tiles) return;
-    produce_warp_tile<DT, VE, RPL, 16>(p, w, -1);
-    __threadfence();  // this lane's slot-row writes before the ticket
-    __syncwarp();
-    int t = 0;
-    if (lane == 0) t = atomicAdd(&p.hdr->pad[0], 1);
-    t = __shfl_sync(0xffffffffu, t, 0);
-    if (t != p.n_tiles - 1) return;
+    const int nw = static_cast<int>(gridDim.x) * kSmallWarps;
+    bool last = false;
+    // tiles in the schedule's order; with a capped grid a warp takes several
+    for (int w = static_cast<int>(blockIdx.x) * kSmallWarps + (threadIdx.x >> 5); w < p.n_tiles && !last; w += nw) {
+        produce_warp_tile<DT, VE, RPL, 16>(p, static_cast<int>(sched_item(p.sched, static_cast<uint32_t>(w))), -1);
+        __threadfence();  // this lane's slot-row writes before the ticket
+        __syncwarp();
+        int t = 0;
+        if (lane == 0) t = atomicAdd(&p.hdr->pad[0], 1);
+        last = __shfl_sync(0xffffffffu, t, 0) == p.n_tiles - 1;
+    }
+    if (!last) return;
     __threadfence();  // every other warp's slot rows are visible after its ticket
     const int n4 = (p.n_tiles + 3) / 4;  // 16-byte groups of 4 tiles per column (the stride is padded to 4)
     for (int c = lane; c < p.H; c += 32) {
@@ -600,65 +618,100 @@ __global__ void __launch_bounds__(kSmallWarps * 32) colsum_small_kernel(const Co
     if (lane == 0) p.hdr->pad[0] = 0;
 }
 
-template <int DT, int VE, int RPT>
-dgr_status launch_one(const ColsumParams &p, int grid, size_t smem, cudaStream_t st) {
-    colsum_kernel<DT, VE, RPT><<<grid, kThreads, smem, st>>>(p);
-    return launch_status();
-}
+using ColsumKernel = void (*)(const ColsumParams);
 
 template <int DT, int VE>
-dgr_status launch_rpt(const ColsumParams &p, int rpt, int grid, size_t smem, cudaStream_t st) {
+ColsumKernel cta_kernel(int rpt) {
     switch (rpt) {
-        case 1: return launch_one<DT, VE, 1>(p, grid, smem, st);
-        case 2: return launch_one<DT, VE, 2>(p, grid, smem, st);
-        case 4: return launch_one<DT, VE, 4>(p, grid, smem, st);
-        case 8: return launch_one<DT, VE, 8>(p, grid, smem, st);
-        case 16: return launch_one<DT, VE, 16>(p, grid, smem, st);
-        default: return DGR_ERR_INVALID_ARG;
-    }
-}
-
-template <int DT, int VE, int RPL>
-dgr_status launch_warp_one(const ColsumParams &p, int grid, cudaStream_t st) {
-    if (cudaFuncSetAttribute(colsum_warp_kernel<DT, VE, RPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kWarpSmemBytes) != cudaSuccess)
-        return DGR_ERR_CUDA;
-    colsum_warp_kernel<DT, VE, RPL><<<grid, kWarpThreads, kWarpSmemBytes, st>>>(p);
-    return launch_status();
-}
-
-template <int DT, int VE, int RPL>
-dgr_status launch_small_one(const ColsumParams &p, cudaStream_t st) {
-    colsum_small_kernel<DT, VE, RPL><<<(p.n_tiles + kSmallWarps - 1) / kSmallWarps, kSmallWarps * 32, 0, st>>>(p);
-    return launch_status();
-}
-
-template <int DT, int VE>
-dgr_status launch_small(const ColsumParams &p, int rpl, cudaStream_t st) {
-    switch (rpl) {
-        case 2: return launch_small_one<DT, VE, 2>(p, st);
-        case 4: return launch_small_one<DT, VE, 4>(p, st);
-        case 8: return launch_small_one<DT, VE, 8>(p, st);
-        case 16: return launch_small_one<DT, VE, 16>(p, st);
-        case 32: return launch_small_one<DT, VE, 32>(p, st);
-        case 64: return launch_small_one<DT, VE, 64>(p, st);
-        case 128: return launch_small_one<DT, VE, 128>(p, st);
-        default: return DGR_ERR_INVALID_ARG;
+        case 1: return colsum_kernel<DT, VE, 1>;
+        case 2: return colsum_kernel<DT, VE, 2>;
+        case 4: return colsum_kernel<DT, VE, 4>;
+        case 8: return colsum_kernel<DT, VE, 8>;
+        case 16: return colsum_kernel<DT, VE, 16>;
+        default: return nullptr;
     }
 }
 
 template <int DT, int VE>
-dgr_status launch_warp(const ColsumParams &p, int rpl, int grid, cudaStream_t st) {
+ColsumKernel warp_kernel(int rpl) {
     switch (rpl) {
-        case 2: return launch_warp_one<DT, VE, 2>(p, grid, st);
-        case 4: return launch_warp_one<DT, VE, 4>(p, grid, st);
-        case 8: return launch_warp_one<DT, VE, 8>(p, grid, st);
-        case 16: return launch_warp_one<DT, VE, 16>(p, grid, st);
-        case 32: return launch_warp_one<DT, VE, 32>(p, grid, st);
-        case 64: return launch_warp_one<DT, VE, 64>(p, grid, st);
-        case 128: return launch_warp_one<DT, VE, 128>(p, grid, st);
-        default: return DGR_ERR_INVALID_ARG;
+        case 2: return colsum_warp_kernel<DT, VE, 2>;
+        case 4: return colsum_warp_kernel<DT, VE, 4>;
+        case 8: return colsum_warp_kernel<DT, VE, 8>;
+        case 16: return colsum_warp_kernel<DT, VE, 16>;
+        case 32: return colsum_warp_kernel<DT, VE, 32>;
+        case 64: return colsum_warp_kernel<DT, VE, 64>;
+        case 128: return colsum_warp_kernel<DT, VE, 128>;
+        default: return nullptr;
     }
+}
+
+template <int DT, int VE>
+ColsumKernel small_kernel(int rpl) {
+    switch (rpl) {
+        case 2: return colsum_small_kernel<DT, VE, 2>;
+        case 4: return colsum_small_kernel<DT, VE, 4>;
+        case 8: return colsum_small_kernel<DT, VE, 8>;
+        case 16: return colsum_small_kernel<DT, VE, 16>;
+        case 32: return colsum_small_kernel<DT, VE, 32>;
+        case 64: return colsum_small_kernel<DT, VE, 64>;
+        case 128: return colsum_small_kernel<DT, VE, 128>;
+        default: return nullptr;
+    }
+}
+
+// How a call is launched.
+//   path 0: at most kSmallTiles warp-producer tiles: one launch, a ticket,
+//           the last warp folds (nothing waits);
+//   path 1: warp producers (persistent, one CTA per SM) and folder CTAs;
+//   path 2: CTA producers (one per unit) and folder CTAs.
+// On paths 1 and 2 the folders wait for the producers, so one launch holds
+// both only when every folder CTA and at least one producer CTA can be
+// resident at once; otherwise the producers run in a first launch and the
+// folders, which then find every tile written, in a second.
+struct ColsumPlan {
+    int32_t path, launches;
+    int64_t prod_ctas;  // producer CTAs (path 0: CTAs of kSmallWarps warps)
+    int32_t fold_ctas;  // folder CTAs (in the one launch, or in the second)
+};
+
+ColsumPlan colsum_plan(int32_t n_tiles, int32_t n_fcb, int64_t n_units, bool warp_producers, int32_t sms,
+                       int32_t cta_occupancy, int32_t cap) {
+    ColsumPlan pl{};
+    auto capped = [cap](int64_t g) { return (cap > 0 && g > cap) ? static_cast<int64_t>(cap) : g; };
+    if (warp_producers && n_tiles <= kSmallTiles) {
+        pl.path = 0;
+        pl.launches = 1;
+        pl.prod_ctas = capped((n_tiles + kSmallWarps - 1) / kSmallWarps);
+        return pl;
+    }
+    if (warp_producers) {
+        pl.path = 1;
+        const int64_t need = (n_tiles + kWarpThreads / 32 - 1) / (kWarpThreads / 32);
+        const int64_t resident = capped(sms);  // one CTA per SM
+        if (resident >= n_fcb + 1) {
+            pl.launches = 1;
+            pl.prod_ctas = need < resident - n_fcb ? need : resident - n_fcb;
+            pl.fold_ctas = n_fcb;
+        } else {
+            pl.launches = 2;
+            pl.prod_ctas = need < resident ? need : (resident > 0 ? resident : 1);
+            pl.fold_ctas = static_cast<int32_t>(n_fcb < resident ? n_fcb : (resident > 0 ? resident : 1));
+        }
+        return pl;
+    }
+    pl.path = 2;
+    const int64_t slots = static_cast<int64_t>(sms) * (cta_occupancy > 0 ? cta_occupancy : 1);
+    if (slots >= n_fcb + 1 && (cap == 0 || cap >= n_fcb + 1)) {
+        pl.launches = 1;
+        pl.fold_ctas = n_fcb;
+        pl.prod_ctas = cap > 0 && n_units > cap - n_fcb ? cap - n_fcb : n_units;
+    } else {
+        pl.launches = 2;
+        pl.prod_ctas = capped(n_units);
+        pl.fold_ctas = static_cast<int32_t>(capped(n_fcb));
+    }
+    return pl;
 }
 
 struct Layout {
@@ -725,6 +778,41 @@ dgr_status colsum_input_checks(const void *x, int32_t dtype, int64_t B, int64_t 
     return DGR_OK;
 }
 
+// Producer geometry: vector width VE (elements per 16-byte load, 1 for the
+// scalar path), column vectors V, the CTA producers' mapping (CB vectors and
+// RG row groups of rpt rows per tile, TPC tiles per CTA, n_pcb column blocks)
+// and, for power-of-two V, the warp producers' rows per lane rpl.
+void colsum_geometry(ColsumParams &p, int64_t H, int32_t tile_rows, int esize, bool vec_ok, int32_t n_tiles,
+                     int &VE, int &rpt, int &rpl) {
+    const int vec = 16 / esize;
+    VE = vec_ok ? vec : 1;
+    p.V = static_cast<int32_t>((H + VE - 1) / VE);
+    p.CB = p.V < 32 ? p.V : 32;
+    // each thread owns up to 16 rows; a tile takes RG * CB threads and a CTA
+    // packs TPC tiles (a power of two dividing the 32-tile counter group)
+    rpt = tile_rows < 16 ? tile_rows : 16;
+    if ((tile_rows / rpt) * p.CB > kThreads) p.CB = kThreads / (tile_rows / rpt);
+    p.RG = tile_rows / rpt;
+    p.n_pcb = (p.V + p.CB - 1) / p.CB;
+    int tpc = 1;
+    const int64_t units_min = 4LL * 152;  // keep enough CTAs to fill the GPU
+    while (tpc < 32 && 2 * tpc * p.RG * p.CB <= kThreads &&
+           (static_cast<int64_t>(n_tiles) + 2 * tpc - 1) / (2 * tpc) * p.n_pcb >= units_min)
+        tpc *= 2;
+    if (n_tiles <= 32) {  // tiny inputs: as few CTAs as the threads allow
+        while (tpc < 32 && 2 * tpc * p.RG * p.CB <= kThreads && tpc < n_tiles) tpc *= 2;
+    }
+    p.TPC = tpc;
+    // Warp producers when a power-of-two number of 16-byte column vectors
+    // (at most 32) tiles a warp and each lane gets 2 .. 128 rows.
+    p.stream_mode = 0;
+    rpl = 0;
+    if (vec_ok && p.V <= 32 && (p.V & (p.V - 1)) == 0) {
+        rpl = static_cast<int>(static_cast<int64_t>(tile_rows) * p.V / 32);
+        if (rpl >= 2 && rpl <= 128) p.stream_mode = 1;
+    }
+}
+
 // Enqueues the call on `stream` once every argument has been checked; ws holds
 // at least colsum_layout(B*S, H, tile_rows).total zeroed bytes.
 dgr_status colsum_enqueue(const void *x, int32_t dtype, int64_t B, int64_t S, int64_t H, int64_t stride_b,
@@ -752,33 +840,8 @@ dgr_status colsum_enqueue(const void *x, int32_t dtype, int64_t B, int64_t S, in
     const int vec = 16 / esize;
     const bool vec_ok = aligned(x, 16) && (H % vec) == 0 && (stride_s * esize) % 16 == 0 &&
                         (stride_b * esize) % 16 == 0;
-    const int VE = vec_ok ? vec : 1;
-    p.V = static_cast<int32_t>((H + VE - 1) / VE);
-    p.CB = p.V < 32 ? p.V : 32;
-    // each thread owns up to 16 rows; a tile takes RG * CB threads and a CTA
-    // packs TPC tiles (a power of two dividing the 32-tile counter group)
-    int rpt = tile_rows < 16 ? tile_rows : 16;
-    if ((tile_rows / rpt) * p.CB > kThreads) p.CB = kThreads / (tile_rows / rpt);
-    p.RG = tile_rows / rpt;
-    p.n_pcb = (p.V + p.CB - 1) / p.CB;
-    int tpc = 1;
-    const int64_t units_min = 4LL * 152;  // keep enough CTAs to fill the GPU
-    while (tpc < 32 && 2 * tpc * p.RG * p.CB <= kThreads &&
-           (static_cast<int64_t>(L.n_tiles) + 2 * tpc - 1) / (2 * tpc) * p.n_pcb >= units_min)
-        tpc *= 2;
-    if (L.n_tiles <= 32) {  // tiny inputs: as few CTAs as the threads allow
-        while (tpc < 32 && 2 * tpc * p.RG * p.CB <= kThreads && tpc < L.n_tiles) tpc *= 2;
-    }
-    p.TPC = tpc;
-    // Warp producers when a power-of-two number of 16-byte column vectors
-    // (at most 32) tiles a warp and each lane gets 2 .. 128 rows.
-    size_t smem_bytes = kFolderSmemBytes;
-    p.stream_mode = 0;
-    int rpl = 0;
-    if (vec_ok && p.V <= 32 && (p.V & (p.V - 1)) == 0) {
-        rpl = static_cast<int>(static_cast<int64_t>(tile_rows) * p.V / 32);
-        if (rpl >= 2 && rpl <= 128) p.stream_mode = 1;
-    }
+    int VE = 1, rpt = 1, rpl = 0;
+    colsum_geometry(p, H, tile_rows, esize, vec_ok, L.n_tiles, VE, rpt, rpl);
     p.FC = L.FC;
     p.n_fcb = L.n_fcb;
     p.batch = (kFolderSmemBytes / (2 * p.FC * 4)) & ~3;  // a multiple of 4: the chain reads 16-byte groups
@@ -792,35 +855,45 @@ dgr_status colsum_enqueue(const void *x, int32_t dtype, int64_t B, int64_t S, in
     // producer scratch: TPC * RG * CB * VE floats must fit the launch's shared memory
     if (static_cast<size_t>(p.TPC) * p.RG * p.CB * VE * 4 > static_cast<size_t>(kFolderSmemBytes))
         return DGR_ERR_UNSUPPORTED;
-    const int64_t n_groups_t = (L.n_tiles + p.TPC - 1) / p.TPC;
-    int64_t n_prod_ctas = n_groups_t * p.n_pcb;
-    if (p.stream_mode) {  // persistent: one producer CTA per SM not taken by a folder
-        int dev = 0, sms = 0;
-        cudaGetDevice(&dev);
-        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DGR_ERR_CUDA;
-        const int64_t need = (L.n_tiles + kWarpThreads / 32 - 1) / (kWarpThreads / 32);
-        int64_t avail = static_cast<int64_t>(sms) - p.n_fcb;
-        if (avail < 1) avail = 1;
-        n_prod_ctas = need < avail ? need : avail;
+    const bool warp_producers = p.stream_mode != 0;
+    if (warp_producers) p.n_pcb = 1;
+    const int64_t n_units = warp_producers ? L.n_tiles : (L.n_tiles + p.TPC - 1) / p.TPC * p.n_pcb;
+    if (n_units > INT32_MAX) return DGR_ERR_UNSUPPORTED;
+    p.n_units = static_cast<int32_t>(n_units);
+    p.sched = sched_for(static_cast<uint32_t>(n_units));
+    ColsumKernel k = nullptr;
+    if (warp_producers && L.n_tiles <= kSmallTiles)
+        k = dtype == DGR_DTYPE_BF16 ? small_kernel<DGR_DTYPE_BF16, 8>(rpl) : small_kernel<DGR_DTYPE_F32, 4>(rpl);
+    else if (warp_producers)
+        k = dtype == DGR_DTYPE_BF16 ? warp_kernel<DGR_DTYPE_BF16, 8>(rpl) : warp_kernel<DGR_DTYPE_F32, 4>(rpl);
+    else if (dtype == DGR_DTYPE_BF16)
+        k = VE == 8 ? cta_kernel<DGR_DTYPE_BF16, 8>(rpt) : cta_kernel<DGR_DTYPE_BF16, 1>(rpt);
+    else
+        k = VE == 4 ? cta_kernel<DGR_DTYPE_F32, 4>(rpt) : cta_kernel<DGR_DTYPE_F32, 1>(rpt);
+    if (!k) return DGR_ERR_INVALID_ARG;
+    int sms = 0, occ = 1;
+    dgr_status st = usable_sms(&sms);
+    if (st != DGR_OK) return st;
+    const bool small = warp_producers && L.n_tiles <= kSmallTiles;
+    const size_t smem = small ? 0 : (warp_producers ? kWarpSmemBytes : kFolderSmemBytes);
+    const unsigned threads = small ? kSmallWarps * 32 : (warp_producers ? kWarpThreads : kThreads);
+    if (warp_producers && !small &&
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kWarpSmemBytes) != cudaSuccess)
+        return DGR_ERR_CUDA;
+    if (!warp_producers && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kThreads, smem) != cudaSuccess)
+        return DGR_ERR_CUDA;
+    const ColsumPlan pl = colsum_plan(L.n_tiles, L.n_fcb, n_units, warp_producers, sms, occ, p.sched.cap);
+    if (pl.prod_ctas + pl.fold_ctas > INT32_MAX) return DGR_ERR_UNSUPPORTED;
+    if (pl.launches == 1) {
+        p.fold_ctas = small ? 0 : pl.fold_ctas;
+        k<<<static_cast<unsigned>(p.fold_ctas + pl.prod_ctas), threads, smem, s>>>(p);
+        return launch_status();
     }
-    const int64_t grid = static_cast<int64_t>(p.n_fcb) + n_prod_ctas;
-    if (grid > INT32_MAX) return DGR_ERR_UNSUPPORTED;
-    if (p.stream_mode && p.n_tiles <= kSmallTiles) {
-        p.n_pcb = 1;
-        if (dtype == DGR_DTYPE_BF16) return launch_small<DGR_DTYPE_BF16, 8>(p, rpl, s);
-        return launch_small<DGR_DTYPE_F32, 4>(p, rpl, s);
-    }
-    if (p.stream_mode) {
-        p.n_pcb = 1;
-        if (dtype == DGR_DTYPE_BF16) return launch_warp<DGR_DTYPE_BF16, 8>(p, rpl, static_cast<int>(grid), s);
-        return launch_warp<DGR_DTYPE_F32, 4>(p, rpl, static_cast<int>(grid), s);
-    }
-    if (dtype == DGR_DTYPE_BF16) {
-        return VE == 8 ? launch_rpt<DGR_DTYPE_BF16, 8>(p, rpt, static_cast<int>(grid), smem_bytes, s)
-                       : launch_rpt<DGR_DTYPE_BF16, 1>(p, rpt, static_cast<int>(grid), smem_bytes, s);
-    }
-    return VE == 4 ? launch_rpt<DGR_DTYPE_F32, 4>(p, rpt, static_cast<int>(grid), smem_bytes, s)
-                   : launch_rpt<DGR_DTYPE_F32, 1>(p, rpt, static_cast<int>(grid), smem_bytes, s);
+    p.fold_ctas = 0;  // producers only: every tile written and counted
+    k<<<static_cast<unsigned>(pl.prod_ctas), threads, smem, s>>>(p);
+    p.fold_ctas = pl.fold_ctas;  // then the folders, whose waits find every count complete
+    k<<<static_cast<unsigned>(pl.fold_ctas), threads, smem, s>>>(p);
+    return launch_status();
 }
 
 }  // namespace
@@ -844,6 +917,30 @@ extern "C" dgr_status dgr_ordered_colsum(const void *x, int32_t dtype, int64_t B
     if (T > 0 && ranges_overlap(out, H * 4, ws, L.total)) return DGR_ERR_ALIAS;
     if ((st = check_device()) != DGR_OK) return st;
     return colsum_enqueue(x, dtype, B, S, H, stride_b, stride_s, out, accumulate, tile_rows, ws, stream);
+}
+
+extern "C" dgr_status dgr_diag_colsum_plan(int64_t T, int64_t H, int32_t tile_rows, int32_t dtype, int32_t vec_ok,
+                                           int32_t sms, int32_t cta_occupancy, int32_t grid_cap, int32_t *plan) {
+    if (!plan || T < 0 || T > INT32_MAX || H < 1 || H > 4096 || !is_pow2(tile_rows) || tile_rows > 4096 ||
+        (dtype != DGR_DTYPE_BF16 && dtype != DGR_DTYPE_F32) || sms < 1 || cta_occupancy < 1 || grid_cap < 0)
+        return DGR_ERR_INVALID_ARG;
+    if (T == 0) {  // nothing is launched (out is written by a memset, or left)
+        plan[0] = -1;
+        plan[1] = plan[2] = plan[3] = 0;
+        return DGR_OK;
+    }
+    const Layout L = colsum_layout(T, H, tile_rows);
+    ColsumParams p{};
+    int VE = 1, rpt = 1, rpl = 0;
+    colsum_geometry(p, H, tile_rows, dtype == DGR_DTYPE_BF16 ? 2 : 4, vec_ok != 0, L.n_tiles, VE, rpt, rpl);
+    const bool warp_producers = p.stream_mode != 0;
+    const int64_t n_units = warp_producers ? L.n_tiles : (L.n_tiles + p.TPC - 1) / p.TPC * p.n_pcb;
+    const ColsumPlan pl = colsum_plan(L.n_tiles, L.n_fcb, n_units, warp_producers, sms, cta_occupancy, grid_cap);
+    plan[0] = pl.path;
+    plan[1] = pl.launches;
+    plan[2] = static_cast<int32_t>(pl.prod_ctas);
+    plan[3] = pl.fold_ctas;
+    return DGR_OK;
 }
 
 // ---------------------------------------------------------------------------

@@ -51,6 +51,51 @@ __device__ __forceinline__ bool wait_counter_geq(const int32_t *p, int32_t targe
     }
 }
 
+// Which CTA (or warp) takes which work item. The product path hands items out
+// in ascending order over as many CTAs as it needs; a test can ask, through
+// dgr_diag_set_schedule(), for descending or shuffled order and for a capped
+// grid, to show that no result depends on it. Item i of n is then
+//   ascending: i;  descending: n - 1 - i;  shuffled: (a * i + b) mod n,
+// with a coprime to n (a bijection of [0, n)).
+struct Sched {
+    int32_t order;  // 0 ascending, 1 descending, 2 shuffled
+    int32_t cap;    // > 0: launches take at most this many CTAs
+    uint32_t seed;
+    uint32_t n, a, b;
+};
+
+// The schedule over n items (a and b from the seed; the order falls back to
+// ascending for n <= 1). On the device for item counts only the GPU knows.
+__host__ __device__ inline Sched sched_over(Sched s, uint32_t n) {
+    s.n = n;
+    s.a = 1;
+    s.b = 0;
+    if (n <= 1) s.order = 0;
+    if (s.order == 2) {
+        uint32_t a = ((s.seed * 2654435761u) | 1u) % n;
+        if (a == 0) a = 1;
+        for (;;) {  // the next multiplier coprime to n (1 always is)
+            uint32_t x = a, y = n;
+            while (y) {
+                const uint32_t t = x % y;
+                x = y;
+                y = t;
+            }
+            if (x == 1) break;
+            a = a + 1 < n ? a + 1 : 1;
+        }
+        s.a = a;
+        s.b = (s.seed ^ 0x9e3779b9u) % n;
+    }
+    return s;
+}
+
+__device__ __forceinline__ uint32_t sched_item(const Sched &s, uint32_t i) {
+    if (s.order == 0) return i;
+    if (s.order == 1) return s.n - 1u - i;
+    return static_cast<uint32_t>((static_cast<uint64_t>(s.a) * i + s.b) % s.n);
+}
+
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t h) {
     return __uint_as_float(static_cast<uint32_t>(h) << 16);
 }
@@ -125,6 +170,21 @@ inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_
 
 // Checks the current device is compute capability 10.3.
 dgr_status check_device();
+
+// The process-wide diagnostic setting (ascending and uncapped unless a test
+// changed it), not yet bound to an item count.
+Sched sched_setting();
+
+// The schedule for a launch over n work items: sched_over(sched_setting(), n).
+Sched sched_for(uint32_t n);
+
+// grid, capped by the diagnostic setting.
+unsigned sched_grid(unsigned grid);
+
+// SMs that the kernels of the current context can hold at once: the device's,
+// or the SM partition of a green context, lowered to the diagnostic grid cap.
+// Persistent kernels whose CTAs wait on one another size their grids by it.
+dgr_status usable_sms(int *sms);
 
 // Device address, on the current device, of the column sum's static scratch
 // array (the no-alloc entry's scratch); looked up once per device.

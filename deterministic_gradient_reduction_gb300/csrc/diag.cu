@@ -22,10 +22,71 @@ __global__ void __launch_bounds__(32) wait_timeout_kernel(int which, uint64_t li
     }
 }
 
+// Controls for the replay tests: the order-varying reductions the pages
+// replace. Each CTA sums its own part in a fixed order and then adds it to
+// the output with a float atomicAdd, so the order in which the parts arrive,
+// and with it the rounding, follows the scheduling of the CTAs.
+constexpr int kAtomicRows = 128;
+
+// Column sum, x bf16 [T, H] row-major: one CTA per tile of 128 rows, thread h
+// of the CTA sums column h of its rows in order, then one atomicAdd per column.
+__global__ void __launch_bounds__(256) atomic_colsum_kernel(const uint16_t *x, int64_t T, int32_t H, float *out) {
+    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kAtomicRows;
+    const int64_t t1 = min(t0 + kAtomicRows, T);
+    for (int h = threadIdx.x; h < H; h += blockDim.x) {
+        float acc = 0.0f;
+        for (int64_t t = t0; t < t1; ++t) acc = __fadd_rn(acc, bf16_bits_to_f32(x[t * H + h]));
+        atomicAdd(out + h, acc);
+    }
+}
+
+// dprob, dY and Y bf16 [M, N] row-major: CTA (row block, N-tile of 128): a
+// warp per row sums its tile's products, lane by lane then by shuffles, and
+// adds the tile's partial to dprob[m] with one atomicAdd; the 32 tiles of a
+// row arrive from 32 CTAs in whatever order they run.
+__global__ void __launch_bounds__(256) atomic_rowdot_kernel(const uint16_t *dY, const uint16_t *Y, int64_t M,
+                                                           int32_t N, float *dprob) {
+    const int lane = threadIdx.x & 31;
+    const int64_t m = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (m >= M) return;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.y) * 128;
+    float v = 0.0f;
+    for (int64_t c = c0 + lane; c < min(c0 + 128, static_cast<int64_t>(N)); c += 32)
+        v = __fadd_rn(v, __fmul_rn(bf16_bits_to_f32(dY[m * N + c]), bf16_bits_to_f32(Y[m * N + c])));
+    for (int d = 16; d; d >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, d));
+    if (lane == 0) atomicAdd(dprob + m, v);
+}
+
 }  // namespace
 }  // namespace dgr
 
 using namespace dgr;
+
+extern "C" dgr_status dgr_diag_atomic_colsum(const uint16_t *x, int64_t T, int32_t H, float *out, void *stream) {
+    if (T < 0 || H < 1 || H > 4096 || !out || (T > 0 && !x) || T > (int64_t{1} << 40)) return DGR_ERR_INVALID_ARG;
+    dgr_status st = check_device();
+    if (st != DGR_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(out, 0, static_cast<size_t>(H) * 4, s) != cudaSuccess) return DGR_ERR_CUDA;
+    if (T == 0) return DGR_OK;
+    const int64_t grid = (T + kAtomicRows - 1) / kAtomicRows;
+    if (grid > INT32_MAX) return DGR_ERR_UNSUPPORTED;
+    atomic_colsum_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(x, T, H, out);
+    return launch_status();
+}
+
+extern "C" dgr_status dgr_diag_atomic_rowdot(const uint16_t *dY, const uint16_t *Y, int64_t M, int32_t N,
+                                             float *dprob, void *stream) {
+    if (M < 0 || N < 1 || N > 65536 || !dprob || (M > 0 && (!dY || !Y)) || M > INT32_MAX) return DGR_ERR_INVALID_ARG;
+    dgr_status st = check_device();
+    if (st != DGR_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(dprob, 0, static_cast<size_t>(M) * 4, s) != cudaSuccess) return DGR_ERR_CUDA;
+    if (M == 0) return DGR_OK;
+    const dim3 grid(static_cast<unsigned>((M + 7) / 8), static_cast<unsigned>((N + 127) / 128));
+    atomic_rowdot_kernel<<<grid, 256, 0, s>>>(dY, Y, M, N, dprob);
+    return launch_status();
+}
 
 extern "C" dgr_status dgr_diag_wait_timeout(int32_t which, int32_t limit_us, void *ws, size_t ws_bytes,
                                             void *stream) {

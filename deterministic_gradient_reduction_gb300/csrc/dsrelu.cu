@@ -82,6 +82,7 @@ struct DsParams {
     float *dprob;         // [T]
     int32_t accumulate;
     WsHeader *hdr;
+    Sched sched;          // the setting; bound to the tile count on the device
 };
 
 
@@ -151,6 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return;
     }
     const int64_t n_tiles = static_cast<int64_t>(mb_base[p.E]) * p.nbs;
+    const Sched sched = sched_over(p.sched, static_cast<uint32_t>(n_tiles));  // the tile count is known here only
     const int n_k = p.K / BK;
 
     if (threadIdx.x == 0) {
@@ -187,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int64_t tau = blockIdx.x; ok && tau < n_tiles; tau += gridDim.x) {
                 int e, mb, nb;
-                tile_of(p, mb_base, tau, e, mb, nb);
+                tile_of(p, mb_base, sched_item(sched, static_cast<uint32_t>(tau)), e, mb, nb);
                 const int32_t row0 = static_cast<int32_t>(p.offs[e]) + mb * BM;
                 for (int kb = 0; kb < n_k; ++kb) {
                     if (!mbar_wait(&ctl->empty[stage], phase ^ 1, abort_flag, p.hdr, 31)) {
@@ -277,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int64_t tau = blockIdx.x; ok && tau < n_tiles; tau += gridDim.x, ++g) {
             int e, mb, nb;
-            tile_of(p, mb_base, tau, e, mb, nb);
+            tile_of(p, mb_base, sched_item(sched, static_cast<uint32_t>(tau)), e, mb, nb);
             const int64_t row = p.offs[e] + static_cast<int64_t>(mb) * BM + 32 * q + lane;
             const bool mine = row < p.offs[e + 1];  // past the expert's end: not this expert's row
             // the row's 128 dY values, in flight while the accumulator fills
@@ -442,7 +444,8 @@ extern "C" dgr_status dgr_dsrelu_dprob(const void *A, const void *B, const int64
             cudaSuccess)
         return DGR_ERR_CUDA;
     const int64_t tiles_max = ((T + BM - 1) / BM + E) * (N / BN);
-    const int grid = static_cast<int>(tiles_max < sms ? tiles_max : sms);
+    p.sched = sched_setting();
+    const unsigned grid = sched_grid(static_cast<unsigned>(tiles_max < sms ? tiles_max : sms));
     dsrelu_gemm<<<grid, kThreads, kSmemBytes, s>>>(mA, mB, p);
     if (cudaGetLastError() != cudaSuccess) return DGR_ERR_CUDA;
     dsrelu_fold<<<static_cast<unsigned>((T + 255) / 256), 256, 0, s>>>(p);

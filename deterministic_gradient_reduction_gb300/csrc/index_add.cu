@@ -68,25 +68,31 @@ struct IdxParams {
     int32_t *incl;               // [2][nb][256] published inclusive counts (bit 31: published)
     int32_t *heavy_rows;         // split rows longer than kWarpFoldTiles tiles (fold-block work)
     int32_t max_fold_rows;       // capacity of heavy_rows
+    Sched sched_tiles;           // which block takes which sort tile (hist, pass 0)
+    Sched sched_pass1;           // the same over pass 1's items (sort tiles and key buckets)
+    Sched sched_warps;           // segsum: the setting, bound on the device to its warp count
     float *slots;
     WsHeader *hdr;  // pad[2]: bad-index total, pad[3]: fold-row count, pad[8..10]: layout tag
 };
 
 // Layout tag (header words 8-10): N, R + 1 and a constant, all non-zero,
-// written by the first call on a zeroed workspace. The regions of the
-// workspace move with N and R, and the arrays one call leaves behind (keys,
-// permutation) would be read as counters by a call of other sizes, so every
-// call checks the tag before it writes anything. hist accepts words that are
-// still zero (a fresh workspace whose tag block 0 is writing); the later
-// launches, which start after hist has completed, want the exact tag.
+// written by hist's block 0 on the first call on a zeroed workspace. The
+// regions of the workspace move with N and R, and the arrays one call leaves
+// behind (keys, permutation) would be read as counters by a call of other
+// sizes, so every launch of a call checks the tag before it writes anything.
+// A word is accepted when it is still zero (a fresh workspace whose tag hist
+// is writing) or holds this call's value; any other value is a workspace of
+// other sizes, which nobody rewrites, so every launch can read the tag early,
+// before its dependency wait, and all of them reach the same answer.
 constexpr int32_t kTagMagic = 0x31584449;
 constexpr int kTagWord = 8;
 
 __device__ __forceinline__ bool tag_word_ok(int32_t have, int32_t want) { return have == 0 || have == want; }
 
-__device__ __forceinline__ bool tag_exact(const IdxParams &p) {
+__device__ __forceinline__ bool tag_ok(const IdxParams &p) {
     const volatile int32_t *t = p.hdr->pad + kTagWord;
-    return t[0] == p.N && t[1] == p.R + 1 && t[2] == kTagMagic;
+    const int32_t t0 = t[0], t1 = t[1], t2 = t[2];
+    return tag_word_ok(t0, p.N) && tag_word_ok(t1, p.R + 1) && tag_word_ok(t2, kTagMagic);
 }
 
 __device__ __forceinline__ int32_t clampi(int32_t v, int32_t lo, int32_t hi) { return min(max(v, lo), hi); }
@@ -115,26 +121,23 @@ __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.w
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kSortThreads) hist_kernel(const IdxParams p) {
     __shared__ int32_t h[2][kDigits];
-    __shared__ int32_t bad_block, pad_block, tag_ok;
+    __shared__ int32_t bad_block, pad_block, tag_good;
     const int tid = threadIdx.x;
     launch_dependents();
-    h[0][tid] = 0;
-    h[1][tid] = 0;
+    // sort tiles in the schedule's order; with a capped grid a block takes several
+    int32_t it = blockIdx.x;
+    int32_t tile = static_cast<int32_t>(sched_item(p.sched_tiles, static_cast<uint32_t>(it)));
     int32_t v[kSortItems];
 #pragma unroll
     for (int r = 0; r < kSortItems; ++r) {
-        const int64_t e = static_cast<int64_t>(blockIdx.x) * kSortTile + r * kSortThreads + tid;
+        const int64_t e = static_cast<int64_t>(tile) * kSortTile + r * kSortThreads + tid;
         v[r] = 0;
         ldg_nc_b32_if(v[r], p.idx + e, e < p.N);
     }
     if (tid == 0) {
-        bad_block = 0;
-        pad_block = 0;
-        const volatile int32_t *t = p.hdr->pad + kTagWord;
-        const int32_t t0 = t[0], t1 = t[1], t2 = t[2];
-        tag_ok = tag_word_ok(t0, p.N) && tag_word_ok(t1, p.R + 1) && tag_word_ok(t2, kTagMagic);
+        tag_good = tag_ok(p);
         if (blockIdx.x == 0) {
-            if (tag_ok) {
+            if (tag_good) {
                 p.hdr->pad[3] = 0;  // fold-row list of this call starts empty
                 p.hdr->pad[kTagWord] = p.N;
                 p.hdr->pad[kTagWord + 1] = p.R + 1;
@@ -144,28 +147,46 @@ __global__ void __launch_bounds__(kSortThreads) hist_kernel(const IdxParams p) {
             }
         }
     }
-    __syncthreads();
-    if (!tag_ok) return;  // a workspace laid out for other sizes: nothing is written
-    int my_bad = 0;
+    for (;;) {
+        h[0][tid] = 0;
+        h[1][tid] = 0;
+        if (tid == 0) {
+            bad_block = 0;
+            pad_block = 0;
+        }
+        __syncthreads();
+        if (!tag_good) return;  // a workspace laid out for other sizes: nothing is written
+        int my_bad = 0;
 #pragma unroll
-    for (int r = 0; r < kSortItems; ++r) {
-        const int64_t e = static_cast<int64_t>(blockIdx.x) * kSortTile + r * kSortThreads + tid;
-        if (e >= p.N) continue;
-        bool bad = false;
-        const int32_t k = map_key(v[r], p.R, bad);
-        my_bad += bad ? 1 : 0;
-        atomicAdd(&h[0][k & 255], 1);
-        atomicAdd(&h[1][k >> 8], 1);
-        if (k == p.R) atomicAdd(&pad_block, 1);
-        else atomicAdd(&p.count[k], 1);
+        for (int r = 0; r < kSortItems; ++r) {
+            const int64_t e = static_cast<int64_t>(tile) * kSortTile + r * kSortThreads + tid;
+            if (e >= p.N) continue;
+            bool bad = false;
+            const int32_t k = map_key(v[r], p.R, bad);
+            my_bad += bad ? 1 : 0;
+            atomicAdd(&h[0][k & 255], 1);
+            atomicAdd(&h[1][k >> 8], 1);
+            if (k == p.R) atomicAdd(&pad_block, 1);
+            else atomicAdd(&p.count[k], 1);
+        }
+        if (my_bad) atomicAdd(&bad_block, my_bad);
+        __syncthreads();
+        if (tid == 0 && pad_block) atomicAdd(&p.count[p.R], pad_block);
+        p.cnt[static_cast<int64_t>(tile) * kDigits + tid] = h[0][tid];
+        if (h[0][tid]) atomicAdd(&p.hist[tid], h[0][tid]);
+        if (h[1][tid]) atomicAdd(&p.hist[kDigits + tid], h[1][tid]);
+        if (tid == 0 && bad_block) atomicAdd(&p.hdr->pad[2], bad_block);
+        it += gridDim.x;
+        if (it >= p.nb) return;
+        tile = static_cast<int32_t>(sched_item(p.sched_tiles, static_cast<uint32_t>(it)));
+        __syncthreads();  // the block's counts of the last tile are read: reuse the arrays
+#pragma unroll
+        for (int r = 0; r < kSortItems; ++r) {
+            const int64_t e = static_cast<int64_t>(tile) * kSortTile + r * kSortThreads + tid;
+            v[r] = 0;
+            ldg_nc_b32_if(v[r], p.idx + e, e < p.N);
+        }
     }
-    if (my_bad) atomicAdd(&bad_block, my_bad);
-    __syncthreads();
-    if (tid == 0 && pad_block) atomicAdd(&p.count[p.R], pad_block);
-    p.cnt[static_cast<int64_t>(blockIdx.x) * kDigits + tid] = h[0][tid];
-    if (h[0][tid]) atomicAdd(&p.hist[tid], h[0][tid]);
-    if (h[1][tid]) atomicAdd(&p.hist[kDigits + tid], h[1][tid]);
-    if (tid == 0 && bad_block) atomicAdd(&p.hdr->pad[2], bad_block);
 }
 
 // Stable in-warp ranking: warp w owns its elements in rounds of 32
@@ -292,179 +313,192 @@ __global__ void __launch_bounds__(kPassThreads) pass_kernel(const IdxParams p) {
     __shared__ int32_t csum[kSortWarps];
     __shared__ int32_t sk[kSortTile], sv[kSortTile];
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-    const int32_t b = blockIdx.x;
     const int64_t tiles = static_cast<int64_t>(p.nb) * kDigits;
     const int32_t *cnt_g = p.cnt + PASS * tiles;
     int32_t *incl_g = p.incl + PASS * tiles;
-    // pass 1's first n_buckets tiles also own the segment starts of bucket b
-    const bool seg_owner = PASS == 1 && b < p.n_buckets;
-    const bool sort_tile = b < p.nb;  // pass 1 may have more blocks than tiles (more buckets)
+    // items: sort tiles, and in pass 1 also key buckets where there are more
+    // buckets than tiles; handed out in the schedule's order (with a capped
+    // grid a block takes several). No item waits for another.
+    const int32_t n_items = PASS == 0 ? p.nb : max(p.nb, p.n_buckets);
+    const Sched &sc = PASS == 0 ? p.sched_tiles : p.sched_pass1;
     for (int q = tid; q < kSortWarps * kDigits; q += kPassThreads) (&cnt[0][0])[q] = 0;
     launch_dependents();
+    const bool good = tag_ok(p);  // read while the previous launch finishes
     grid_dep_wait();
-    if (!tag_exact(p)) return;  // hist refused the workspace (the same answer in every thread)
+    if (!good) return;  // hist refused the workspace (the same answer in every thread)
     __syncthreads();
-    int32_t key[kSortItems], val[kSortItems], rank[kSortItems];
-    int32_t gx = 0, my_count = 0;
-    int32_t kc = 0, kx = 0;  // prefix warps of a segment-start owner: the key's count, warp prefix
-    if (w < kSortWarps) {
-        // ranking warps: warp w owns elements [b*2048 + w*256, +256) in 8 rounds of 32
-        const int64_t e0 = static_cast<int64_t>(b) * kSortTile + w * (kSortItems * 32) + lane;
+    for (int32_t it = blockIdx.x; it < n_items; it += gridDim.x) {
+        const int32_t b = static_cast<int32_t>(sched_item(sc, static_cast<uint32_t>(it)));
+        // pass 1's first n_buckets items also own the segment starts of bucket b
+        const bool seg_owner = PASS == 1 && b < p.n_buckets;
+        const bool sort_tile = b < p.nb;  // pass 1 may have more items than tiles (more buckets)
+        if (it != static_cast<int32_t>(blockIdx.x)) {
+            for (int q = tid; q < kSortWarps * kDigits; q += kPassThreads) (&cnt[0][0])[q] = 0;
+            __syncthreads();
+        }
+        int32_t key[kSortItems], val[kSortItems], rank[kSortItems];
+        int32_t gx = 0, my_count = 0;
+        int32_t kc = 0, kx = 0;  // prefix warps of a segment-start owner: the key's count, warp prefix
+        if (w < kSortWarps) {
+            // ranking warps: warp w owns elements [b*2048 + w*256, +256) in 8 rounds of 32
+            const int64_t e0 = static_cast<int64_t>(b) * kSortTile + w * (kSortItems * 32) + lane;
 #pragma unroll
-        for (int r = 0; r < kSortItems; ++r) {
-            const int64_t e = e0 + r * 32;
-            key[r] = 0;
-            val[r] = static_cast<int32_t>(e);
-            if (PASS == 0) {
-                ldg_nc_b32_if(key[r], p.idx + e, e < p.N);
-            } else {
-                ldg_nc_b32_if(key[r], p.keys_a + e, e < p.N);
-                ldg_nc_b32_if(val[r], p.vals_a + e, e < p.N);
+            for (int r = 0; r < kSortItems; ++r) {
+                const int64_t e = e0 + r * 32;
+                key[r] = 0;
+                val[r] = static_cast<int32_t>(e);
+                if (PASS == 0) {
+                    ldg_nc_b32_if(key[r], p.idx + e, e < p.N);
+                } else {
+                    ldg_nc_b32_if(key[r], p.keys_a + e, e < p.N);
+                    ldg_nc_b32_if(val[r], p.vals_a + e, e < p.N);
+                }
             }
-        }
-        const int32_t hc = __ldcg(&p.hist[PASS * kDigits + tid]);
-        if (sort_tile) my_count = __ldcg(&cnt_g[static_cast<int64_t>(b) * kDigits + tid]);
+            const int32_t hc = __ldcg(&p.hist[PASS * kDigits + tid]);
+            if (sort_tile) my_count = __ldcg(&cnt_g[static_cast<int64_t>(b) * kDigits + tid]);
 #pragma unroll
-        for (int r = 0; r < kSortItems; ++r) {
-            const int64_t e = e0 + r * 32;
-            if (e >= p.N) {
-                key[r] = -1;
-            } else if (PASS == 0) {
-                bool bad = false;
-                key[r] = map_key(key[r], p.R, bad);
-            } else {
-                key[r] = clampi(key[r], 0, p.R);  // a key read back from the workspace stays a key
+            for (int r = 0; r < kSortItems; ++r) {
+                const int64_t e = e0 + r * 32;
+                if (e >= p.N) {
+                    key[r] = -1;
+                } else if (PASS == 0) {
+                    bool bad = false;
+                    key[r] = map_key(key[r], p.R, bad);
+                } else {
+                    key[r] = clampi(key[r], 0, p.R);  // a key read back from the workspace stays a key
+                }
             }
-        }
 #pragma unroll
-        for (int r = 0; r < kSortItems; ++r)
-            warp_rank(key[r] >= 0 ? pass_digit<PASS>(key[r]) : 0, key[r] >= 0, cnt, w, rank[r]);
-        // exclusive scans over digits of the global histogram (global digit
-        // bases) and of this tile's counts (local digit bases)
-        int32_t gi = hc, li = my_count;
-#pragma unroll
-        for (int s = 1; s < 32; s <<= 1) {
-            const int32_t tg = __shfl_up_sync(0xffffffffu, gi, s);
-            const int32_t tl = __shfl_up_sync(0xffffffffu, li, s);
-            if (lane >= s) {
-                gi += tg;
-                li += tl;
-            }
-        }
-        if (lane == 31) {
-            wsum[w] = gi;
-            lsum[w] = li;
-        }
-        gx = gi - hc;
-        lbase[tid] = li - my_count;
-    } else {
-        if (seg_owner) {  // the counts of keys 256b .. 256b + 255, scanned within each warp
-            const int32_t k = b * kDigits + (tid - kSortThreads);
-            if (k <= p.R) kc = __ldcg(&p.count[k]);
-            int32_t ci = kc;
+            for (int r = 0; r < kSortItems; ++r)
+                warp_rank(key[r] >= 0 ? pass_digit<PASS>(key[r]) : 0, key[r] >= 0, cnt, w, rank[r]);
+            // exclusive scans over digits of the global histogram (global digit
+            // bases) and of this tile's counts (local digit bases)
+            int32_t gi = hc, li = my_count;
 #pragma unroll
             for (int s = 1; s < 32; s <<= 1) {
-                const int32_t tv = __shfl_up_sync(0xffffffffu, ci, s);
-                if (lane >= s) ci += tv;
+                const int32_t tg = __shfl_up_sync(0xffffffffu, gi, s);
+                const int32_t tl = __shfl_up_sync(0xffffffffu, li, s);
+                if (lane >= s) {
+                    gi += tg;
+                    li += tl;
+                }
             }
-            if (lane == 31) csum[w - kSortWarps] = ci;
-            kx = ci - kc;
-        }
-        if (sort_tile && b < kDirectTiles) direct_prefix(cnt_g, b, w - kSortWarps, lane, red);
-    }
-    __syncthreads();
-    if (w < kSortWarps) {
-        int32_t lx = lbase[tid];
-        for (int ww = 0; ww < w; ++ww) {
-            gx += wsum[ww];
-            lx += lsum[ww];
-        }
-        lbase[tid] = lx;
-        dbase_s[tid] = gx;
-        int32_t run = 0;
-#pragma unroll
-        for (int ww = 0; ww < kSortWarps; ++ww) {
-            const int32_t c = cnt[ww][tid];
-            cnt[ww][tid] = run;
-            run += c;
-        }
-    } else {
-        const int d = tid - kSortThreads;
-        const int32_t mine = sort_tile ? __ldcg(&cnt_g[static_cast<int64_t>(b) * kDigits + d]) : 0;
-        int32_t excl = 0;
-        if (!sort_tile) {
-        } else if (b < kDirectTiles) {
-#pragma unroll
-            for (int v = 0; v < kSortWarps; ++v) excl += red[v][d];
-            asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(incl_g + static_cast<int64_t>(b) * kDigits + d),
-                         "r"(kPublished | (excl + mine))
-                         : "memory");
-        } else {
-            LookWin L;
-            look_load(L, cnt_g, incl_g, b - 1, d);
-            excl = look_finish(L, cnt_g, incl_g, b, d, mine);
-        }
-        excl_s[d] = excl;
-        if (seg_owner)
-            for (int ww = 0; ww < w - kSortWarps; ++ww) kx += csum[ww];
-    }
-    __syncthreads();
-    if (w < kSortWarps) {
-        gbase[tid] = gx + excl_s[tid];
-        // the tile in digit order in shared memory
-#pragma unroll
-        for (int r = 0; r < kSortItems; ++r) {
-            if (key[r] < 0) continue;
-            const int d = pass_digit<PASS>(key[r]);
-            // the local bases come from counts in the workspace: keep the
-            // position inside the tile whatever they hold
-            const int32_t lp = clampi(lbase[d] + cnt[w][d] + rank[r], 0, kSortTile - 1);
-            sk[lp] = key[r];
-            sv[lp] = val[r];
-        }
-    } else if (seg_owner) {
-        // segment starts of bucket b: the bucket's first position plus the
-        // counts of its smaller keys; its long rows go on the fold-block list
-        // (in any order: each row is folded by one block, the same way)
-        const int32_t k = b * kDigits + (tid - kSortThreads);
-        if (k <= p.R) {
-            p.seg_start[k] = clampi(dbase_s[b] + kx, 0, p.N);
-            if (k == p.R) p.seg_start[p.R + 1] = p.N;
-            if (p.seg_tile == kSegTile && kc > kWarpFoldTiles * kSegTile) {
-                const int32_t at = atomicAdd(&p.hdr->pad[3], 1);
-                if (at < p.max_fold_rows) p.heavy_rows[at] = k;
+            if (lane == 31) {
+                wsum[w] = gi;
+                lsum[w] = li;
             }
-            p.count[k] = 0;  // read no more: cleared for the next call
-        }
-        if (b == 0 && tid == kSortThreads) {  // every hist block has counted by now
-            const int32_t bad = atomicAdd(&p.hdr->pad[2], 0);
-            if (p.bad_count) *p.bad_count = bad;
-            p.hdr->pad[2] = 0;
-        }
-    }
-    __syncthreads();
-    // each digit's run written out contiguously
-    const int n_here = static_cast<int>(
-        min(static_cast<int64_t>(kSortTile), static_cast<int64_t>(p.N) - static_cast<int64_t>(b) * kSortTile));
-#pragma unroll
-    for (int r = 0; r < kSortTile / kPassThreads; ++r) {
-        const int i = r * kPassThreads + tid;
-        if (i >= n_here) continue;
-        const int32_t k = clampi(sk[i], 0, p.R);
-        const int d = pass_digit<PASS>(k);
-        // digit bases come from counts in the workspace: the write stays in [0, N)
-        const int32_t pos = clampi(gbase[d] + (i - lbase[d]), 0, p.N - 1);
-        if (PASS == 0) {
-            p.keys_a[pos] = k;
-            p.vals_a[pos] = sv[i];
-            atomicAdd(&p.cnt[tiles + static_cast<int64_t>(pos / kSortTile) * kDigits + (k >> 8)], 1);
+            gx = gi - hc;
+            lbase[tid] = li - my_count;
         } else {
-            p.perm[pos] = sv[i];
-            p.skey[pos] = k;
+            if (seg_owner) {  // the counts of keys 256b .. 256b + 255, scanned within each warp
+                const int32_t k = b * kDigits + (tid - kSortThreads);
+                if (k <= p.R) kc = __ldcg(&p.count[k]);
+                int32_t ci = kc;
+#pragma unroll
+                for (int s = 1; s < 32; s <<= 1) {
+                    const int32_t tv = __shfl_up_sync(0xffffffffu, ci, s);
+                    if (lane >= s) ci += tv;
+                }
+                if (lane == 31) csum[w - kSortWarps] = ci;
+                kx = ci - kc;
+            }
+            if (sort_tile && b < kDirectTiles) direct_prefix(cnt_g, b, w - kSortWarps, lane, red);
         }
+        __syncthreads();
+        if (w < kSortWarps) {
+            int32_t lx = lbase[tid];
+            for (int ww = 0; ww < w; ++ww) {
+                gx += wsum[ww];
+                lx += lsum[ww];
+            }
+            lbase[tid] = lx;
+            dbase_s[tid] = gx;
+            int32_t run = 0;
+#pragma unroll
+            for (int ww = 0; ww < kSortWarps; ++ww) {
+                const int32_t c = cnt[ww][tid];
+                cnt[ww][tid] = run;
+                run += c;
+            }
+        } else {
+            const int d = tid - kSortThreads;
+            const int32_t mine = sort_tile ? __ldcg(&cnt_g[static_cast<int64_t>(b) * kDigits + d]) : 0;
+            int32_t excl = 0;
+            if (!sort_tile) {
+            } else if (b < kDirectTiles) {
+#pragma unroll
+                for (int v = 0; v < kSortWarps; ++v) excl += red[v][d];
+                asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(incl_g + static_cast<int64_t>(b) * kDigits + d),
+                             "r"(kPublished | (excl + mine))
+                             : "memory");
+            } else {
+                LookWin L;
+                look_load(L, cnt_g, incl_g, b - 1, d);
+                excl = look_finish(L, cnt_g, incl_g, b, d, mine);
+            }
+            excl_s[d] = excl;
+            if (seg_owner)
+                for (int ww = 0; ww < w - kSortWarps; ++ww) kx += csum[ww];
+        }
+        __syncthreads();
+        if (w < kSortWarps) {
+            gbase[tid] = gx + excl_s[tid];
+            // the tile in digit order in shared memory
+#pragma unroll
+            for (int r = 0; r < kSortItems; ++r) {
+                if (key[r] < 0) continue;
+                const int d = pass_digit<PASS>(key[r]);
+                // the local bases come from counts in the workspace: keep the
+                // position inside the tile whatever they hold
+                const int32_t lp = clampi(lbase[d] + cnt[w][d] + rank[r], 0, kSortTile - 1);
+                sk[lp] = key[r];
+                sv[lp] = val[r];
+            }
+        } else if (seg_owner) {
+            // segment starts of bucket b: the bucket's first position plus the
+            // counts of its smaller keys; its long rows go on the fold-block list
+            // (in any order: each row is folded by one block, the same way)
+            const int32_t k = b * kDigits + (tid - kSortThreads);
+            if (k <= p.R) {
+                p.seg_start[k] = clampi(dbase_s[b] + kx, 0, p.N);
+                if (k == p.R) p.seg_start[p.R + 1] = p.N;
+                if (p.seg_tile == kSegTile && kc > kWarpFoldTiles * kSegTile) {
+                    const int32_t at = atomicAdd(&p.hdr->pad[3], 1);
+                    if (at < p.max_fold_rows) p.heavy_rows[at] = k;
+                }
+                p.count[k] = 0;  // read no more: cleared for the next call
+            }
+            if (b == 0 && tid == kSortThreads) {  // every hist block has counted by now
+                const int32_t bad = atomicAdd(&p.hdr->pad[2], 0);
+                if (p.bad_count) *p.bad_count = bad;
+                p.hdr->pad[2] = 0;
+            }
+        }
+        __syncthreads();
+        // each digit's run written out contiguously
+        const int n_here = static_cast<int>(
+            min(static_cast<int64_t>(kSortTile), static_cast<int64_t>(p.N) - static_cast<int64_t>(b) * kSortTile));
+#pragma unroll
+        for (int r = 0; r < kSortTile / kPassThreads; ++r) {
+            const int i = r * kPassThreads + tid;
+            if (i >= n_here) continue;
+            const int32_t k = clampi(sk[i], 0, p.R);
+            const int d = pass_digit<PASS>(k);
+            // digit bases come from counts in the workspace: the write stays in [0, N)
+            const int32_t pos = clampi(gbase[d] + (i - lbase[d]), 0, p.N - 1);
+            if (PASS == 0) {
+                p.keys_a[pos] = k;
+                p.vals_a[pos] = sv[i];
+                atomicAdd(&p.cnt[tiles + static_cast<int64_t>(pos / kSortTile) * kDigits + (k >> 8)], 1);
+            } else {
+                p.perm[pos] = sv[i];
+                p.skey[pos] = k;
+            }
+        }
+        // pass 0's inclusive words are read no more: clear them for the next call
+        if (PASS == 1 && sort_tile && tid < kDigits) p.incl[static_cast<int64_t>(b) * kDigits + tid] = 0;
+        __syncthreads();  // the item's shared arrays are read: the next item may reuse them
     }
-    // pass 0's inclusive words are read no more: clear them for the next call
-    if (PASS == 1 && sort_tile && tid < kDigits) p.incl[static_cast<int64_t>(b) * kDigits + tid] = 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -516,15 +550,17 @@ __device__ void warp_fold(const IdxParams &p, int32_t k, int64_t s0, int32_t n_t
 // and the row counts it (an integer ticket). The last of the row's
 // tiles x column blocks to arrive folds a row of at most kWarpFoldTiles tiles;
 // a longer row is folded by a fold block.
+// (long_by_warp: no fold block runs - a one-block grid - so the last tile
+// folds a longer row too.)
 __device__ __noinline__ void tile_done(const IdxParams &p, int32_t k, int32_t p0, bool tfirst, float4 P, int col,
-                                       bool act, int lane) {
+                                       bool act, int lane, bool long_by_warp) {
     if (act) *tile_slot(p, p0, tfirst, col) = P;
     __threadfence();
     __syncwarp();
     int32_t s0 = 0, e0 = 0, tk = 0;
     if (lane == 0) {
-        s0 = p.seg_start[k];
-        e0 = p.seg_start[k + 1];
+        s0 = clampi(p.seg_start[k], 0, p.N);
+        e0 = clampi(p.seg_start[k + 1], s0, p.N);
         tk = atomicAdd(&p.tickets[k], 1);
     }
     s0 = __shfl_sync(0xffffffffu, s0, 0);
@@ -532,7 +568,7 @@ __device__ __noinline__ void tile_done(const IdxParams &p, int32_t k, int32_t p0
     tk = __shfl_sync(0xffffffffu, tk, 0);
     const int32_t n_tiles = (e0 - s0 + kSegTile - 1) / kSegTile;
     const int32_t n_cb = (p.D + 127) / 128;
-    if (n_tiles > kWarpFoldTiles || tk != n_tiles * n_cb - 1) return;
+    if ((n_tiles > kWarpFoldTiles && !long_by_warp) || tk != n_tiles * n_cb - 1) return;
     __threadfence();
     warp_fold(p, k, s0, n_tiles, lane);
     if (lane == 0) p.tickets[k] = 0;
@@ -779,7 +815,8 @@ struct RowAcc {
 // partials into F in order and its last group writes out[key] + F; a split
 // row's tile partial goes to the tile's slot.
 __device__ __forceinline__ void consume_group(const IdxParams &p, const float4 *slot, const int32_t *dslot, RowAcc &ra,
-                                              GStack &S, int gs, int gpt, int col, bool act, int lane) {
+                                              GStack &S, int gs, int gpt, int col, bool act, int lane,
+                                              bool long_by_warp) {
     __syncwarp();
     const int32_t gd = dslot[0];
     const int nv = gd_nv(gd);
@@ -805,7 +842,7 @@ __device__ __forceinline__ void consume_group(const IdxParams &p, const float4 *
     if (last || gi == gpt - 1) {
         const float4 P = gpartial(S, gi + 1);
         if (sp) {
-            tile_done(p, gd_key(gd), dslot[1], gd_tfirst(gd), P, col, act, lane);
+            tile_done(p, gd_key(gd), dslot[1], gd_tfirst(gd), P, col, act, lane, long_by_warp);
             return;
         }
         ra.F = (ra.tix == 0) ? P : f4add(ra.F, P);
@@ -820,7 +857,8 @@ __device__ __forceinline__ void consume_group(const IdxParams &p, const float4 *
 // keys [k_first, k_end), walked as one stream of groups. Perm entries come one
 // quad (4 groups) ahead; source rows land in the warp's shared-memory ring
 // kStages - 1 groups ahead of the sums.
-__device__ void walk(const IdxParams &p, int32_t P0, int32_t P1, int lane, float4 *ring, int32_t *dring) {
+__device__ void walk(const IdxParams &p, int32_t P0, int32_t P1, int lane, float4 *ring, int32_t *dring,
+                     bool long_by_warp) {
     // keys from the one at P0 to the one at P1: key_rows keeps what starts in [P0, P1)
     const int32_t k_first = clampi(p.skey[P0], 0, p.R);
     const int32_t k_end = P1 < p.N ? clampi(p.skey[P1] + 1, k_first, p.R + 1) : p.R + 1;
@@ -876,7 +914,7 @@ __device__ void walk(const IdxParams &p, int32_t P0, int32_t P1, int lane, float
             issue_next();
             cp_async_wait<kStages - 1>();
             const int slot = consumed % kStages;
-            consume_group(p, ring + slot * kSlotF4, dring + slot * 2, ra, S, gs, gpt, col, act, lane);
+            consume_group(p, ring + slot * kSlotF4, dring + slot * 2, ra, S, gs, gpt, col, act, lane, long_by_warp);
             ++consumed;
         }
         cp_async_wait<0>();
@@ -945,8 +983,9 @@ __device__ void fold_rows(const IdxParams &p, int first, int stride, int n_rows,
 __global__ void __launch_bounds__(kSegThreads, 1) segsum_kernel(const IdxParams p) {
     extern __shared__ __align__(16) float4 seg_smem[];
     const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
+    const bool good = tag_ok(p);  // read while the previous launch finishes
     grid_dep_wait();
-    if (!tag_exact(p)) return;  // hist refused the workspace: nothing is written
+    if (!good) return;  // hist refused the workspace: nothing is written
     {  // what the sort passes leave behind, cleared for the next call
         const int64_t tiles = static_cast<int64_t>(p.nb) * kDigits;
         const int64_t g = static_cast<int64_t>(blockIdx.x) * kSegThreads + threadIdx.x;
@@ -964,7 +1003,9 @@ __global__ void __launch_bounds__(kSegThreads, 1) segsum_kernel(const IdxParams 
         return;
     }
     const int64_t W = static_cast<int64_t>(gridDim.x - n_fold) * kSegWarps;
-    const int64_t w = static_cast<int64_t>(blockIdx.x - n_fold) * kSegWarps + wi;
+    // shares handed to warps in the schedule's order (the warp count is known here only)
+    const Sched sw = sched_over(p.sched_warps, static_cast<uint32_t>(W));
+    const int64_t w = sched_item(sw, static_cast<uint32_t>((blockIdx.x - n_fold) * kSegWarps + wi));
     int64_t span = (static_cast<int64_t>(p.N) + W - 1) / W;
     if (span < 32) span = 32;
     const int64_t P0 = w * span;
@@ -972,7 +1013,7 @@ __global__ void __launch_bounds__(kSegThreads, 1) segsum_kernel(const IdxParams 
     const int32_t P1 = static_cast<int32_t>(min(P0 + span, static_cast<int64_t>(p.N)));
     float4 *ring = seg_smem + wi * (kStages * kSlotF4);
     int32_t *dring = reinterpret_cast<int32_t *>(seg_smem + kSegWarps * kStages * kSlotF4) + wi * (kStages * 2);
-    walk(p, static_cast<int32_t>(P0), P1, lane, ring, dring);
+    walk(p, static_cast<int32_t>(P0), P1, lane, ring, dring, n_fold == 0);
 }
 
 static_assert(2 * kFoldTiles * 32 * 16 <= kSegSmemBytes, "fold stage fits the segsum shared memory");
@@ -1097,18 +1138,23 @@ extern "C" dgr_status dgr_det_index_add(float *out, int64_t R, int64_t D, int64_
     p.slots = reinterpret_cast<float *>(w + L.slots);
     p.heavy_rows = reinterpret_cast<int32_t *>(w + L.heavy);
     p.max_fold_rows = L.max_fold_rows;
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaFuncSetAttribute(segsum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSegSmemBytes) != cudaSuccess)
+    // segsum's fold blocks wait for tiles summed by other blocks: its grid is
+    // the SMs usable at once (one block each), so every block is resident
+    int sms = 0;
+    dgr_status us = usable_sms(&sms);
+    if (us != DGR_OK) return us;
+    if (cudaFuncSetAttribute(segsum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSegSmemBytes) != cudaSuccess)
         return DGR_ERR_CUDA;
-    hist_kernel<<<L.nb, kSortThreads, 0, s>>>(p);
-    // pass 1 also has one block per 256-key bucket, where there are more buckets than tiles
-    const unsigned pass1_blocks = static_cast<unsigned>(L.nb > p.n_buckets ? L.nb : p.n_buckets);
+    // pass 1 also has one item per 256-key bucket, where there are more buckets than tiles
+    const unsigned pass1_items = static_cast<unsigned>(L.nb > p.n_buckets ? L.nb : p.n_buckets);
+    p.sched_tiles = sched_for(static_cast<uint32_t>(L.nb));
+    p.sched_pass1 = sched_for(pass1_items);
+    p.sched_warps = sched_setting();
+    hist_kernel<<<sched_grid(static_cast<unsigned>(L.nb)), kSortThreads, 0, s>>>(p);
     // segsum (persistent: one block per SM, each warp one share of the sorted
     // order) runs even without columns: it clears the sort's counters
-    if (launch_after(pass_kernel<0>, L.nb, kPassThreads, 0, s, p) != cudaSuccess ||
-        launch_after(pass_kernel<1>, pass1_blocks, kPassThreads, 0, s, p) != cudaSuccess ||
+    if (launch_after(pass_kernel<0>, sched_grid(static_cast<unsigned>(L.nb)), kPassThreads, 0, s, p) != cudaSuccess ||
+        launch_after(pass_kernel<1>, sched_grid(pass1_items), kPassThreads, 0, s, p) != cudaSuccess ||
         launch_after(segsum_kernel, static_cast<unsigned>(sms), kSegThreads, kSegSmemBytes, s, p) != cudaSuccess)
         return DGR_ERR_CUDA;
     return launch_status();

@@ -28,6 +28,7 @@ struct RowdotParams {
     float *dprob;
     int32_t accumulate;
     float *slots;         // nullable [M][n_tiles]
+    Sched sched;          // which warp takes which row
 };
 
 template <int DT>
@@ -126,11 +127,9 @@ __device__ __forceinline__ void unpack_raw(const uint4 *r, float *f) {
     }
 }
 
+// One row: its tiles' partials and their ordered fold.
 template <int DT>
-__global__ void __launch_bounds__(kWarps * 32) rowdot_kernel(const RowdotParams p, int vec) {
-    const int lane = threadIdx.x & 31;
-    const int64_t m = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-    if (m >= p.M) return;
+__device__ __forceinline__ void rowdot_row(const RowdotParams &p, int64_t m, int vec, int lane) {
     const int es = DT == DGR_DTYPE_BF16 ? 2 : 4;
     const char *rdy = p.dY + m * p.ld_dy * es;
     const char *ry = p.Y + m * p.ld_y * es;
@@ -184,6 +183,16 @@ __global__ void __launch_bounds__(kWarps * 32) rowdot_kernel(const RowdotParams 
         }
     }
     if (lane == 0) p.dprob[m] = p.accumulate ? __fadd_rn(p.dprob[m], F) : F;
+}
+
+// One warp per row (rows handed out in the schedule's order; with a capped
+// grid a warp takes several).
+template <int DT>
+__global__ void __launch_bounds__(kWarps * 32) rowdot_kernel(const RowdotParams p, int vec) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nw = static_cast<int64_t>(gridDim.x) * kWarps;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); i < p.M; i += nw)
+        rowdot_row<DT>(p, sched_item(p.sched, static_cast<uint32_t>(i)), vec, lane);
 }
 
 }  // namespace
@@ -240,10 +249,11 @@ extern "C" dgr_status dgr_ordered_rowdot_dprob(const void *dY, const void *Y, in
     p.accumulate = accumulate ? 1 : 0;
     p.slots = slots;
     const int vec = (aligned(dY, 16) && aligned(Y, 16) && (ld_dy * es) % 16 == 0 && (ld_y * es) % 16 == 0) ? 1 : 0;
-    const int64_t grid = (M + kWarps - 1) / kWarps;
+    p.sched = sched_for(static_cast<uint32_t>(M));
+    const unsigned grid = sched_grid(static_cast<unsigned>((M + kWarps - 1) / kWarps));
     if (dtype == DGR_DTYPE_BF16)
-        rowdot_kernel<DGR_DTYPE_BF16><<<static_cast<unsigned>(grid), kWarps * 32, 0, s>>>(p, vec);
+        rowdot_kernel<DGR_DTYPE_BF16><<<grid, kWarps * 32, 0, s>>>(p, vec);
     else
-        rowdot_kernel<DGR_DTYPE_F32><<<static_cast<unsigned>(grid), kWarps * 32, 0, s>>>(p, vec);
+        rowdot_kernel<DGR_DTYPE_F32><<<grid, kWarps * 32, 0, s>>>(p, vec);
     return launch_status();
 }

@@ -77,6 +77,7 @@ struct WgradParams {
     int32_t n_blk, k_blk, n_tiles;
     float *main_grad;
     WsHeader *hdr;
+    Sched sched;  // the order in which the CTAs walk the tiles
 };
 
 __device__ __forceinline__ void tile_coords(const WgradParams &p, int tau, int &e, int &nb, int &kb) {
@@ -139,7 +140,7 @@ __global__ void __launch_bounds__(kThreadsW, 1)
             bool ok = true;
             for (int tau = blockIdx.x; ok && tau < p.n_tiles; tau += gridDim.x) {
                 int e, nb, kb;
-                tile_coords(p, tau, e, nb, kb);
+                tile_coords(p, static_cast<int>(sched_item(p.sched, tau)), e, nb, kb);
                 int32_t t_beg, te;
                 expert_range(p, e, t_beg, te);
                 for (int32_t c0 = 0; ok && c0 < te; c0 += kChunk) {
@@ -183,7 +184,7 @@ __global__ void __launch_bounds__(kThreadsW, 1)
         bool committed = false, ok = true;
         for (int tau = blockIdx.x; ok && tau < p.n_tiles; tau += gridDim.x) {
             int e, nb, kb;
-            tile_coords(p, tau, e, nb, kb);
+            tile_coords(p, static_cast<int>(sched_item(p.sched, tau)), e, nb, kb);
             int32_t t_beg, te;
             expert_range(p, e, t_beg, te);
             for (int32_t c0 = 0; ok && c0 < te; c0 += kChunk, ++g) {
@@ -277,7 +278,7 @@ __global__ void __launch_bounds__(kThreadsW, 1)
         float F[128];
         for (int tau = blockIdx.x; ok && tau < p.n_tiles; tau += gridDim.x) {
             int e, nb, kb;
-            tile_coords(p, tau, e, nb, kb);
+            tile_coords(p, static_cast<int>(sched_item(p.sched, tau)), e, nb, kb);
             int32_t t_beg, te;
             expert_range(p, e, t_beg, te);
             if (te == 0) continue;  // empty expert: main_grad untouched
@@ -528,7 +529,8 @@ extern "C" dgr_status dgr_grouped_wgrad_accumulate(const void *G, const void *X,
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DGR_ERR_CUDA;
-    const int grid = static_cast<int>(n_tiles < sms ? n_tiles : sms);
+    p.sched = sched_for(static_cast<uint32_t>(n_tiles));
+    const unsigned grid = sched_grid(static_cast<unsigned>(n_tiles < sms ? n_tiles : sms));
     wgrad_kernel<<<grid, kThreadsW, kSmemBytes, static_cast<cudaStream_t>(stream)>>>(mG, mX, p);
     return launch_status();
 }

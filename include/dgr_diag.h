@@ -58,6 +58,52 @@ dgr_status dgr_diag_wait_timeout(int32_t which, int32_t limit_us, void *ws, size
  */
 dgr_status dgr_diag_noalloc_wait_timeout(int32_t which, int32_t limit_us, void *stream);
 
+/*
+ * How dgr_ordered_colsum() would launch a call of T tokens and H columns,
+ * computed on the host alone (no device needed): plan[0] = path (0: at most
+ * 512 tiles, one launch whose last warp folds; 1: warp producers and folder
+ * CTAs; 2: CTA producers and folder CTAs; -1: T = 0, nothing launched),
+ * plan[1] = launches (1, or 2 when the folders, which wait for the producers,
+ * could not all be resident beside at least one producer: producers first,
+ * folders second), plan[2] = producer CTAs, plan[3] = folder CTAs. vec_ok:
+ * whether 16-byte loads apply (x, strides and H aligned to 16 bytes). sms:
+ * SMs usable at once; cta_occupancy: CTAs of the path-2 kernel an SM holds;
+ * grid_cap: as for dgr_diag_set_schedule (0 = none).
+ */
+dgr_status dgr_diag_colsum_plan(int64_t T, int64_t H, int32_t tile_rows, int32_t dtype, int32_t vec_ok, int32_t sms,
+                                int32_t cta_occupancy, int32_t grid_cap, int32_t *plan);
+
+/*
+ * Test-only: how every later launch of this process hands out its work. The
+ * kernels take work items (tiles, rows, token chunks, warp shares) in
+ * ascending order over as many CTAs as they need; here a test can ask for
+ * order = 1 (descending) or 2 (shuffled: item i -> (a i + b) mod n with a
+ * coprime to n, a and b derived from seed), and for grid_cap > 0: no launch
+ * takes more than grid_cap CTAs (persistent kernels then have fewer CTAs and
+ * one-CTA-per-item kernels loop over their items; the column sum switches to
+ * its two-launch form when its folders and producers could not all be
+ * resident). Bits of every output must not change. (0, 0, 0) restores the
+ * default. Process-wide; not for use while other threads launch.
+ */
+dgr_status dgr_diag_set_schedule(int32_t order, uint32_t seed, int32_t grid_cap);
+
+/*
+ * Non-deterministic controls, for tests only: the reductions the pages
+ * replace, whose parts meet in float atomicAdds (Megatron-LM PR #8244: the
+ * default path's atomics across programs; cuDNN-frontend PR #521: dprob's
+ * inter-CTA atomics). A replay test that passes says something only if these
+ * change bits from run to run on the same data.
+ *   dgr_diag_atomic_colsum: out[h] = sum over t of x[t][h], x bf16 [T, H]
+ *     row-major (H <= 4096); one CTA per 128 rows, each adds its column
+ *     partials to out (zeroed first, on `stream`) with atomicAdd.
+ *   dgr_diag_atomic_rowdot: dprob[m] = sum over n of dY[m][n] Y[m][n], bf16
+ *     [M, N] row-major; one CTA per (8 rows, 128-column tile), each tile's
+ *     partial added to dprob[m] (zeroed first) with atomicAdd.
+ */
+dgr_status dgr_diag_atomic_colsum(const uint16_t *x, int64_t T, int32_t H, float *out, void *stream);
+dgr_status dgr_diag_atomic_rowdot(const uint16_t *dY, const uint16_t *Y, int64_t M, int32_t N, float *dprob,
+                                  void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -189,3 +189,33 @@ def test_noalloc_host_checks(L):
     assert L.dgr_ordered_colsum_noalloc(_p(0x10001), 1, 1, 64, 16, 0, 16, out, 0, 128, None) == 5  # x misaligned
     assert L.dgr_colsum_noalloc_read_status(0, None, None) == 1
     assert L.dgr_diag_noalloc_wait_timeout(2, 1000, None) == 1
+
+
+def test_colsum_launch_plan(L):
+    # the column sum's folders wait for its producers, so one launch holds
+    # both only when all folders and a producer can be resident at once;
+    # otherwise producers and folders run as two launches
+    plan = (ctypes.c_int32 * 4)()
+
+    def p(T, H, W=128, dtype=1, vec=1, sms=152, occ=4, cap=0):
+        assert L.dgr_diag_colsum_plan(T, H, W, dtype, vec, sms, occ, cap, plan) == 0
+        return tuple(plan)
+
+    # at most 512 tiles: one launch of 4-warp CTAs, the last warp folds
+    assert p(2048, 16) == (0, 1, 4, 0)
+    assert p(8192, 64) == (0, 1, 16, 0)
+    assert p(8192, 64, cap=3) == (0, 1, 3, 0)
+    # 65536 tiles of 64 bf16 columns: 16 folders and 136 persistent producers
+    assert p(8388608, 64) == (1, 1, 136, 16)
+    assert p(8388608, 64, sms=17) == (1, 1, 1, 16)       # just enough SMs
+    assert p(8388608, 64, sms=16) == (1, 2, 16, 16)      # a green context of 16 SMs: two launches
+    assert p(8388608, 64, cap=8) == (1, 2, 8, 8)         # the diagnostic grid cap
+    assert p(8388608, 64, cap=1) == (1, 2, 1, 1)
+    # H = 520: CTA producers, 44 folders
+    path, launches, prod, fold = p(70000, 520)
+    assert (path, launches, fold) == (2, 1, 44) and prod > 0
+    assert p(70000, 520, sms=8, occ=4)[:2] == (2, 2)     # 32 CTA slots < 45
+    assert p(70000, 520, cap=44)[1] == 2
+    assert p(0, 64) == (-1, 0, 0, 0)
+    assert L.dgr_diag_colsum_plan(100, 0, 128, 1, 1, 152, 1, 0, plan) == 1
+    assert L.dgr_diag_set_schedule(3, 0, 0) == 1 and L.dgr_diag_set_schedule(0, 0, -1) == 1

@@ -5,8 +5,11 @@ exact small integer, so the result must equal numpy's int64 G_e^T X_e plus
 main_grad bit for bit whatever the arithmetic inside a tensor-core step: this
 checks the shared-memory layout and descriptors, the pipeline, expert offsets
 (ragged, empty, not multiples of the 64-token stage or 16-token step), chunk
-tails and the final add. Empty experts must leave main_grad bitwise unchanged,
-and repeated calls must give identical bits.
+tails and the final add. Empty experts must leave main_grad bitwise unchanged.
+With random inputs, full outputs at small shapes and sampled elements of the
+full workload equal the oracle (whose tensor-core step model is pinned against
+the hardware), and the full workload gives identical bits over 20 replays,
+every other one under side-stream contention.
 """
 import numpy as np
 import pytest
@@ -81,12 +84,13 @@ def test_random_parity_full_output(counts, N, K):
 
 def test_full_workload_sampled_parity_and_replay():
     import oracle
+    from gpu_util import assert_replays_identical
     wi = gi.wgrad_full()
     dev = (wi.G.cuda(), wi.X.cuda(), wi.offs.cuda(), wi.main_grad.cuda())
-    first = _gpu(wi, dev)
-    for _ in range(2):
-        assert torch.equal(_gpu(wi, dev).view(torch.int32), first.view(torch.int32))
-    got = first.cpu().numpy()
+    ws = dgr.workspace(dgr.wgrad_workspace_bytes(8, 4096, 2048))
+    # 20 replays, every other one under side-stream contention (matmuls and a 1 GiB copy)
+    got = assert_replays_identical(lambda: _gpu(wi, dev, ws=ws), n=20).view(np.float32)
+    assert dgr.read_device_status(ws) == 0
     rng = np.random.default_rng(11)
     e = [rng.integers(0, 8, 4096)]
     n = [rng.integers(0, 4096, 4096)]
