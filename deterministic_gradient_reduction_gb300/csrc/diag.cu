@@ -40,16 +40,18 @@ __global__ void __launch_bounds__(256) atomic_colsum_kernel(const uint16_t *x, i
     }
 }
 
-// dprob, dY and Y bf16 [M, N] row-major: CTA (row block, N-tile of 128): a
+// dprob, dY and Y bf16 [M, N] row-major: CTA (N-tile of 128, row block): a
 // warp per row sums its tile's products, lane by lane then by shuffles, and
-// adds the tile's partial to dprob[m] with one atomicAdd; the 32 tiles of a
-// row arrive from 32 CTAs in whatever order they run.
+// adds the tile's partial to dprob[m] with one atomicAdd. The N-tile is the
+// fastest grid index, so a row's tiles run side by side on different SMs and
+// their atomics race (with the row block fastest, a row's tiles would run in
+// launch order, one wave after another, and the sum would look stable).
 __global__ void __launch_bounds__(256) atomic_rowdot_kernel(const uint16_t *dY, const uint16_t *Y, int64_t M,
                                                            int32_t N, float *dprob) {
     const int lane = threadIdx.x & 31;
-    const int64_t m = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const int64_t m = static_cast<int64_t>(blockIdx.y) * 8 + (threadIdx.x >> 5);
     if (m >= M) return;
-    const int64_t c0 = static_cast<int64_t>(blockIdx.y) * 128;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 128;
     float v = 0.0f;
     for (int64_t c = c0 + lane; c < min(c0 + 128, static_cast<int64_t>(N)); c += 32)
         v = __fadd_rn(v, __fmul_rn(bf16_bits_to_f32(dY[m * N + c]), bf16_bits_to_f32(Y[m * N + c])));
@@ -77,13 +79,13 @@ extern "C" dgr_status dgr_diag_atomic_colsum(const uint16_t *x, int64_t T, int32
 
 extern "C" dgr_status dgr_diag_atomic_rowdot(const uint16_t *dY, const uint16_t *Y, int64_t M, int32_t N,
                                              float *dprob, void *stream) {
-    if (M < 0 || N < 1 || N > 65536 || !dprob || (M > 0 && (!dY || !Y)) || M > INT32_MAX) return DGR_ERR_INVALID_ARG;
+    if (M < 0 || N < 1 || N > 65536 || !dprob || (M > 0 && (!dY || !Y)) || M > 65535LL * 8) return DGR_ERR_INVALID_ARG;
     dgr_status st = check_device();
     if (st != DGR_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(dprob, 0, static_cast<size_t>(M) * 4, s) != cudaSuccess) return DGR_ERR_CUDA;
     if (M == 0) return DGR_OK;
-    const dim3 grid(static_cast<unsigned>((M + 7) / 8), static_cast<unsigned>((N + 127) / 128));
+    const dim3 grid(static_cast<unsigned>((N + 127) / 128), static_cast<unsigned>((M + 7) / 8));
     atomic_rowdot_kernel<<<grid, 256, 0, s>>>(dY, Y, M, N, dprob);
     return launch_status();
 }

@@ -97,8 +97,9 @@ dgr_status dgr_diag_set_schedule(int32_t order, uint32_t seed, int32_t grid_cap)
  *     row-major (H <= 4096); one CTA per 128 rows, each adds its column
  *     partials to out (zeroed first, on `stream`) with atomicAdd.
  *   dgr_diag_atomic_rowdot: dprob[m] = sum over n of dY[m][n] Y[m][n], bf16
- *     [M, N] row-major; one CTA per (8 rows, 128-column tile), each tile's
- *     partial added to dprob[m] (zeroed first) with atomicAdd.
+ *     [M, N] row-major (M <= 524280); one CTA per (128-column tile, 8 rows),
+ *     the tile the fastest grid index, each tile's partial added to dprob[m]
+ *     (zeroed first) with atomicAdd.
  */
 dgr_status dgr_diag_atomic_colsum(const uint16_t *x, int64_t T, int32_t H, float *out, void *stream);
 dgr_status dgr_diag_atomic_rowdot(const uint16_t *dY, const uint16_t *Y, int64_t M, int32_t N, float *dprob,

@@ -82,6 +82,10 @@ def lib() -> ctypes.CDLL:
         L.dgro_grouped_dbias.restype = I32
         L.dgro_topk_canonicalize.argtypes = [P, I64, P, I64, I64, I64, P, P, P, I64]
         L.dgro_topk_canonicalize.restype = I32
+        L.dgro_exp_tang_array.argtypes = [P, P, I64]
+        L.dgro_exp_tang_array.restype = None
+        L.dgro_exp_tang_constants.argtypes = [P, P]
+        L.dgro_exp_tang_constants.restype = None
         L.dgro_aux_loss.argtypes = [P, I64, I64, I64, P, F32, P]
         L.dgro_aux_loss.restype = I32
         L.dgro_dsrelu_dprob.argtypes = [P, P, P, I64, I64, I64, I64, P, P, I32, P, I64, P]
@@ -232,6 +236,22 @@ def grouped_dbias(dY: np.ndarray, T: int, H: int, ld: int, offs: np.ndarray, out
     rc = lib().dgro_grouped_dbias(_ptr(dY), _dtype_code(dY), T, H, ld, _ptr(o), E, tile_rows, _ptr(out),
                                   ld_out, int(accumulate))
     _check(rc, "grouped_dbias")
+
+
+def exp_tang(x: np.ndarray) -> np.ndarray:
+    """The top-K softmax's binary32 exponential (Tang's table-driven method), elementwise."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty_like(x)
+    lib().dgro_exp_tang_array(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def exp_tang_constants() -> tuple[np.ndarray, np.ndarray]:
+    """The method's table: S_lead[j] and S_trail[j], 2^(j/32) split in two binary32 parts."""
+    lead = np.empty(32, np.float32)
+    trail = np.empty(32, np.float32)
+    lib().dgro_exp_tang_constants(_ptr(lead), _ptr(trail))
+    return lead, trail
 
 
 def topk_canonicalize(ids: np.ndarray, logits: np.ndarray):

