@@ -112,6 +112,15 @@ dgr_status dgr_query_device_status(const void *ws, void *stream);
  * ws:       dgr_colsum_workspace_bytes(B*S, H, tile_rows) bytes, zeroed once.
  *           Holds the [tiles, H] FP32 slots and the ready counters.
  * out must not overlap x or ws.
+ * Residency: above 512 tiles (of the 16-byte-vector shapes; every tile count
+ * for the others) folder CTAs wait, bounded, for producer CTAs of the same
+ * launch, so both must be resident together. The call sizes that launch by
+ * the SMs usable at once (the device's, or the SM partition of a green
+ * context) and, where the folders and one producer would not fit, runs the
+ * producers and then the folders as two launches. A share of the GPU the
+ * driver does not report (e.g. an MPS active-thread percentage) can still
+ * starve the producers: the folders then give up after 2 s and record
+ * DGR_ERR_TIMEOUT in the status word; out is then unspecified.
  */
 size_t dgr_colsum_workspace_bytes(int64_t T, int64_t H, int32_t tile_rows);
 dgr_status dgr_ordered_colsum(const void *x, int32_t dtype, int64_t B, int64_t S, int64_t H,
@@ -217,6 +226,10 @@ dgr_status dgr_ordered_rowdot_dprob(const void *dY, const void *Y, int32_t dtype
  *           other sizes. Offsets read back from the workspace are clamped to
  *           their arrays, so a workspace left inconsistent (e.g. by a call that
  *           timed out) gives wrong sums, never an access out of bounds.
+ * Residency: rows longer than 32 tiles of 128 are folded by blocks that wait,
+ * bounded, for the tiles other blocks sum; the last launch takes one block
+ * per SM usable at once (the device's, or a green context's partition), so
+ * all are resident; the limits of the column sum's residency note apply.
  * out must not overlap src, idx, bad_count or ws.
  */
 size_t dgr_index_add_workspace_bytes(int64_t N, int64_t R, int64_t D);
