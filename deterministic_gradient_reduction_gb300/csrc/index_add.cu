@@ -765,6 +765,23 @@ __device__ __forceinline__ void cp_async16_if(void *smem, const void *gmem, bool
         : "memory");
 }
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) { cp_async16_if(smem, gmem, true); }
+
+// The same with an L2 eviction-priority policy (src rows: read once, so
+// evict_first keeps them from pushing the workspace and out rows out of L2;
+// measured 65 -> 59 us a call with L2 flushed before each).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void cp_async16_hint_if(void *smem, const void *gmem, bool pred, uint64_t pol) {
+    const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
+        "@q cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %3;\n\t}" ::"r"(s),
+        "l"(gmem), "r"(static_cast<int>(pred)), "l"(pol)
+        : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
@@ -785,7 +802,7 @@ constexpr int kSegSmemBytes = kSegWarps * (kStages * kSlotF4 * 16 + kStages * 2 
 // only its own 16-byte column slice; the descriptor words (dslot) are written
 // by lane 0 and read by all lanes after a warp barrier.
 __device__ __forceinline__ void issue_group(const IdxParams &p, float4 *slot, int32_t *dslot, const Quad &Q, int j,
-                                            int col, bool act, int lane) {
+                                            int col, bool act, int lane, uint64_t src_pol) {
     const unsigned full = 0xffffffffu;
     const int32_t gd = __shfl_sync(full, Q.desc, j * 8);
     const int32_t aux = __shfl_sync(full, Q.aux, j * 8);
@@ -798,7 +815,8 @@ __device__ __forceinline__ void issue_group(const IdxParams &p, float4 *slot, in
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
         const int32_t row = clampi(__shfl_sync(full, Q.pq, j * 8 + u), 0, p.N - 1);  // a perm entry is a row of src
-        cp_async16_if(slot + u * 32 + lane, p.src + static_cast<int64_t>(row) * p.ld_src + col, u < nv && act);
+        cp_async16_hint_if(slot + u * 32 + lane, p.src + static_cast<int64_t>(row) * p.ld_src + col, u < nv && act,
+                           src_pol);
     }
     cp_async16_if(slot + 8 * 32 + lane, p.out + static_cast<int64_t>(gd_key(gd)) * p.ld_out + col,
                   gd_first(gd) && !gd_split(gd) && act);
@@ -865,6 +883,7 @@ __device__ void walk(const IdxParams &p, int32_t P0, int32_t P1, int lane, float
     const int gs = min(8, p.seg_tile);
     const int gpt = p.seg_tile / gs;
     const bool split_on = p.seg_tile == kSegTile;
+    const uint64_t src_pol = l2_evict_first_policy();
     for (int c0 = 0; c0 < p.D; c0 += 128) {
         const int col = c0 + lane * 4;
         const bool act = col < p.D;
@@ -894,7 +913,7 @@ __device__ void walk(const IdxParams &p, int32_t P0, int32_t P1, int lane, float
         auto issue_next = [&]() {
             if (have) {
                 const int slot = issued % kStages;
-                issue_group(p, ring + slot * kSlotF4, dring + slot * 2, Qc, ji, col, act, lane);
+                issue_group(p, ring + slot * kSlotF4, dring + slot * 2, Qc, ji, col, act, lane, src_pol);
                 ++issued;
                 if (++ji == Qc.n) {
                     ji = 0;
