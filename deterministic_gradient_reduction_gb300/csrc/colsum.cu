@@ -23,15 +23,11 @@
 // counters only tell the folder when to look, and a word the folder reads
 // before its write has arrived is read again (bounded). Producers never wait,
 // so the folders' waits always end.
-#include <cooperative_groups.h>
-
 #include "dgr_common.cuh"
 #include "dgr_diag.h"
 
 namespace dgr {
 namespace {
-
-namespace cg = cooperative_groups;
 
 constexpr int kThreads = 256;
 constexpr int kWarpThreads = 512;                 // warp-producer kernel: one CTA per SM
@@ -279,11 +275,8 @@ __device__ __forceinline__ void publish_tile(const ColsumParams &p, int pending)
 
 // MAXB: raw 16-byte loads a lane keeps in flight (a batch); the tree is the
 // same for any batch size (batches are aligned subtrees of the tile).
-// part: null, or the row [H] (in any CTA's shared memory of the cluster) that
-// receives the tile partial instead of the workspace slots.
 template <int DT, int VE, int RPL, int MAXB = 8>
-__device__ __forceinline__ void produce_warp_tile(const ColsumParams &p, int64_t wunit, int pending,
-                                                  float *part = nullptr) {
+__device__ __forceinline__ void produce_warp_tile(const ColsumParams &p, int64_t wunit, int pending) {
     using E = Elem<DT>;
     constexpr int BATCH = RPL < MAXB ? RPL : MAXB;
     constexpr int NB = RPL / BATCH;  // batches, a power of two <= 16
@@ -391,13 +384,8 @@ __device__ __forceinline__ void produce_warp_tile(const ColsumParams &p, int64_t
         present = left_present;
     }
     if (g == 0) {
-        if (part) {
 #pragma unroll
-            for (int e = 0; e < VE; ++e) part[c0 + e] = acc[e];
-        } else {
-#pragma unroll
-            for (int e = 0; e < VE; ++e) st_slot(p, c0 + e, j, acc[e]);
-        }
+        for (int e = 0; e < VE; ++e) st_slot(p, c0 + e, j, acc[e]);
     }
 }
 
@@ -632,52 +620,6 @@ __global__ void __launch_bounds__(kSmallWarps * 32) colsum_small_kernel(const Co
 
 using ColsumKernel = void (*)(const ColsumParams);
 
-// Inputs of at most kClusterTiles tiles (warp-producer shapes): one thread-
-// block cluster of up to kClusterMax CTAs of kClusterWarps warps, one warp
-// per tile (all of a lane's rows in flight at once). Each warp writes its
-// tile partial straight into CTA 0's shared memory (distributed shared
-// memory), the cluster barrier orders those writes before CTA 0 reads them,
-// and CTA 0 folds every column over the tiles in ascending order. Nothing
-// goes to the workspace and nothing waits but the barrier.
-constexpr int kClusterWarps = 8;
-constexpr int kClusterMax = 8;
-constexpr int kClusterTiles = kClusterWarps * kClusterMax;
-
-template <int DT, int VE, int RPL>
-__global__ void __launch_bounds__(kClusterWarps * 32, 1) colsum_cluster_kernel(const ColsumParams p) {
-    extern __shared__ __align__(16) float part[];  // CTA 0: [n_tiles][H]
-    cg::cluster_group cluster = cg::this_cluster();
-    float *part0 = cluster.map_shared_rank(part, 0);
-    const int nw = static_cast<int>(cluster.num_blocks()) * kClusterWarps;
-    // tiles in the schedule's order; with a capped cluster a warp takes several
-    for (int w = static_cast<int>(cluster.block_rank()) * kClusterWarps + (threadIdx.x >> 5); w < p.n_tiles;
-         w += nw) {
-        const int tile = static_cast<int>(sched_item(p.sched, static_cast<uint32_t>(w)));
-        produce_warp_tile<DT, VE, RPL, 32>(p, tile, -1, part0 + static_cast<int64_t>(tile) * p.H);
-    }
-    cluster.sync();  // release of the partials, acquire by CTA 0
-    if (cluster.block_rank() != 0) return;
-    for (int c = threadIdx.x; c < p.H; c += blockDim.x) {
-        float F = part[c];
-        for (int j = 1; j < p.n_tiles; ++j) F = __fadd_rn(F, part[static_cast<int64_t>(j) * p.H + c]);
-        p.out[c] = p.accumulate ? __fadd_rn(p.out[c], F) : F;
-    }
-}
-
-template <int DT, int VE>
-ColsumKernel cluster_kernel(int rpl) {
-    switch (rpl) {
-        case 2: return colsum_cluster_kernel<DT, VE, 2>;
-        case 4: return colsum_cluster_kernel<DT, VE, 4>;
-        case 8: return colsum_cluster_kernel<DT, VE, 8>;
-        case 16: return colsum_cluster_kernel<DT, VE, 16>;
-        case 32: return colsum_cluster_kernel<DT, VE, 32>;
-        default: return nullptr;
-    }
-}
-
-
-
 template <int DT, int VE>
 ColsumKernel cta_kernel(int rpt) {
     switch (rpt) {
@@ -719,8 +661,6 @@ ColsumKernel small_kernel(int rpl) {
 }
 
 // How a call is launched.
-//   path 3: at most kClusterTiles warp-producer tiles of at most 32 rows a
-//           lane: one cluster, partials in CTA 0's shared memory;
 //   path 0: at most kSmallTiles warp-producer tiles: one launch, a ticket,
 //           the last warp folds (nothing waits);
 //   path 1: warp producers (persistent, one CTA per SM) and folder CTAs;
@@ -735,16 +675,10 @@ struct ColsumPlan {
     int32_t fold_ctas;  // folder CTAs (in the one launch, or in the second)
 };
 
-ColsumPlan colsum_plan(int32_t n_tiles, int32_t n_fcb, int64_t n_units, bool warp_producers, bool cluster_ok,
-                       int32_t sms, int32_t cta_occupancy, int32_t cap) {
+ColsumPlan colsum_plan(int32_t n_tiles, int32_t n_fcb, int64_t n_units, bool warp_producers, int32_t sms,
+                       int32_t cta_occupancy, int32_t cap) {
     ColsumPlan pl{};
     auto capped = [cap](int64_t g) { return (cap > 0 && g > cap) ? static_cast<int64_t>(cap) : g; };
-    if (warp_producers && cluster_ok && n_tiles <= kClusterTiles) {
-        pl.path = 3;
-        pl.launches = 1;
-        pl.prod_ctas = capped((n_tiles + kClusterWarps - 1) / kClusterWarps);
-        return pl;
-    }
     if (warp_producers && n_tiles <= kSmallTiles) {
         pl.path = 0;
         pl.launches = 1;
@@ -927,11 +861,8 @@ dgr_status colsum_enqueue(const void *x, int32_t dtype, int64_t B, int64_t S, in
     if (n_units > INT32_MAX) return DGR_ERR_UNSUPPORTED;
     p.n_units = static_cast<int32_t>(n_units);
     p.sched = sched_for(static_cast<uint32_t>(n_units));
-    const bool cluster_ok = rpl <= 32;
     ColsumKernel k = nullptr;
-    if (warp_producers && cluster_ok && L.n_tiles <= kClusterTiles)
-        k = dtype == DGR_DTYPE_BF16 ? cluster_kernel<DGR_DTYPE_BF16, 8>(rpl) : cluster_kernel<DGR_DTYPE_F32, 4>(rpl);
-    else if (warp_producers && L.n_tiles <= kSmallTiles)
+    if (warp_producers && L.n_tiles <= kSmallTiles)
         k = dtype == DGR_DTYPE_BF16 ? small_kernel<DGR_DTYPE_BF16, 8>(rpl) : small_kernel<DGR_DTYPE_F32, 4>(rpl);
     else if (warp_producers)
         k = dtype == DGR_DTYPE_BF16 ? warp_kernel<DGR_DTYPE_BF16, 8>(rpl) : warp_kernel<DGR_DTYPE_F32, 4>(rpl);
@@ -951,27 +882,8 @@ dgr_status colsum_enqueue(const void *x, int32_t dtype, int64_t B, int64_t S, in
         return DGR_ERR_CUDA;
     if (!warp_producers && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kThreads, smem) != cudaSuccess)
         return DGR_ERR_CUDA;
-    const ColsumPlan pl = colsum_plan(L.n_tiles, L.n_fcb, n_units, warp_producers, cluster_ok, sms, occ, p.sched.cap);
+    const ColsumPlan pl = colsum_plan(L.n_tiles, L.n_fcb, n_units, warp_producers, sms, occ, p.sched.cap);
     if (pl.prod_ctas + pl.fold_ctas > INT32_MAX) return DGR_ERR_UNSUPPORTED;
-    if (pl.path == 3) {  // one cluster of pl.prod_ctas CTAs; the partials in CTA 0's shared memory
-        const size_t part_bytes = static_cast<size_t>(L.n_tiles) * H * 4;
-        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(part_bytes)) !=
-            cudaSuccess)
-            return DGR_ERR_CUDA;
-        cudaLaunchConfig_t cfg{};
-        cfg.gridDim = dim3(static_cast<unsigned>(pl.prod_ctas));
-        cfg.blockDim = dim3(kClusterWarps * 32);
-        cfg.dynamicSmemBytes = part_bytes;
-        cfg.stream = s;
-        cudaLaunchAttribute at[1];
-        at[0].id = cudaLaunchAttributeClusterDimension;
-        at[0].val.clusterDim.x = static_cast<unsigned>(pl.prod_ctas);
-        at[0].val.clusterDim.y = 1;
-        at[0].val.clusterDim.z = 1;
-        cfg.attrs = at;
-        cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, k, p) == cudaSuccess ? launch_status() : DGR_ERR_CUDA;
-    }
     if (pl.launches == 1) {
         p.fold_ctas = small ? 0 : pl.fold_ctas;
         k<<<static_cast<unsigned>(p.fold_ctas + pl.prod_ctas), threads, smem, s>>>(p);
@@ -1023,8 +935,7 @@ extern "C" dgr_status dgr_diag_colsum_plan(int64_t T, int64_t H, int32_t tile_ro
     colsum_geometry(p, H, tile_rows, dtype == DGR_DTYPE_BF16 ? 2 : 4, vec_ok != 0, L.n_tiles, VE, rpt, rpl);
     const bool warp_producers = p.stream_mode != 0;
     const int64_t n_units = warp_producers ? L.n_tiles : (L.n_tiles + p.TPC - 1) / p.TPC * p.n_pcb;
-    const ColsumPlan pl =
-        colsum_plan(L.n_tiles, L.n_fcb, n_units, warp_producers, rpl <= 32, sms, cta_occupancy, grid_cap);
+    const ColsumPlan pl = colsum_plan(L.n_tiles, L.n_fcb, n_units, warp_producers, sms, cta_occupancy, grid_cap);
     plan[0] = pl.path;
     plan[1] = pl.launches;
     plan[2] = static_cast<int32_t>(pl.prod_ctas);

@@ -60,11 +60,10 @@ dgr_status dgr_diag_noalloc_wait_timeout(int32_t which, int32_t limit_us, void *
 
 /*
  * How dgr_ordered_colsum() would launch a call of T tokens and H columns,
- * computed on the host alone (no device needed): plan[0] = path (3: at most
- * 64 tiles of 16-byte-vector shapes, one thread-block cluster whose CTA 0
- * folds from shared memory; 0: at most 512 such tiles, one launch whose last
- * warp folds; 1: warp producers and folder CTAs; 2: CTA producers and folder
- * CTAs; -1: T = 0, nothing launched),
+ * computed on the host alone (no device needed): plan[0] = path (0: at most
+ * 512 tiles of 16-byte-vector shapes, one launch whose last warp folds; 1:
+ * warp producers and folder CTAs; 2: CTA producers and folder CTAs; -1: T = 0,
+ * nothing launched),
  * plan[1] = launches (1, or 2 when the folders, which wait for the producers,
  * could not all be resident beside at least one producer: producers first,
  * folders second), plan[2] = producer CTAs, plan[3] = folder CTAs. vec_ok:

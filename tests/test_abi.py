@@ -201,12 +201,10 @@ def test_colsum_launch_plan(L):
         assert L.dgr_diag_colsum_plan(T, H, W, dtype, vec, sms, occ, cap, plan) == 0
         return tuple(plan)
 
-    # at most 64 tiles: one cluster of 8-warp CTAs, one warp a tile
-    assert p(2048, 16) == (3, 1, 2, 0)
-    assert p(8192, 64) == (3, 1, 8, 0)
-    assert p(8192, 64, cap=3) == (3, 1, 3, 0)
-    assert p(8192, 256)[0] == 0                          # 128 rows a lane: the ticket path
     # at most 512 tiles: one launch of 4-warp CTAs, the last warp folds
+    assert p(2048, 16) == (0, 1, 4, 0)
+    assert p(8192, 64) == (0, 1, 16, 0)
+    assert p(8192, 64, cap=3) == (0, 1, 3, 0)
     assert p(65536, 64) == (0, 1, 128, 0)
     assert p(65536, 64, cap=5) == (0, 1, 5, 0)
     # 65536 tiles of 64 bf16 columns: 16 folders and 136 persistent producers
