@@ -321,12 +321,13 @@ __global__ void __launch_bounds__(kPassThreads) pass_kernel(const IdxParams p) {
     // grid a block takes several). No item waits for another.
     const int32_t n_items = PASS == 0 ? p.nb : max(p.nb, p.n_buckets);
     const Sched &sc = PASS == 0 ? p.sched_tiles : p.sched_pass1;
+    __shared__ int32_t s_good;
     for (int q = tid; q < kSortWarps * kDigits; q += kPassThreads) (&cnt[0][0])[q] = 0;
     launch_dependents();
-    const bool good = tag_ok(p);  // read while the previous launch finishes
+    if (tid == 0) s_good = tag_ok(p);  // read while the previous launch finishes
     grid_dep_wait();
-    if (!good) return;  // hist refused the workspace (the same answer in every thread)
     __syncthreads();
+    if (!s_good) return;  // hist refused the workspace
     for (int32_t it = blockIdx.x; it < n_items; it += gridDim.x) {
         const int32_t b = static_cast<int32_t>(sched_item(sc, static_cast<uint32_t>(it)));
         // pass 1's first n_buckets items also own the segment starts of bucket b
@@ -1002,9 +1003,11 @@ __device__ void fold_rows(const IdxParams &p, int first, int stride, int n_rows,
 __global__ void __launch_bounds__(kSegThreads, 1) segsum_kernel(const IdxParams p) {
     extern __shared__ __align__(16) float4 seg_smem[];
     const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
-    const bool good = tag_ok(p);  // read while the previous launch finishes
+    __shared__ int32_t s_good;
+    if (threadIdx.x == 0) s_good = tag_ok(p);  // read while the previous launch finishes
     grid_dep_wait();
-    if (!good) return;  // hist refused the workspace: nothing is written
+    __syncthreads();
+    if (!s_good) return;  // hist refused the workspace: nothing is written
     {  // what the sort passes leave behind, cleared for the next call
         const int64_t tiles = static_cast<int64_t>(p.nb) * kDigits;
         const int64_t g = static_cast<int64_t>(blockIdx.x) * kSegThreads + threadIdx.x;
