@@ -12,7 +12,10 @@
 //   main_grad = RN(main_grad + dW), read-modify-write in the same kernel.
 //
 // Persistent kernel, one CTA per SM, 128 x 256 output tiles (n x k) walked
-// expert by expert. Warp 0 issues TMA loads (64-token stages, 128-byte
+// expert by expert; when the last wave of tiles would keep at most half the
+// CTAs busy, its tiles run as halves of 128 k columns (MMA N = 128) instead,
+// twice as many items of half the work (each output element is computed the
+// same way by either MMA shape). Warp 0 issues TMA loads (64-token stages, 128-byte
 // swizzle; G and X are MN-major as they lie in memory, so no transpose), warp
 // 1 issues tcgen05.mma into one of two TMEM accumulators (256 columns each),
 // warps 4-11 read the accumulator back, fold the chunks and finish the tile
@@ -56,6 +59,7 @@ constexpr uint32_t kStageBytes = kStageA + kStageB;
 constexpr uint32_t kLBO = kBoxBytes;                      // between 64-wide atoms along n / k
 constexpr uint32_t kSBO = 1024;                           // between 8-token row groups
 constexpr uint32_t kIdesc = idesc_bf16_mn(BM, BN);
+constexpr uint32_t kIdescHalf = idesc_bf16_mn(BM, BN / 2);  // a half tile: 128 k columns
 constexpr uint32_t kTmemCols = 2 * BN;
 
 struct Ctl {
@@ -78,8 +82,23 @@ struct WgradParams {
     int32_t n_blk, k_blk, n_tiles;
     float *main_grad;
     WsHeader *hdr;
-    Sched sched;  // the order in which the CTAs walk the tiles
+    // Work items: tiles below n_split whole, the rest as two halves of 128 k
+    // columns each (items n_split + 2j and + 2j + 1), so that a last wave that
+    // would leave more than half the CTAs idle is spread over twice as many.
+    int32_t n_split, n_items;
+    Sched sched;  // the order in which the CTAs walk the items
 };
+
+// item -> tile, and its half (-1: the whole tile)
+__device__ __forceinline__ int item_tile(const WgradParams &p, int item, int &half) {
+    if (item < p.n_split) {
+        half = -1;
+        return item;
+    }
+    const int j = item - p.n_split;
+    half = j & 1;
+    return p.n_split + (j >> 1);
+}
 
 __device__ __forceinline__ void tile_coords(const WgradParams &p, int tau, int &e, int &nb, int &kb) {
     const int per = p.n_blk * p.k_blk;
@@ -98,7 +117,7 @@ __device__ __forceinline__ void expert_range(const WgradParams &p, int e, int32_
 
 __global__ void __launch_bounds__(kThreadsW, 1)
     wgrad_kernel(const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmX,
-                 const WgradParams p) {
+                 const __grid_constant__ CUtensorMap tmX2, const WgradParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *xpose = reinterpret_cast<float *>(smem + kStages * kStageBytes);
@@ -120,6 +139,7 @@ __global__ void __launch_bounds__(kThreadsW, 1)
         fence_mbar_init();
         prefetch_tmap(&tmG);
         prefetch_tmap(&tmX);
+        prefetch_tmap(&tmX2);
     }
     if (warp == 1) {
         tmem_alloc(&ctl->tmem_base, kTmemCols);
@@ -139,9 +159,10 @@ __global__ void __launch_bounds__(kThreadsW, 1)
             bool armed[kStages] = {};
             uint32_t armed_phase[kStages] = {};
             bool ok = true;
-            for (int tau = blockIdx.x; ok && tau < p.n_tiles; tau += gridDim.x) {
+            for (int tau = blockIdx.x; ok && tau < p.n_items; tau += gridDim.x) {
                 int e, nb, kb;
-                tile_coords(p, static_cast<int>(sched_item(p.sched, tau)), e, nb, kb);
+                int half;
+                tile_coords(p, item_tile(p, static_cast<int>(sched_item(p.sched, tau)), half), e, nb, kb);
                 int32_t t_beg, te;
                 expert_range(p, e, t_beg, te);
                 for (int32_t c0 = 0; ok && c0 < te; c0 += kChunk) {
@@ -154,12 +175,13 @@ __global__ void __launch_bounds__(kThreadsW, 1)
                         uint8_t *sA = smem + stage * kStageBytes;
                         uint8_t *sB = sA + kStageA;
                         const int32_t t = t_beg + c0 + s0;
-                        mbar_arrive_expect_tx(&ctl->full[stage], kStageBytes);
+                        mbar_arrive_expect_tx(&ctl->full[stage], half < 0 ? kStageBytes : kStageA + 2 * kBoxBytes);
                         armed[stage] = true;
                         armed_phase[stage] = phase;
                         // G: 2 column blocks of 64, X: 4, one copy each
                         tma_load_3d(sA, &tmG, &ctl->full[stage], 0, t, nb * (BM / 64));
-                        tma_load_3d(sB, &tmX, &ctl->full[stage], 0, t, kb * (BN / 64));
+                        if (half < 0) tma_load_3d(sB, &tmX, &ctl->full[stage], 0, t, kb * (BN / 64));
+                        else tma_load_3d(sB, &tmX2, &ctl->full[stage], 0, t, kb * (BN / 64) + 2 * half);
                         if (++stage == kStages) {
                             stage = 0;
                             phase ^= 1;
@@ -178,9 +200,10 @@ __global__ void __launch_bounds__(kThreadsW, 1)
         uint32_t stage = 0, phase = 0, g = 0;
         uint32_t last_stage = 0, last_phase = 0;  // the latest stage-release commit
         bool committed = false, ok = true;
-        for (int tau = blockIdx.x; ok && tau < p.n_tiles; tau += gridDim.x) {
+        for (int tau = blockIdx.x; ok && tau < p.n_items; tau += gridDim.x) {
             int e, nb, kb;
-            tile_coords(p, static_cast<int>(sched_item(p.sched, tau)), e, nb, kb);
+            int half;
+            tile_coords(p, item_tile(p, static_cast<int>(sched_item(p.sched, tau)), half), e, nb, kb);
             int32_t t_beg, te;
             expert_range(p, e, t_beg, te);
             for (int32_t c0 = 0; ok && c0 < te; c0 += kChunk, ++g) {
@@ -230,15 +253,16 @@ __global__ void __launch_bounds__(kThreadsW, 1)
                                 bd[kk] = smem_desc_sw128(b0 + kk * 2048, kLBO, kSBO);
                             }
                             const uint32_t acc0 = s0 > 0 ? 1u : 0u;
-                            mma_bf16(d_tmem, ad[0], bd[0], kIdesc, acc0);
-                            mma_bf16(d_tmem, ad[1], bd[1], kIdesc, 1u);
-                            mma_bf16(d_tmem, ad[2], bd[2], kIdesc, 1u);
-                            mma_bf16(d_tmem, ad[3], bd[3], kIdesc, 1u);
+                            const uint32_t idesc = half < 0 ? kIdesc : kIdescHalf;
+                            mma_bf16(d_tmem, ad[0], bd[0], idesc, acc0);
+                            mma_bf16(d_tmem, ad[1], bd[1], idesc, 1u);
+                            mma_bf16(d_tmem, ad[2], bd[2], idesc, 1u);
+                            mma_bf16(d_tmem, ad[3], bd[3], idesc, 1u);
                         } else {
                             for (int kk = 0; kk < nk; ++kk) {
                                 const uint64_t ad = smem_desc_sw128(a0 + kk * 2048, kLBO, kSBO);
                                 const uint64_t bd = smem_desc_sw128(b0 + kk * 2048, kLBO, kSBO);
-                                mma_bf16(d_tmem, ad, bd, kIdesc, (s0 > 0 || kk > 0) ? 1u : 0u);
+                                mma_bf16(d_tmem, ad, bd, half < 0 ? kIdesc : kIdescHalf, (s0 > 0 || kk > 0) ? 1u : 0u);
                             }
                         }
                         mma_commit(&ctl->empty[stage]);
@@ -272,12 +296,16 @@ __global__ void __launch_bounds__(kThreadsW, 1)
         uint32_t g = 0;
         bool ok = true;
         float F[128];
-        for (int tau = blockIdx.x; ok && tau < p.n_tiles; tau += gridDim.x) {
+        for (int tau = blockIdx.x; ok && tau < p.n_items; tau += gridDim.x) {
             int e, nb, kb;
-            tile_coords(p, static_cast<int>(sched_item(p.sched, tau)), e, nb, kb);
+            int half;
+            tile_coords(p, item_tile(p, static_cast<int>(sched_item(p.sched, tau)), half), e, nb, kb);
             int32_t t_beg, te;
             expert_range(p, e, t_beg, te);
             if (te == 0) continue;  // empty expert: main_grad untouched
+            // a half tile's 128 columns are the first column half's (h = 0)
+            const bool active = half < 0 || h == 0;
+            const int coff = half < 0 ? 128 * h : 128 * half;
             // The warp's 32 rows of this tile's main_grad (its column half, 512 B a
             // row) are brought into L2 a share per chunk, ahead of the add at the
             // tile's end. (Issued by the TMA thread as one burst of 128 prefetches
@@ -285,13 +313,13 @@ __global__ void __launch_bounds__(kThreadsW, 1)
             const int n_ch = (te + kChunk - 1) / kChunk;
             const int pf_per = (32 + n_ch - 1) / n_ch;
             const float *mg_pf =
-                p.main_grad + (static_cast<int64_t>(e) * p.N + nb * BM + 32 * q) * p.K + kb * BN + 128 * h;
+                p.main_grad + (static_cast<int64_t>(e) * p.N + nb * BM + 32 * q) * p.K + kb * BN + coff;
             int pf_row = 0;
             for (int32_t c0 = 0; c0 < te; c0 += kChunk, ++g) {
                 const uint32_t buf = g & 1, tph = (g >> 1) & 1;
                 {
                     const int r1 = min(32, pf_row + pf_per);
-                    if (lane < r1 - pf_row)
+                    if (active && lane < r1 - pf_row)
                         prefetch_l2_bulk(mg_pf + static_cast<int64_t>(pf_row + lane) * p.K, 128 * 4);
                     pf_row = r1;
                 }
@@ -300,9 +328,10 @@ __global__ void __launch_bounds__(kThreadsW, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t base = tmem + (static_cast<uint32_t>(32 * q) << 16) + buf * BN + 128 * h;
+                const uint32_t base = tmem + (static_cast<uint32_t>(32 * q) << 16) + buf * BN + (half < 0 ? 128 * h : 0);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
+                    if (!active) break;
                     uint32_t r[32];
                     tmem_ld32(base + 32 * j, r);
                     tmem_wait_ld();
@@ -319,13 +348,14 @@ __global__ void __launch_bounds__(kThreadsW, 1)
                 if (lane == 0) mbar_arrive(&ctl->tempty[buf]);
             }
             if (!ok) break;
+            if (!active) continue;
             // main_grad += dW through the warp's transpose tile: lane i holds row
             // (32q + i) of the tile; each 32-column slice is written row-wise to
             // shared memory and read back column-wise, so that lane i then owns
             // column i of the slice and every load/store covers one 128-byte line
             float *xt = xpose + (warp - 4) * 32 * 33;
             const int64_t row0 = static_cast<int64_t>(e) * p.N + nb * BM + 32 * q;
-            float *mg = p.main_grad + row0 * p.K + kb * BN + 128 * h + lane;
+            float *mg = p.main_grad + row0 * p.K + kb * BN + coff + lane;
             // slice j (32 rows x 32 columns): all 32 reads in flight
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -522,9 +552,10 @@ extern "C" dgr_status dgr_grouped_wgrad_accumulate(const void *G, const void *X,
     if (T_total == 0) return DGR_OK;
     st = set_smem_attrs();
     if (st != DGR_OK) return st;
-    CUtensorMap mG, mX;
+    CUtensorMap mG, mX, mX2;
     if ((st = make_map(&mG, G, T_total, N, BM / 64)) != DGR_OK) return st;
     if ((st = make_map(&mX, X, T_total, K, BN / 64)) != DGR_OK) return st;
+    if ((st = make_map(&mX2, X, T_total, K, BN / 128)) != DGR_OK) return st;
     WgradParams p{};
     p.offs = d_offs;
     p.E = E;
@@ -540,9 +571,16 @@ extern "C" dgr_status dgr_grouped_wgrad_accumulate(const void *G, const void *X,
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DGR_ERR_CUDA;
-    p.sched = sched_for(static_cast<uint32_t>(n_tiles));
-    const unsigned grid = sched_grid(static_cast<unsigned>(n_tiles < sms ? n_tiles : sms));
-    wgrad_kernel<<<grid, kThreadsW, kSmemBytes, static_cast<cudaStream_t>(stream)>>>(mG, mX, p);
+    // a last wave filling at most half the CTAs runs as half tiles instead
+    const int64_t G0 = n_tiles < sms ? n_tiles : sms;
+    const int64_t rem = n_tiles % G0;
+    p.n_split = static_cast<int32_t>(rem > 0 && 2 * rem <= G0 ? n_tiles - rem : n_tiles);
+    const int64_t n_items = p.n_split + 2 * (n_tiles - p.n_split);
+    if (n_items > INT32_MAX) return DGR_ERR_UNSUPPORTED;
+    p.n_items = static_cast<int32_t>(n_items);
+    p.sched = sched_for(static_cast<uint32_t>(n_items));
+    const unsigned grid = sched_grid(static_cast<unsigned>(n_items < sms ? n_items : sms));
+    wgrad_kernel<<<grid, kThreadsW, kSmemBytes, static_cast<cudaStream_t>(stream)>>>(mG, mX, mX2, p);
     return launch_status();
 }
 
