@@ -14,7 +14,8 @@ moves several GB, far more than the 129 MB L2, so no operation finds its
 inputs in L2 from the previous step (no separate flush is needed).
 
 Printed (rank 0, one JSON line): the ordered-reduction throughput in GB/s
-(algorithmic bytes of the five reductions over their device time), the wgrad
+(algorithmic bytes of the five reductions over their device time, the five
+run back to back K times between one pair of CUDA events), the wgrad
 TFLOP/s, per-operation figures, the roofline of the dominant operation, the
 end-to-end figure through host buffers, SM clocks sampled during the timed
 region and the CPU oracle's own rate on the host cores.
@@ -365,11 +366,30 @@ def run_ours(args, rank, world, local_rank):
     total_ms = step0.elapsed_time(step1)
     per_ms = {n: sum(a.elapsed_time(b) for a, b in ev[n]) / K for n in order}
 
+    # The five reductions back to back, K times, between one pair of events:
+    # the whole-job time of the reduction work, without the per-operation
+    # event records (each bracket above holds a launch and two records, about
+    # 4.7 us even around an empty kernel on this GPU).
+    red_order = [n for n in order if n in REDUCTIONS]
+    for n in red_order:
+        ops[n]()
+    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    r0.record(stream)
+    for k in range(K):
+        for n in red_order:
+            ops[n]()
+    r1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    red_b2b_ms = r0.elapsed_time(r1) / K
+
     # max over ranks
     if world > 1:
-        m = max_over_ranks([total_ms] + [per_ms[n] for n in order], dev)
-        total_ms = m[0]
-        per_ms = {n: m[i + 1] for i, n in enumerate(order)}
+        m = max_over_ranks([total_ms, red_b2b_ms] + [per_ms[n] for n in order], dev)
+        total_ms, red_b2b_ms = m[0], m[1]
+        per_ms = {n: m[i + 2] for i, n in enumerate(order)}
 
     # end to end through host buffers: pinned host inputs copied in, outputs read back, every step
     # the next rows of the scope, each timed on its own after the step (not in
@@ -434,7 +454,8 @@ def run_ours(args, rank, world, local_rank):
     traffic = load_traffic()  # per-launch DRAM bytes of the kernels as they stand (profiles/)
     red_ms = sum(per_ms[n] for n in REDUCTIONS)
     red_bytes = sum(ALGO[n] for n in REDUCTIONS)
-    value = world * red_bytes / (red_ms * 1e-3) / 1e9
+    value = world * red_bytes / (red_b2b_ms * 1e-3) / 1e9
+    value_per_op = world * red_bytes / (red_ms * 1e-3) / 1e9
     parts = {}
     for n in order:
         ms = per_ms[n]
@@ -482,9 +503,12 @@ def run_ours(args, rank, world, local_rank):
                    "l2_next_rows": L2_NEXT_ROWS,
                    "parallelism": f"replicas x{world}", "wgrad": "included" if with_wgrad else "not built"},
         "reductions_frac_hbm": round(value / world / peaks["hbm"], 4),
+        "reductions_us": {"back_to_back": round(red_b2b_ms * 1e3, 2), "sum_of_brackets": round(red_ms * 1e3, 2),
+                          "value_from_brackets": round(value_per_op, 1)},
         "wgrad_tflops": parts.get("wgrad", {}).get("tflops"),
         "parts": parts, "next_rows": next_rows, "roofline": roof, "e2e": e2e, "clocks": clocks,
         "gpu_launches": K * sum(LAUNCHES[n] for n in order),
+        "gpu_launches_reductions_loop": K * sum(LAUNCHES[n] for n in order if n in REDUCTIONS),
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
