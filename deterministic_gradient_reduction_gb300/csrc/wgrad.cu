@@ -9,7 +9,11 @@
 //         expert's first token, a fresh accumulator per chunk, K16 steps in
 //         ascending token order;
 //   dW  = fold_c p_c (ascending, in registers of the epilogue warps);
-//   main_grad = RN(main_grad + dW), read-modify-write in the same kernel.
+//   main_grad = RN(main_grad + dW), in the same kernel: the epilogue hands dW
+//         to the bulk copy engine's tensor reduce-add, which adds it into
+//         main_grad in L2 (one round-to-nearest add per element, subnormals
+//         kept; each element has exactly this one writer, so no order is
+//         involved).
 //
 // Persistent kernel, one CTA per SM, 128 x 256 output tiles (n x k) walked
 // expert by expert; when the last wave of tiles would keep at most half the
@@ -20,8 +24,8 @@
 // 1 issues tcgen05.mma into one of two TMEM accumulators (256 columns each),
 // warps 4-11 read the accumulator back, fold the chunks and finish the tile
 // (the epilogue warpgroups hold the running fold, 128 fp32 per thread, so
-// they take most of the registers; warps 2-3 idle); they also bring the
-// tile's main_grad into L2, a share with each chunk, ahead of its update.
+// they take most of the registers; warps 2-3 idle) and issue the tile's
+// reduce-adds through a 4 KB shared-memory box each.
 // Rows of a stage past the expert's end are zeroed in shared memory before
 // the MMA reads them (TMA fills rows past the tensor's end with zeros).
 // Every wait is bounded; a timeout records DGR_ERR_TIMEOUT and aborts the
@@ -70,10 +74,11 @@ struct Ctl {
     uint32_t tmem_base;
     int abort;
 };
-// per epilogue warp, a 32 x 33 fp32 tile to turn its rows (one per lane, as
-// TMEM gives them) into columns, so main_grad is read and written in whole
-// 128-byte lines
-constexpr uint32_t kXposeBytes = kEpiWarps * 32 * 33 * 4;
+// per epilogue warp, one 32 x 32 fp32 box (4 KB, 1024-byte aligned) for the
+// reduce-add of a 32-column slice of its 32 rows, in the 128-byte swizzle of
+// the main_grad tensor map
+constexpr uint32_t kBoxM = 32 * 32 * 4;
+constexpr uint32_t kXposeBytes = kEpiWarps * kBoxM;
 constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + kXposeBytes + sizeof(Ctl);
 
 struct WgradParams {
@@ -90,6 +95,22 @@ struct WgradParams {
 };
 
 // item -> tile, and its half (-1: the whole tile)
+// main_grad[y .. y + 31][x .. x + 31] += the box at src (bulk async group).
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap *map, uint32_t src, int32_t x, int32_t y) {
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the thread's committed bulk operations have read their shared memory
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// ... and are complete
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void st_shared_v4(uint32_t a, float x, float y, float z, float w) {
+    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(x), "f"(y), "f"(z), "f"(w) : "memory");
+}
+
 __device__ __forceinline__ int item_tile(const WgradParams &p, int item, int &half) {
     if (item < p.n_split) {
         half = -1;
@@ -117,10 +138,11 @@ __device__ __forceinline__ void expert_range(const WgradParams &p, int e, int32_
 
 __global__ void __launch_bounds__(kThreadsW, 1)
     wgrad_kernel(const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmX,
-                 const __grid_constant__ CUtensorMap tmX2, const WgradParams p) {
+                 const __grid_constant__ CUtensorMap tmX2, const __grid_constant__ CUtensorMap tmM,
+                 const WgradParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float *xpose = reinterpret_cast<float *>(smem + kStages * kStageBytes);
+    uint8_t *xbox = smem + kStages * kStageBytes;
     Ctl *ctl = reinterpret_cast<Ctl *>(smem + kStages * kStageBytes + kXposeBytes);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -140,6 +162,7 @@ __global__ void __launch_bounds__(kThreadsW, 1)
         prefetch_tmap(&tmG);
         prefetch_tmap(&tmX);
         prefetch_tmap(&tmX2);
+        prefetch_tmap(&tmM);
     }
     if (warp == 1) {
         tmem_alloc(&ctl->tmem_base, kTmemCols);
@@ -306,23 +329,8 @@ __global__ void __launch_bounds__(kThreadsW, 1)
             // a half tile's 128 columns are the first column half's (h = 0)
             const bool active = half < 0 || h == 0;
             const int coff = half < 0 ? 128 * h : 128 * half;
-            // The warp's 32 rows of this tile's main_grad (its column half, 512 B a
-            // row) are brought into L2 a share per chunk, ahead of the add at the
-            // tile's end. (Issued by the TMA thread as one burst of 128 prefetches
-            // at the last chunk, they held up its stage copies: 481 -> 445 us.)
-            const int n_ch = (te + kChunk - 1) / kChunk;
-            const int pf_per = (32 + n_ch - 1) / n_ch;
-            const float *mg_pf =
-                p.main_grad + (static_cast<int64_t>(e) * p.N + nb * BM + 32 * q) * p.K + kb * BN + coff;
-            int pf_row = 0;
             for (int32_t c0 = 0; c0 < te; c0 += kChunk, ++g) {
                 const uint32_t buf = g & 1, tph = (g >> 1) & 1;
-                {
-                    const int r1 = min(32, pf_row + pf_per);
-                    if (active && lane < r1 - pf_row)
-                        prefetch_l2_bulk(mg_pf + static_cast<int64_t>(pf_row + lane) * p.K, 128 * 4);
-                    pf_row = r1;
-                }
                 if (!mbar_wait(&ctl->tfull[buf], tph, abort_flag, p.hdr, 13)) {
                     ok = false;
                     break;
@@ -349,29 +357,36 @@ __global__ void __launch_bounds__(kThreadsW, 1)
             }
             if (!ok) break;
             if (!active) continue;
-            // main_grad += dW through the warp's transpose tile: lane i holds row
-            // (32q + i) of the tile; each 32-column slice is written row-wise to
-            // shared memory and read back column-wise, so that lane i then owns
-            // column i of the slice and every load/store covers one 128-byte line
-            float *xt = xpose + (warp - 4) * 32 * 33;
-            const int64_t row0 = static_cast<int64_t>(e) * p.N + nb * BM + 32 * q;
-            float *mg = p.main_grad + row0 * p.K + kb * BN + coff + lane;
-            // slice j (32 rows x 32 columns): all 32 reads in flight
+            // main_grad += dW, a 32-column slice at a time: row i of the warp's 32
+            // rows (lane i, as TMEM gives them) goes to the warp's box in the map's
+            // 128-byte swizzle (16-byte chunk c of row i at chunk c ^ (i % 8), so
+            // the 32 lanes' stores spread over the banks), one tensor reduce-add
+            // sends the box to main_grad, and the next slice waits until the
+            // engine has read the box. The SM never reads main_grad: the add
+            // happens in L2 (442 us a call with the read-modify-write in the
+            // epilogue warps, through a transpose tile, after an L2 prefetch of
+            // the tile's main_grad; 423 us this way, the same bits).
+            const uint32_t xs = smem_u32(xbox) + (warp - 4) * kBoxM;
+            const int32_t row0 = e * p.N + nb * BM + 32 * q;
+            const int32_t col0 = kb * BN + coff;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) xt[lane * 33 + i] = F[32 * j + i];
+                if (lane == 0) bulk_wait_read0();
                 __syncwarp();
-                float m[32];
 #pragma unroll
-                for (int r = 0; r < 32; ++r) m[r] = mg[static_cast<int64_t>(r) * p.K + 32 * j];
-#pragma unroll
-                for (int r = 0; r < 32; ++r)
-                    mg[static_cast<int64_t>(r) * p.K + 32 * j] = __fadd_rn(m[r], xt[r * 33 + lane]);
+                for (int c = 0; c < 8; ++c)
+                    st_shared_v4(xs + lane * 128 + 16 * (c ^ (lane & 7)), F[32 * j + 4 * c], F[32 * j + 4 * c + 1],
+                                 F[32 * j + 4 * c + 2], F[32 * j + 4 * c + 3]);
+                fence_proxy_async_smem();
                 __syncwarp();
+                if (lane == 0) {
+                    tma_reduce_add_2d(&tmM, xs, col0 + 32 * j, row0);
+                    bulk_commit();
+                }
             }
         }
     }
+    if (warp >= 4 && lane == 0) bulk_wait0();  // the warp's last reduce-adds are done
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -502,6 +517,22 @@ dgr_status make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols
     return r == CUDA_SUCCESS ? DGR_OK : DGR_ERR_CUDA;
 }
 
+// Tensor map over main_grad as fp32 [rows, cols] row-major: a box of 32 rows x
+// 32 columns (128 bytes a row), 128-byte swizzle.
+dgr_status make_mg_map(CUtensorMap *m, void *base, int64_t rows, int64_t cols) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    dgr_status st = encode_fn(&enc);
+    if (st != DGR_OK) return st;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 4)};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? DGR_OK : DGR_ERR_CUDA;
+}
+
 std::once_flag g_attr_once[64];
 cudaError_t g_attr_err[64];
 
@@ -535,7 +566,8 @@ extern "C" dgr_status dgr_grouped_wgrad_accumulate(const void *G, const void *X,
                                                    int64_t T_total, int64_t N, int64_t K, float *main_grad,
                                                    int32_t chunk_tokens, void *ws, size_t ws_bytes, void *stream) {
     if (E < 1 || T_total < 0 || N <= 0 || K <= 0 || chunk_tokens != kChunk) return DGR_ERR_INVALID_ARG;
-    if (N % BM != 0 || K % BN != 0 || T_total >= INT32_MAX || N > (1 << 20) || K > (1 << 20))
+    if (N % BM != 0 || K % BN != 0 || T_total >= INT32_MAX || N > (1 << 20) || K > (1 << 20) ||
+        static_cast<int64_t>(E) * N > INT32_MAX)
         return DGR_ERR_UNSUPPORTED;
     if (!main_grad || !d_offs || !ws || (T_total > 0 && (!G || !X))) return DGR_ERR_INVALID_ARG;
     if (ws_bytes < sizeof(WsHeader)) return DGR_ERR_WORKSPACE_TOO_SMALL;
@@ -556,6 +588,8 @@ extern "C" dgr_status dgr_grouped_wgrad_accumulate(const void *G, const void *X,
     if ((st = make_map(&mG, G, T_total, N, BM / 64)) != DGR_OK) return st;
     if ((st = make_map(&mX, X, T_total, K, BN / 64)) != DGR_OK) return st;
     if ((st = make_map(&mX2, X, T_total, K, BN / 128)) != DGR_OK) return st;
+    CUtensorMap mM;  // main_grad as [E * N, K]: the row coordinate fits 32 bits
+    if ((st = make_mg_map(&mM, main_grad, static_cast<int64_t>(E) * N, K)) != DGR_OK) return st;
     WgradParams p{};
     p.offs = d_offs;
     p.E = E;
@@ -580,7 +614,7 @@ extern "C" dgr_status dgr_grouped_wgrad_accumulate(const void *G, const void *X,
     p.n_items = static_cast<int32_t>(n_items);
     p.sched = sched_for(static_cast<uint32_t>(n_items));
     const unsigned grid = sched_grid(static_cast<unsigned>(n_items < sms ? n_items : sms));
-    wgrad_kernel<<<grid, kThreadsW, kSmemBytes, static_cast<cudaStream_t>(stream)>>>(mG, mX, mX2, p);
+    wgrad_kernel<<<grid, kThreadsW, kSmemBytes, static_cast<cudaStream_t>(stream)>>>(mG, mX, mX2, mM, p);
     return launch_status();
 }
 

@@ -253,13 +253,18 @@ dgr_status dgr_det_index_add(float *out, int64_t R, int64_t D, int64_t ld_out, c
  *                 from a fresh accumulator, K16 steps in ascending token order;
  *   dW = fold_c p_c (ascending, starting from p_0);
  *   main_grad[e][n][k] = main_grad[e][n][k] + dW[n][k]   (one rounding).
+ * The last add is made in L2 by the bulk copy engine's tensor reduce-add,
+ * one round-to-nearest-even binary32 add per element with subnormals kept;
+ * every element has exactly one writer, so nothing depends on timing. (A NaN
+ * result is a NaN; its payload is not specified.)
  *
  * G:        [T_total, N] bf16 row-major; X: [T_total, K] bf16 row-major.
  * d_offs:   [E+1] int64 DEVICE array, non-decreasing, d_offs[0] = 0,
  *           d_offs[E] = T_total (not read by the host: no synchronisation).
  * main_grad: [E, N, K] fp32, dense.
  * chunk_tokens: 512.
- * Limits:   N a multiple of 128, K a multiple of 256, E >= 1, T_total < 2^31.
+ * Limits:   N a multiple of 128, K a multiple of 256, E >= 1, T_total < 2^31,
+ *           N, K <= 2^20, E * N < 2^31 (DGR_ERR_UNSUPPORTED otherwise).
  * Alignment: G, X 16-byte aligned; main_grad 32-byte aligned.
  * ws:       dgr_wgrad_workspace_bytes() bytes, zeroed once (status word).
  * main_grad must not overlap G, X, d_offs or ws.

@@ -126,6 +126,11 @@ def test_host_rejects_bad_arguments_before_any_launch(L):
     assert L.dgr_grouped_dbias(dy, 1, 256, 12, 12, offs, 2, db, 12, 0, 128, ws, 1 << 20, None) == 5
     assert L.dgr_grouped_dbias(dy, 1, 256, 16, 16, offs, 2, db, 16, 0, 128, ws, 64, None) == 3
     assert L.dgr_grouped_dbias(dy, 1, 256, 16, 16, offs, 2, _p(0x100040), 16, 0, 128, ws, 1 << 20, None) == 4
+    # wgrad: chunk other than 512, N not a multiple of 128, E * N beyond 32-bit rows of main_grad
+    g, x, mg = _p(0x100000), _p(0x200000), _p(0x300000)
+    assert L.dgr_grouped_wgrad_accumulate(g, x, offs, 2, 1024, 128, 256, mg, 256, ws, 1 << 20, None) == 1
+    assert L.dgr_grouped_wgrad_accumulate(g, x, offs, 2, 1024, 100, 256, mg, 512, ws, 1 << 20, None) == 2
+    assert L.dgr_grouped_wgrad_accumulate(g, x, offs, 4096, 1024, 1 << 20, 256, mg, 512, ws, 1 << 20, None) == 2
 
 
 def test_dbias_workspace_size(L):

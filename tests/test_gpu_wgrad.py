@@ -66,6 +66,32 @@ def test_full_shape_ternary_and_replay():
         assert torch.equal(again.view(torch.int32), first.view(torch.int32))
 
 
+def test_subnormal_main_grad_kept():
+    # main_grad full of subnormals: where dW is exactly 0 (the X columns made
+    # zero) they must come back unchanged, which an add that flushed
+    # subnormals would not do; elsewhere the ternary dW is an exact integer and
+    # the result is numpy's float32 (round-to-nearest) sum
+    counts = [300, 0, 529]
+    wi = gi.wgrad_input(3, sum(counts), 128, 512, seed=31, dist="ternary", counts=counts)
+    wi.X[:, 64:192] = 0
+    rng = np.random.default_rng(31)
+    shape = tuple(wi.main_grad.shape)
+    bits = (rng.integers(1, 1 << 23, size=shape, dtype=np.int64)
+            | (rng.integers(0, 2, size=shape, dtype=np.int64) << 31)).astype(np.uint32)
+    wi.main_grad = torch.from_numpy(bits.view(np.float32).copy())
+    got = _gpu(wi).cpu().numpy()
+    G = wi.G.to(torch.float64).numpy()
+    X = wi.X.to(torch.float64).numpy()
+    o = wi.offs.numpy()
+    want = bits.view(np.float32).copy()
+    for e in range(wi.E):
+        if o[e + 1] > o[e]:
+            want[e] = want[e] + (G[o[e]:o[e + 1]].T @ X[o[e]:o[e + 1]]).astype(np.float32)
+    assert_bits_equal(got, want, "wgrad onto subnormal main_grad")
+    assert_bits_equal(got[:, :, 64:192], bits.view(np.float32)[:, :, 64:192], "dW = 0 columns untouched")
+    assert_bits_equal(got[1], bits.view(np.float32)[1], "empty expert")
+
+
 def _oracle_full(wi: gi.WgradInput) -> np.ndarray:
     import oracle
     T, N = wi.G.shape
