@@ -94,7 +94,6 @@ struct WgradParams {
     Sched sched;  // the order in which the CTAs walk the items
 };
 
-// item -> tile, and its half (-1: the whole tile)
 // main_grad[y .. y + 31][x .. x + 31] += the box at src (bulk async group).
 __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap *map, uint32_t src, int32_t x, int32_t y) {
     asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
@@ -129,6 +128,7 @@ __device__ __forceinline__ int my_items(const WgradParams &p) {
     return b < p.n_items ? (p.n_items - b + G - 1) / G : 0;
 }
 
+// item -> tile, and its half (-1: the whole tile)
 __device__ __forceinline__ int item_tile(const WgradParams &p, int item, int &half) {
     if (item < p.n_split) {
         half = -1;
