@@ -25,7 +25,7 @@
 // warps 4-11 read the accumulator back, fold the chunks and finish the tile
 // (the epilogue warpgroups hold the running fold, 128 fp32 per thread, so
 // they take most of the registers; warps 2-3 idle) and issue the tile's
-// reduce-adds through a 4 KB shared-memory box each.
+// reduce-adds through a 16 KB shared-memory box per column half.
 // Rows of a stage past the expert's end are zeroed in shared memory before
 // the MMA reads them (TMA fills rows past the tensor's end with zeros).
 // Every wait is bounded; a timeout records DGR_ERR_TIMEOUT and aborts the
@@ -71,12 +71,15 @@ struct Ctl {
     uint64_t empty[kStages];
     uint64_t tfull[2];
     uint64_t tempty[2];
+    uint64_t gsync[2];  // the four epilogue warps of a column half, per reduce-add box
+    uint64_t dead;      // never arrived at: the diagnostic stall waits on it
     uint32_t tmem_base;
     int abort;
 };
-// per epilogue warp, one 32 x 32 fp32 box (4 KB, 1024-byte aligned) for the
-// reduce-add of a 32-column slice of its 32 rows, in the 128-byte swizzle of
-// the main_grad tensor map
+// per epilogue column half (four warps), one 128 x 32 fp32 box (16 KB,
+// 1024-byte aligned) for the reduce-add of a 32-column slice of the tile's 128
+// rows, in the 128-byte swizzle of the main_grad tensor map; warp q writes
+// rows 32q .. 32q + 31
 constexpr uint32_t kBoxM = 32 * 32 * 4;
 constexpr uint32_t kXposeBytes = kEpiWarps * kBoxM;
 constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + kXposeBytes + sizeof(Ctl);
@@ -92,9 +95,22 @@ struct WgradParams {
     // would leave more than half the CTAs idle is spread over twice as many.
     int32_t n_split, n_items;
     Sched sched;  // the order in which the CTAs walk the items
+    // Diagnostic stall (dgr_diag_wgrad_stall; 0 in every product call): CTA 0's
+    // role stall_role (1 TMA producer, 2 MMA issuer, 3 epilogue warp 4) waits on
+    // a barrier nobody arrives at, at its stall_after-th stage (roles 1, 2) or
+    // tile end (role 3), until stall_ns runs out; the CTA then aborts like on
+    // any other timeout.
+    int32_t stall_role, stall_after;
+    uint64_t stall_ns;
 };
 
-// main_grad[y .. y + 31][x .. x + 31] += the box at src (bulk async group).
+// The diagnostic stall of role r at count n: false once its wait ran out.
+__device__ __forceinline__ bool stall_point(const WgradParams &p, Ctl *ctl, volatile int *abort_flag, int r, int n) {
+    if (p.stall_role != r || n != p.stall_after || blockIdx.x != 0) return true;
+    return mbar_wait(&ctl->dead, 0, abort_flag, p.hdr, 14 + r, p.stall_ns);
+}
+
+// main_grad[y .. y + 127][x .. x + 31] += the box at src (bulk async group).
 __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap *map, uint32_t src, int32_t x, int32_t y) {
     asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
                      reinterpret_cast<uint64_t>(map)),
@@ -174,7 +190,9 @@ __global__ void __launch_bounds__(kThreadsW, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(&ctl->tfull[b], 1);
             mbar_init(&ctl->tempty[b], kEpiWarps);
+            mbar_init(&ctl->gsync[b], 4);
         }
+        mbar_init(&ctl->dead, 1);
         ctl->abort = 0;
         fence_mbar_init();
         prefetch_tmap(&tmG);
@@ -200,6 +218,7 @@ __global__ void __launch_bounds__(kThreadsW, 1)
             bool armed[kStages] = {};
             uint32_t armed_phase[kStages] = {};
             bool ok = true;
+            int n_stage = 0;
             for (int k = 0, n_my = my_items(p); ok && k < n_my; ++k) {
                 const int tau = my_item(p, k, n_my);
                 int e, nb, kb;
@@ -210,7 +229,8 @@ __global__ void __launch_bounds__(kThreadsW, 1)
                 for (int32_t c0 = 0; ok && c0 < te; c0 += kChunk) {
                     const int32_t vc = min(kChunk, te - c0);
                     for (int32_t s0 = 0; s0 < vc; s0 += BK) {
-                        if (!mbar_wait(&ctl->empty[stage], phase ^ 1, abort_flag, p.hdr, 10)) {
+                        if (!stall_point(p, ctl, abort_flag, 1, n_stage++) ||
+                            !mbar_wait(&ctl->empty[stage], phase ^ 1, abort_flag, p.hdr, 10)) {
                             ok = false;
                             break;
                         }
@@ -242,6 +262,7 @@ __global__ void __launch_bounds__(kThreadsW, 1)
         uint32_t stage = 0, phase = 0, g = 0;
         uint32_t last_stage = 0, last_phase = 0;  // the latest stage-release commit
         bool committed = false, ok = true;
+        int n_stage = 0;
         for (int k = 0, n_my = my_items(p); ok && k < n_my; ++k) {
             const int tau = my_item(p, k, n_my);
             int e, nb, kb;
@@ -259,7 +280,8 @@ __global__ void __launch_bounds__(kThreadsW, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + buf * BN;
                 for (int32_t s0 = 0; s0 < vc; s0 += BK) {
-                    if (!mbar_wait(&ctl->full[stage], phase, abort_flag, p.hdr, 12)) {
+                    if (!stall_point(p, ctl, abort_flag, 2, n_stage++) ||
+                        !mbar_wait(&ctl->full[stage], phase, abort_flag, p.hdr, 12)) {
                         ok = false;
                         break;
                     }
@@ -336,8 +358,9 @@ __global__ void __launch_bounds__(kThreadsW, 1)
         setmaxnreg_inc<kRegsHigh>();
         const int q = warp & 3;                 // TMEM lane quarter this warp may access
         const int h = (warp - 4) >> 2;          // column half of the tile
-        uint32_t g = 0;
+        uint32_t g = 0, gph = 0;
         bool ok = true;
+        int n_end = 0;
         float F[128];
         for (int k = 0, n_my = my_items(p); ok && k < n_my; ++k) {
             const int tau = my_item(p, k, n_my);
@@ -378,30 +401,54 @@ __global__ void __launch_bounds__(kThreadsW, 1)
             }
             if (!ok) break;
             if (!active) continue;
-            // main_grad += dW, a 32-column slice at a time: row i of the warp's 32
-            // rows (lane i, as TMEM gives them) goes to the warp's box in the map's
-            // 128-byte swizzle (16-byte chunk c of row i at chunk c ^ (i % 8), so
-            // the 32 lanes' stores spread over the banks), one tensor reduce-add
-            // sends the box to main_grad, and the next slice waits until the
-            // engine has read the box. The SM never reads main_grad: the add
-            // happens in L2 (442 us a call with the read-modify-write in the
-            // epilogue warps, through a transpose tile, after an L2 prefetch of
-            // the tile's main_grad; 423 us this way, the same bits).
-            const uint32_t xs = smem_u32(xbox) + (warp - 4) * kBoxM;
-            const int32_t row0 = e * p.N + nb * BM + 32 * q;
+            if (warp == 4 && !stall_point(p, ctl, abort_flag, 3, n_end)) {
+                ok = false;
+                break;
+            }
+            ++n_end;
+            // main_grad += dW, a 32-column slice at a time: the four warps of the
+            // column half write their rows into the half's box (row i of a warp
+            // from lane i, as TMEM gives them, in the map's 128-byte swizzle:
+            // 16-byte chunk c of a row at chunk c ^ (row % 8), so the 32 lanes'
+            // stores spread over the banks), and one tensor reduce-add, issued by
+            // warp q = 0, sends the 128 x 32 box to main_grad; the box is written
+            // again once the engine has read it. The SM never reads main_grad: the
+            // add happens in L2 (442 us a call with the read-modify-write in the
+            // epilogue warps, through a transpose tile, after an L2 prefetch of the
+            // tile's main_grad; 423 us with a reduce-add of a 32 x 32 box per
+            // warp, 414.5 against 416.8 us with one per column half, the same
+            // bits). The four warps meet on an mbarrier (bounded waits) before
+            // writing the box and before it is sent.
+            const uint32_t gbox = smem_u32(xbox) + h * (4 * kBoxM);
+            const uint32_t xs = gbox + q * kBoxM;
+            const int32_t rowg = e * p.N + nb * BM;
             const int32_t col0 = kb * BN + coff;
+            const bool issuer = q == 0 && lane == 0;
+            auto group_sync = [&]() -> bool {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->gsync[h]);
+                const bool r = mbar_wait(&ctl->gsync[h], gph, abort_flag, p.hdr, 14);
+                gph ^= 1;
+                return r;
+            };
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                if (lane == 0) bulk_wait_read0();
-                __syncwarp();
+                if (issuer) bulk_wait_read0();
+                if (!group_sync()) {
+                    ok = false;
+                    break;
+                }
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
                     st_shared_v4(xs + lane * 128 + 16 * (c ^ (lane & 7)), F[32 * j + 4 * c], F[32 * j + 4 * c + 1],
                                  F[32 * j + 4 * c + 2], F[32 * j + 4 * c + 3]);
                 fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_reduce_add_2d(&tmM, xs, col0 + 32 * j, row0);
+                if (!group_sync()) {
+                    ok = false;
+                    break;
+                }
+                if (issuer) {
+                    tma_reduce_add_2d(&tmM, gbox, col0 + 32 * j, rowg);
                     bulk_commit();
                 }
             }
@@ -538,7 +585,7 @@ dgr_status make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols
     return r == CUDA_SUCCESS ? DGR_OK : DGR_ERR_CUDA;
 }
 
-// Tensor map over main_grad as fp32 [rows, cols] row-major: a box of 32 rows x
+// Tensor map over main_grad as fp32 [rows, cols] row-major: a box of 128 rows x
 // 32 columns (128 bytes a row), 128-byte swizzle.
 dgr_status make_mg_map(CUtensorMap *m, void *base, int64_t rows, int64_t cols) {
     PFN_cuTensorMapEncodeTiled_v12000 enc;
@@ -546,7 +593,7 @@ dgr_status make_mg_map(CUtensorMap *m, void *base, int64_t rows, int64_t cols) {
     if (st != DGR_OK) return st;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 4)};
-    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t box[2] = {32, 128};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -583,9 +630,12 @@ extern "C" size_t dgr_wgrad_workspace_bytes(int32_t E, int64_t N, int64_t K) {
     return sizeof(WsHeader);
 }
 
-extern "C" dgr_status dgr_grouped_wgrad_accumulate(const void *G, const void *X, const int64_t *d_offs, int32_t E,
-                                                   int64_t T_total, int64_t N, int64_t K, float *main_grad,
-                                                   int32_t chunk_tokens, void *ws, size_t ws_bytes, void *stream) {
+namespace dgr {
+namespace {
+
+dgr_status wgrad_call(const void *G, const void *X, const int64_t *d_offs, int32_t E, int64_t T_total, int64_t N,
+                      int64_t K, float *main_grad, int32_t chunk_tokens, void *ws, size_t ws_bytes, void *stream,
+                      int32_t stall_role, int32_t stall_after, uint64_t stall_ns) {
     if (E < 1 || T_total < 0 || N <= 0 || K <= 0 || chunk_tokens != kChunk) return DGR_ERR_INVALID_ARG;
     if (N % BM != 0 || K % BN != 0 || T_total >= INT32_MAX || N > (1 << 20) || K > (1 << 20) ||
         static_cast<int64_t>(E) * N > INT32_MAX)
@@ -634,9 +684,30 @@ extern "C" dgr_status dgr_grouped_wgrad_accumulate(const void *G, const void *X,
     if (n_items > INT32_MAX) return DGR_ERR_UNSUPPORTED;
     p.n_items = static_cast<int32_t>(n_items);
     p.sched = sched_for(static_cast<uint32_t>(n_items));
+    p.stall_role = stall_role;
+    p.stall_after = stall_after;
+    p.stall_ns = stall_ns;
     const unsigned grid = sched_grid(static_cast<unsigned>(n_items < sms ? n_items : sms));
     wgrad_kernel<<<grid, kThreadsW, kSmemBytes, static_cast<cudaStream_t>(stream)>>>(mG, mX, mX2, mM, p);
     return launch_status();
+}
+
+}  // namespace
+}  // namespace dgr
+
+extern "C" dgr_status dgr_grouped_wgrad_accumulate(const void *G, const void *X, const int64_t *d_offs, int32_t E,
+                                                   int64_t T_total, int64_t N, int64_t K, float *main_grad,
+                                                   int32_t chunk_tokens, void *ws, size_t ws_bytes, void *stream) {
+    return wgrad_call(G, X, d_offs, E, T_total, N, K, main_grad, chunk_tokens, ws, ws_bytes, stream, 0, 0, 0);
+}
+
+extern "C" dgr_status dgr_diag_wgrad_stall(const void *G, const void *X, const int64_t *d_offs, int32_t E,
+                                           int64_t T_total, int64_t N, int64_t K, float *main_grad, void *ws,
+                                           size_t ws_bytes, int32_t role, int32_t after, int32_t limit_us,
+                                           void *stream) {
+    if (role < 1 || role > 3 || after < 0 || limit_us < 1 || limit_us > 1000000) return DGR_ERR_INVALID_ARG;
+    return wgrad_call(G, X, d_offs, E, T_total, N, K, main_grad, kChunk, ws, ws_bytes, stream, role, after,
+                      static_cast<uint64_t>(limit_us) * 1000ull);
 }
 
 extern "C" dgr_status dgr_tc_probe_k16(const uint16_t *A, const uint16_t *B, const float *C, float *D, int32_t n_prob,

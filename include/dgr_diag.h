@@ -59,6 +59,26 @@ dgr_status dgr_diag_wait_timeout(int32_t which, int32_t limit_us, void *ws, size
 dgr_status dgr_diag_noalloc_wait_timeout(int32_t which, int32_t limit_us, void *stream);
 
 /*
+ * The grouped wgrad (dgr_grouped_wgrad_accumulate, same arguments and checks,
+ * chunk_tokens 512) with one of CTA 0's roles made to time out inside the
+ * tensor-core pipeline: role 1, the TMA producer, before its after-th stage
+ * copy; role 2, the MMA issuer, before its after-th stage; role 3, epilogue
+ * warp 4, at its after-th tile end (before that tile's reduce-adds). The role
+ * waits, bounded by limit_us, on an mbarrier nobody arrives at, records
+ * DGR_ERR_TIMEOUT (where = 14 + role) and sets the CTA's abort flag; the CTA's
+ * other roles give up their waits, the producer waits (bounded) for its copies
+ * in flight, the MMA issuer for the completion of the MMAs it issued, the
+ * epilogue for its reduce-adds, and only then is TMEM freed and the CTA done.
+ * The other CTAs finish their tiles. main_grad is left partly updated (the
+ * stalled CTA's tiles); no GPU fault or hang is involved, and the context
+ * stays usable. role: 1 .. 3; after >= 0 (a count never reached: no stall);
+ * limit_us: 1 .. 1,000,000.
+ */
+dgr_status dgr_diag_wgrad_stall(const void *G, const void *X, const int64_t *d_offs, int32_t E, int64_t T_total,
+                                int64_t N, int64_t K, float *main_grad, void *ws, size_t ws_bytes, int32_t role,
+                                int32_t after, int32_t limit_us, void *stream);
+
+/*
  * How dgr_ordered_colsum() would launch a call of T tokens and H columns,
  * computed on the host alone (no device needed): plan[0] = path (0: at most
  * 512 tiles of 16-byte-vector shapes, one launch whose last warp folds; 1:

@@ -46,3 +46,50 @@ def test_wait_runs_out_and_the_context_stays_usable(which):
     out = torch.zeros(64, device="cuda")
     dgr.ordered_colsum(ci.base.cuda().view(1, 3000, 64), out)
     assert_bits_equal(out.cpu().numpy(), want, "colsum after a timeout")
+
+
+@pytest.mark.parametrize("role,after", [(1, 9), (1, 25), (2, 0), (2, 9), (2, 25), (3, 0), (3, 1)])
+def test_wgrad_pipeline_role_times_out_and_drains(role, after):
+    # one role of the tensor-core pipeline (1 TMA producer, 2 MMA issuer, 3 an
+    # epilogue warp) of CTA 0 waits on a barrier nobody arrives at, mid-run
+    # (256 tiles: CTA 0 takes two, of 18 and 15 stages): the call returns, the status
+    # names the role, and the CTA's drains (copies in flight, issued MMAs,
+    # reduce-adds) let it free TMEM and exit; the context then runs the wgrad
+    # bit-exactly
+    counts = [1100, 900]
+    N, K = 2048, 2048
+    wi = gi.wgrad_input(2, sum(counts), N, K, seed=41, dist="ternary", counts=counts)
+    G, X, offs, mg = wi.G.cuda(), wi.X.cuda(), wi.offs.cuda(), wi.main_grad.cuda()
+    ws = dgr.workspace(256)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    rc = dgr.lib().dgr_diag_wgrad_stall(G.data_ptr(), X.data_ptr(), offs.data_ptr(), 2, sum(counts), N, K,
+                                         mg.data_ptr(), ws.data_ptr(), ws.numel(), role, after, 20000, None)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert time.perf_counter() - t0 < 2.0
+    assert dgr.read_device_status(ws) == 7  # DGR_ERR_TIMEOUT
+    assert int(ws[4:8].view(torch.int32).item()) == 14 + role
+    out = wi.main_grad.cuda()
+    dgr.grouped_wgrad_accumulate(G, X, offs, out)
+    Gd, Xd = wi.G.to(torch.float64).numpy(), wi.X.to(torch.float64).numpy()
+    want = wi.main_grad.to(torch.float64).numpy().copy()
+    o = wi.offs.numpy()
+    for e in range(2):
+        want[e] += Gd[o[e]:o[e + 1]].T @ Xd[o[e]:o[e + 1]]
+    assert_bits_equal(out.cpu().numpy(), want.astype(np.float32), "wgrad after a pipeline timeout")
+
+
+def test_wgrad_stall_count_never_reached_changes_nothing():
+    # a stall point past the end of the run: an ordinary call, status clear
+    counts = [700, 300]
+    wi = gi.wgrad_input(2, sum(counts), 128, 256, seed=42, dist="ternary", counts=counts)
+    G, X, offs, mg = wi.G.cuda(), wi.X.cuda(), wi.offs.cuda(), wi.main_grad.cuda()
+    ws = dgr.workspace(256)
+    rc = dgr.lib().dgr_diag_wgrad_stall(G.data_ptr(), X.data_ptr(), offs.data_ptr(), 2, sum(counts), 128, 256,
+                                         mg.data_ptr(), ws.data_ptr(), ws.numel(), 2, 1 << 30, 20000, None)
+    assert rc == 0
+    assert dgr.read_device_status(ws) == 0
+    ref = wi.main_grad.cuda()
+    dgr.grouped_wgrad_accumulate(G, X, offs, ref)
+    assert torch.equal(mg.view(torch.int32), ref.view(torch.int32))
