@@ -322,7 +322,7 @@ __device__ __forceinline__ void produce_warp_tile(const ColsumParams &p, int64_t
                     float b2[VE];
                     E::unpack(raw[r + 1], b2);
 #pragma unroll
-                    for (int e = 0; e < VE; ++e) lv[i][e] = __fadd_rn(lv[i][e], b2[e]);
+                    vadd<VE>(lv[i], lv[i], b2);
                 }
             }
         }
@@ -331,10 +331,7 @@ __device__ __forceinline__ void produce_warp_tile(const ColsumParams &p, int64_t
         for (int sft = 1; sft < NP; sft *= 2) {
 #pragma unroll
             for (int i = 0; i + sft < NP; i += 2 * sft)
-                if (i + sft < np_present) {
-#pragma unroll
-                    for (int e = 0; e < VE; ++e) lv[i][e] = __fadd_rn(lv[i][e], lv[i + sft][e]);
-                }
+                if (i + sft < np_present) vadd<VE>(lv[i], lv[i], lv[i + sft]);
         }
         // push batch bi (a compile-time index) onto the binary-counter stack
         if (nb_rows > 0) {
@@ -344,8 +341,7 @@ __device__ __forceinline__ void produce_warp_tile(const ColsumParams &p, int64_t
 #pragma unroll
             for (int l = 0; l < LV; ++l) {
                 if (((bi >> l) & 1) == 0) break;
-#pragma unroll
-                for (int e = 0; e < VE; ++e) acc[e] = __fadd_rn(stack[l][e], acc[e]);
+                vadd<VE>(acc, stack[l], acc);
                 lvl = l + 1;
             }
 #pragma unroll

@@ -184,8 +184,7 @@ __global__ void __launch_bounds__(kProdThreads, 1) dbias_produce(const DbiasPara
                 if (BATCH > 1 && 2 * i + 1 < nb_rows) {
                     float b2[VE];
                     unpack<DT_BF16>(raw[2 * i + 1], b2);
-#pragma unroll
-                    for (int e = 0; e < VE; ++e) lv[i][e] = __fadd_rn(lv[i][e], b2[e]);
+                    vadd<VE>(lv[i], lv[i], b2);
                 }
             }
             const int np_present = (nb_rows + 1) / 2;
@@ -193,10 +192,7 @@ __global__ void __launch_bounds__(kProdThreads, 1) dbias_produce(const DbiasPara
             for (int sft = 1; sft < NP; sft *= 2) {
 #pragma unroll
                 for (int i = 0; i + sft < NP; i += 2 * sft)
-                    if (i + sft < np_present) {
-#pragma unroll
-                        for (int e = 0; e < VE; ++e) lv[i][e] = __fadd_rn(lv[i][e], lv[i + sft][e]);
-                    }
+                    if (i + sft < np_present) vadd<VE>(lv[i], lv[i], lv[i + sft]);
             }
             // push batch bi (a compile-time index) onto the binary-counter stack
             if (nb_rows > 0) {
@@ -206,8 +202,7 @@ __global__ void __launch_bounds__(kProdThreads, 1) dbias_produce(const DbiasPara
 #pragma unroll
                 for (int l = 0; l < LV; ++l) {
                     if (((bi >> l) & 1) == 0) break;
-#pragma unroll
-                    for (int e = 0; e < VE; ++e) acc[e] = __fadd_rn(stack[l][e], acc[e]);
+                    vadd<VE>(acc, stack[l], acc);
                     lvl = l + 1;
                 }
 #pragma unroll

