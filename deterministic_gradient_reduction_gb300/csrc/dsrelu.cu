@@ -302,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < 4; ++j) {
                 uint32_t r[32];
                 tmem_ld32(base + 32 * j, r);
-                tmem_wait_ld();
+                tmem_wait_ld(r);
                 // leaves RN(dY * RN(r * r)), two columns a packed multiply (the
                 // same bits as scalar ones; 221.1 -> 214.9 us a call)
                 float v[32];

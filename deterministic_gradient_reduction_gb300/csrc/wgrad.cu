@@ -386,7 +386,7 @@ __global__ void __launch_bounds__(kThreadsW, 1)
                     if (!active) break;
                     uint32_t r[32];
                     tmem_ld32(base + 32 * j, r);
-                    tmem_wait_ld();
+                    tmem_wait_ld(r);
                     if (c0 == 0) {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) F[32 * j + i] = __uint_as_float(r[i]);
@@ -542,7 +542,7 @@ __global__ void __launch_bounds__(128, 1)
         for (int j = 0; j < BN / 32; ++j) {
             uint32_t r[32];
             tmem_ld32(lane_base + 32 * j, r);
-            tmem_wait_ld();
+            tmem_wait_ld(r);
 #pragma unroll
             for (int i = 0; i < 32; ++i) D[row * 256 + 32 * j + i] = __uint_as_float(r[i]);
         }
