@@ -68,10 +68,12 @@ struct Ctl {
     uint64_t empty[kStages];
     uint64_t tfull[2];
     uint64_t tempty[2];
+    uint64_t dead;  // never arrived at: the diagnostic stall waits on it
     uint32_t tmem_base;
     int abort;
 };
 constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + sizeof(Ctl);
+
 
 struct DsParams {
     const int64_t *offs;
@@ -83,7 +85,19 @@ struct DsParams {
     int32_t accumulate;
     WsHeader *hdr;
     Sched sched;          // the setting; bound to the tile count on the device
+    // Diagnostic stall (dgr_diag_dsrelu_stall; 0 in every product call): CTA 0's
+    // role stall_role (1 TMA producer, 2 MMA issuer, 3 epilogue warp 4) waits on
+    // a barrier nobody arrives at before its stall_after-th stage (roles 1, 2)
+    // or accumulator (role 3), until stall_ns runs out, then aborts the CTA.
+    int32_t stall_role, stall_after;
+    uint64_t stall_ns;
 };
+
+// The diagnostic stall of role r at count n: false once its wait ran out.
+__device__ __forceinline__ bool stall_point(const DsParams &p, Ctl *ctl, volatile int *abort_flag, int r, int64_t n) {
+    if (p.stall_role != r || n != p.stall_after || blockIdx.x != 0) return true;
+    return mbar_wait(&ctl->dead, 0, abort_flag, p.hdr, 40 + r, p.stall_ns);
+}
 
 
 // mb_base[e] = first m-block of expert e (mb_base[E] = all m-blocks), by the
@@ -164,6 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&ctl->tfull[b], 1);
             mbar_init(&ctl->tempty[b], kEpiWarps);
         }
+        mbar_init(&ctl->dead, 1);
         ctl->abort = 0;
         fence_mbar_init();
         prefetch_tmap(&tmA);
@@ -187,12 +202,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool armed[kStages] = {};
             uint32_t armed_phase[kStages] = {};
             bool ok = true;
+            int64_t n_stage = 0;
             for (int64_t tau = blockIdx.x; ok && tau < n_tiles; tau += gridDim.x) {
                 int e, mb, nb;
                 tile_of(p, mb_base, sched_item(sched, static_cast<uint32_t>(tau)), e, mb, nb);
                 const int32_t row0 = static_cast<int32_t>(p.offs[e]) + mb * BM;
                 for (int kb = 0; kb < n_k; ++kb) {
-                    if (!mbar_wait(&ctl->empty[stage], phase ^ 1, abort_flag, p.hdr, 31)) {
+                    if (!stall_point(p, ctl, abort_flag, 1, n_stage++) ||
+                        !mbar_wait(&ctl->empty[stage], phase ^ 1, abort_flag, p.hdr, 31)) {
                         ok = false;
                         break;
                     }
@@ -221,6 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t stage = 0, phase = 0, g = 0;
         uint32_t last_stage = 0, last_phase = 0;  // the latest stage-release commit
         bool committed = false, ok = true;
+        int64_t n_stage = 0;
         for (int64_t tau = blockIdx.x; ok && tau < n_tiles; tau += gridDim.x, ++g) {
             const uint32_t buf = g & 1, tph = (g >> 1) & 1;
             if (!mbar_wait(&ctl->tempty[buf], tph ^ 1, abort_flag, p.hdr, 32)) {
@@ -230,7 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint32_t d_tmem = tmem + buf * BN;
             for (int kb = 0; kb < n_k; ++kb) {
-                if (!mbar_wait(&ctl->full[stage], phase, abort_flag, p.hdr, 33)) {
+                if (!stall_point(p, ctl, abort_flag, 2, n_stage++) ||
+                    !mbar_wait(&ctl->full[stage], phase, abort_flag, p.hdr, 33)) {
                     ok = false;
                     break;
                 }
@@ -291,7 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ldg_nc_v4u_if(dy[i], p.dY + row * p.N + col0 + 8 * i, mine);
             }
             const uint32_t buf = g & 1, tph = (g >> 1) & 1;
-            if (!mbar_wait(&ctl->tfull[buf], tph, abort_flag, p.hdr, 34)) {
+            if ((warp == 4 && !stall_point(p, ctl, abort_flag, 3, static_cast<int64_t>(g))) ||
+                !mbar_wait(&ctl->tfull[buf], tph, abort_flag, p.hdr, 34)) {
                 ok = false;
                 break;
             }
@@ -399,9 +419,12 @@ extern "C" size_t dgr_dsrelu_dprob_workspace_bytes(int64_t T, int64_t N) {
     return sizeof(WsHeader) + align_up(static_cast<size_t>(T) * static_cast<size_t>((N + 127) / 128) * 4);
 }
 
-extern "C" dgr_status dgr_dsrelu_dprob(const void *A, const void *B, const int64_t *d_offs, int32_t E, int64_t T,
-                                       int64_t K, int64_t N, const void *dY, float *dprob, int32_t accumulate,
-                                       void *ws, size_t ws_bytes, void *stream) {
+namespace dgr {
+namespace {
+
+dgr_status dsrelu_call(const void *A, const void *B, const int64_t *d_offs, int32_t E, int64_t T, int64_t K, int64_t N,
+                       const void *dY, float *dprob, int32_t accumulate, void *ws, size_t ws_bytes, void *stream,
+                       int32_t stall_role, int32_t stall_after, uint64_t stall_ns) {
     if (E < 1 || T < 0 || K < 1 || N < 1) return DGR_ERR_INVALID_ARG;
     if (E > kMaxExperts || T > INT32_MAX || (K % BK) != 0 || (N % BN) != 0 || N > (1 << 20) ||
         static_cast<int64_t>(E) * K > INT32_MAX)
@@ -447,9 +470,30 @@ extern "C" dgr_status dgr_dsrelu_dprob(const void *A, const void *B, const int64
         return DGR_ERR_CUDA;
     const int64_t tiles_max = ((T + BM - 1) / BM + E) * (N / BN);
     p.sched = sched_setting();
+    p.stall_role = stall_role;
+    p.stall_after = stall_after;
+    p.stall_ns = stall_ns;
     const unsigned grid = sched_grid(static_cast<unsigned>(tiles_max < sms ? tiles_max : sms));
     dsrelu_gemm<<<grid, kThreads, kSmemBytes, s>>>(mA, mB, p);
     if (cudaGetLastError() != cudaSuccess) return DGR_ERR_CUDA;
     dsrelu_fold<<<static_cast<unsigned>((T + 255) / 256), 256, 0, s>>>(p);
     return cudaGetLastError() == cudaSuccess ? DGR_OK : DGR_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace dgr
+
+extern "C" dgr_status dgr_dsrelu_dprob(const void *A, const void *B, const int64_t *d_offs, int32_t E, int64_t T,
+                                       int64_t K, int64_t N, const void *dY, float *dprob, int32_t accumulate,
+                                       void *ws, size_t ws_bytes, void *stream) {
+    return dsrelu_call(A, B, d_offs, E, T, K, N, dY, dprob, accumulate, ws, ws_bytes, stream, 0, 0, 0);
+}
+
+extern "C" dgr_status dgr_diag_dsrelu_stall(const void *A, const void *B, const int64_t *d_offs, int32_t E,
+                                            int64_t T, int64_t K, int64_t N, const void *dY, float *dprob,
+                                            void *ws, size_t ws_bytes, int32_t role, int32_t after,
+                                            int32_t limit_us, void *stream) {
+    if (role < 1 || role > 3 || after < 0 || limit_us < 1 || limit_us > 1000000) return DGR_ERR_INVALID_ARG;
+    return dsrelu_call(A, B, d_offs, E, T, K, N, dY, dprob, 0, ws, ws_bytes, stream, role, after,
+                       static_cast<uint64_t>(limit_us) * 1000ull);
 }

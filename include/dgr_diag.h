@@ -79,6 +79,19 @@ dgr_status dgr_diag_wgrad_stall(const void *G, const void *X, const int64_t *d_o
                                 int32_t after, int32_t limit_us, void *stream);
 
 /*
+ * The same for the dsReLU dprob GEMM (dgr_dsrelu_dprob, same arguments and
+ * checks, accumulate 0): role 1, CTA 0's TMA producer, before its after-th
+ * stage copy; role 2, its MMA issuer, before its after-th stage; role 3,
+ * epilogue warp 4, before its after-th accumulator. DGR_ERR_TIMEOUT is
+ * recorded with where = 40 + role; the CTA drains as the wgrad's does, the
+ * other CTAs and the fold launch run to the end, dprob is left invalid, and
+ * the context stays usable.
+ */
+dgr_status dgr_diag_dsrelu_stall(const void *A, const void *B, const int64_t *d_offs, int32_t E, int64_t T, int64_t K,
+                                 int64_t N, const void *dY, float *dprob, void *ws, size_t ws_bytes, int32_t role,
+                                 int32_t after, int32_t limit_us, void *stream);
+
+/*
  * The packed binary32 arithmetic the kernels use (add.rn.f32x2,
  * mul.rn.f32x2), exposed so that a test can pin it: for i < n_pairs,
  * sum[2i..2i+1] = a + b and prod[2i..2i+1] = a * b, each half rounded to

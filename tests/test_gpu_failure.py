@@ -93,3 +93,32 @@ def test_wgrad_stall_count_never_reached_changes_nothing():
     ref = wi.main_grad.cuda()
     dgr.grouped_wgrad_accumulate(G, X, offs, ref)
     assert torch.equal(mg.view(torch.int32), ref.view(torch.int32))
+
+
+@pytest.mark.parametrize("role,after", [(1, 5), (1, 12), (2, 0), (2, 5), (2, 12), (3, 0), (3, 1)])
+def test_dsrelu_pipeline_role_times_out_and_drains(role, after):
+    # the fused dsReLU dprob GEMM's roles, as for wgrad: 272 tiles, so CTA 0
+    # takes two of 8 stages each; the call returns, the status names the role,
+    # the CTA drains and exits, and the context then computes dprob bit-exactly
+    counts = [1100, 900]
+    T, K, N = sum(counts), 512, 4096
+    ds = gi.dsrelu_input(2, T, K, N, seed=43, counts=counts)
+    A, B, offs, dY = ds.A.cuda(), ds.B.cuda(), ds.offs.cuda(), ds.dY.cuda()
+    dp = torch.zeros(T, device="cuda")
+    ws = dgr.workspace(dgr.dsrelu_dprob_workspace_bytes(T, N))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    rc = dgr.lib().dgr_diag_dsrelu_stall(A.data_ptr(), B.data_ptr(), offs.data_ptr(), 2, T, K, N, dY.data_ptr(),
+                                          dp.data_ptr(), ws.data_ptr(), ws.numel(), role, after, 20000, None)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert time.perf_counter() - t0 < 2.0
+    assert dgr.read_device_status(ws) == 7  # DGR_ERR_TIMEOUT
+    assert int(ws[4:8].view(torch.int32).item()) == 40 + role
+    # the context still works: the smoke's case against the oracle, bit for bit
+    sm = gi.dsrelu_input(2, 128, 64, 256, seed=9, counts=[100, 28])
+    want = np.zeros(128, np.float32)
+    oracle.dsrelu_dprob(gi.bits(sm.A), gi.bits(sm.B), sm.offs.numpy(), gi.bits(sm.dY), want)
+    got = torch.zeros(128, device="cuda")
+    dgr.dsrelu_dprob(sm.A.cuda(), sm.B.cuda(), sm.offs.cuda(), sm.dY.cuda(), got)
+    assert_bits_equal(got.cpu().numpy(), want, "dsrelu dprob after a pipeline timeout")
