@@ -102,17 +102,52 @@ def tensor_peak(peaks: dict, clocks: dict | None) -> tuple[float, str]:
     return peaks["bf16"], "bf16 burst"
 
 
+# The sources each captured operation's kernels are built from: a capture's
+# DRAM bytes hold only while these files are as they were when it was taken.
+TRAFFIC_SOURCES = {
+    "colsum_large": ["colsum.cu", "dgr_common.cuh"],
+    "dprob": ["rowdot.cu", "dgr_common.cuh"],
+    "index_add": ["index_add.cu", "dgr_common.cuh"],
+    "wgrad": ["wgrad.cu", "tc_common.cuh", "dgr_common.cuh"],
+    "dbias": ["dbias.cu", "dgr_common.cuh"],
+    "topk": ["topk.cu", "dgr_common.cuh"],
+    "aux_loss": ["aux_loss.cu", "dgr_common.cuh"],
+}
+
+
+def source_digest(op: str) -> str | None:
+    """SHA-256 over the sources of op's kernels (TRAFFIC_SOURCES), or None."""
+    import hashlib
+    files = TRAFFIC_SOURCES.get(op)
+    if not files:
+        return None
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "deterministic_gradient_reduction_gb300", "csrc")
+    for f in files:
+        path = os.path.join(csrc, f)
+        if not os.path.isfile(path):
+            return None
+        h.update(f.encode() + b"\0" + open(path, "rb").read())
+    return h.hexdigest()
+
+
 def load_traffic() -> dict:
     """DRAM bytes per launch from the committed ncu summaries (profiles/*.md):
-    a line `traffic: <op> <bytes>` per captured operation."""
+    a line `traffic: <op> <bytes>` per captured operation, kept only when the
+    summary's `source: <op> <sha256>` line matches the kernels' sources as they
+    are now (a figure taken on a kernel that has changed since is dropped)."""
     out = {}
     d = os.path.join(ROOT, "profiles")
     if not os.path.isdir(d):
         return out
     for f in sorted(os.listdir(d)):
         if f.endswith(".md"):
-            for m in re.finditer(r"^traffic:\s*(\w+)\s+(\d+)\s*$", open(os.path.join(d, f)).read(), re.M):
-                out[m.group(1)] = int(m.group(2))
+            text = open(os.path.join(d, f)).read()
+            src = {m.group(1): m.group(2) for m in re.finditer(r"^source:\s*(\w+)\s+([0-9a-f]{64})\s*$", text, re.M)}
+            for m in re.finditer(r"^traffic:\s*(\w+)\s+(\d+)\s*$", text, re.M):
+                op = m.group(1)
+                if src.get(op) is not None and src[op] == source_digest(op):
+                    out[op] = int(m.group(2))
     return out
 
 

@@ -61,3 +61,24 @@ def test_tensor_peak_follows_the_clock_record():
                                      "reasons": ["sw_power_cap"]})[1] == "bf16 sustained"
     assert bench.tensor_peak(peaks, {"sm_mhz": 1700.0, "sm_max_mhz": 2070.0, "reasons": []})[0] == 1702.9
     assert bench.tensor_peak(peaks, None) == (1916.5, "bf16 burst")
+
+
+def test_traffic_kept_only_while_the_kernel_sources_match(tmp_path, monkeypatch):
+    # a summary's DRAM bytes count only while its `source:` digest matches the
+    # kernel's sources; after a change to them the figure is dropped (null)
+    csrc = tmp_path / "deterministic_gradient_reduction_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "wgrad.cu").write_text("kernel v1\n")
+    (csrc / "tc_common.cuh").write_text("helpers\n")
+    (csrc / "dgr_common.cuh").write_text("common\n")
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    digest = bench.source_digest("wgrad")
+    assert digest is not None and len(digest) == 64
+    (prof / "wgrad.md").write_text(f"text\n\nsource: wgrad {digest}\ntraffic: wgrad 1234\n")
+    (prof / "other.md").write_text("traffic: dprob 99\n")  # no source line: not kept
+    assert bench.load_traffic() == {"wgrad": 1234}
+    (csrc / "tc_common.cuh").write_text("helpers, changed\n")
+    assert bench.source_digest("wgrad") != digest
+    assert bench.load_traffic() == {}
