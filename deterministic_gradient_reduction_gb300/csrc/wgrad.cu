@@ -361,7 +361,52 @@ __global__ void __launch_bounds__(kThreadsW, 1)
         uint32_t g = 0, gph = 0;
         bool ok = true;
         int n_end = 0;
-        float F[128];
+        // main_grad += dW, a 32-column slice at a time (send): the four warps of
+        // the column half write their rows into the half's box (row i of a warp
+        // from lane i, as TMEM gives them, in the map's 128-byte swizzle: 16-byte
+        // chunk c of a row at chunk c ^ (row % 8), so the 32 lanes' stores spread
+        // over the banks), and one tensor reduce-add, issued by warp q = 0, sends
+        // the 128 x 32 box to main_grad; the box is written again once the engine
+        // has read it. The four warps meet on an mbarrier (bounded waits) before
+        // writing the box and before it is sent. The SM never reads main_grad:
+        // the add happens in L2 (442 us a call with the read-modify-write in the
+        // epilogue warps, through a transpose tile, after an L2 prefetch of the
+        // tile's main_grad; 423 us with a reduce-add of a 32 x 32 box per warp;
+        // 414.5 against 416.8 us with one per column half). A tile's last slice
+        // goes out one chunk later, after the next tile's first accumulator is
+        // read, so that less of every SM's update traffic falls on the moment
+        // all CTAs reach their tile ends (423.7-424.0 against 426.5-428.7 us;
+        // deferring two slices needs more registers than the warps have). The
+        // same bits every way.
+        float F[4][32];
+        float Fd[32];           // the last slice of the previous tile, sent one chunk later
+        bool have_def = false;
+        int32_t def_rowg = 0, def_col = 0;
+        const bool issuer = q == 0 && lane == 0;
+        const uint32_t gbox = smem_u32(xbox) + h * (4 * kBoxM);
+        const uint32_t xs = gbox + q * kBoxM;
+        auto group_sync = [&]() -> bool {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->gsync[h]);
+            const bool r = mbar_wait(&ctl->gsync[h], gph, abort_flag, p.hdr, 14);
+            gph ^= 1;
+            return r;
+        };
+        // one 32-column slice of the column half's 128 rows to main_grad
+        auto send = [&](const float (&v)[32], int32_t col, int32_t rowg) -> bool {
+            if (issuer) bulk_wait_read0();
+            if (!group_sync()) return false;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                st_shared_v4(xs + lane * 128 + 16 * (c ^ (lane & 7)), v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+            fence_proxy_async_smem();
+            if (!group_sync()) return false;
+            if (issuer) {
+                tma_reduce_add_2d(&tmM, gbox, col, rowg);
+                bulk_commit();
+            }
+            return true;
+        };
         for (int k = 0, n_my = my_items(p); ok && k < n_my; ++k) {
             const int tau = my_item(p, k, n_my);
             int e, nb, kb;
@@ -370,7 +415,6 @@ __global__ void __launch_bounds__(kThreadsW, 1)
             int32_t t_beg, te;
             expert_range(p, e, t_beg, te);
             if (te == 0) continue;  // empty expert: main_grad untouched
-            // a half tile's 128 columns are the first column half's (h = 0)
             const bool active = half < 0 || h == 0;
             const int coff = half < 0 ? 128 * h : 128 * half;
             for (int32_t c0 = 0; c0 < te; c0 += kChunk, ++g) {
@@ -389,22 +433,29 @@ __global__ void __launch_bounds__(kThreadsW, 1)
                     tmem_wait_ld(r);
                     if (c0 == 0) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) F[32 * j + i] = __uint_as_float(r[i]);
+                        for (int i = 0; i < 32; ++i) F[j][i] = __uint_as_float(r[i]);
                     } else {
                         // packed pairs: the same bits as 32 scalar adds, half the issue
                         // slots (434.2 -> 426.3 us a call, alternating on one box)
 #pragma unroll
                         for (int i = 0; i < 32; i += 2) {
-                            const float2 d = add2(make_float2(F[32 * j + i], F[32 * j + i + 1]),
+                            const float2 d = add2(make_float2(F[j][i], F[j][i + 1]),
                                                   make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])));
-                            F[32 * j + i] = d.x;
-                            F[32 * j + i + 1] = d.y;
+                            F[j][i] = d.x;
+                            F[j][i + 1] = d.y;
                         }
                     }
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctl->tempty[buf]);
+                if (c0 == 0 && have_def) {  // the previous tile's last slice, a chunk after its others
+                    if (!send(Fd, def_col, def_rowg)) {
+                        ok = false;
+                        break;
+                    }
+                    have_def = false;
+                }
             }
             if (!ok) break;
             if (!active) continue;
@@ -413,53 +464,19 @@ __global__ void __launch_bounds__(kThreadsW, 1)
                 break;
             }
             ++n_end;
-            // main_grad += dW, a 32-column slice at a time: the four warps of the
-            // column half write their rows into the half's box (row i of a warp
-            // from lane i, as TMEM gives them, in the map's 128-byte swizzle:
-            // 16-byte chunk c of a row at chunk c ^ (row % 8), so the 32 lanes'
-            // stores spread over the banks), and one tensor reduce-add, issued by
-            // warp q = 0, sends the 128 x 32 box to main_grad; the box is written
-            // again once the engine has read it. The SM never reads main_grad: the
-            // add happens in L2 (442 us a call with the read-modify-write in the
-            // epilogue warps, through a transpose tile, after an L2 prefetch of the
-            // tile's main_grad; 423 us with a reduce-add of a 32 x 32 box per
-            // warp, 414.5 against 416.8 us with one per column half, the same
-            // bits). The four warps meet on an mbarrier (bounded waits) before
-            // writing the box and before it is sent.
-            const uint32_t gbox = smem_u32(xbox) + h * (4 * kBoxM);
-            const uint32_t xs = gbox + q * kBoxM;
             const int32_t rowg = e * p.N + nb * BM;
             const int32_t col0 = kb * BN + coff;
-            const bool issuer = q == 0 && lane == 0;
-            auto group_sync = [&]() -> bool {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&ctl->gsync[h]);
-                const bool r = mbar_wait(&ctl->gsync[h], gph, abort_flag, p.hdr, 14);
-                gph ^= 1;
-                return r;
-            };
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if (issuer) bulk_wait_read0();
-                if (!group_sync()) {
-                    ok = false;
-                    break;
-                }
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    st_shared_v4(xs + lane * 128 + 16 * (c ^ (lane & 7)), F[32 * j + 4 * c], F[32 * j + 4 * c + 1],
-                                 F[32 * j + 4 * c + 2], F[32 * j + 4 * c + 3]);
-                fence_proxy_async_smem();
-                if (!group_sync()) {
-                    ok = false;
-                    break;
-                }
-                if (issuer) {
-                    tma_reduce_add_2d(&tmM, gbox, col0 + 32 * j, rowg);
-                    bulk_commit();
-                }
+            if (!send(F[0], col0, rowg) || !send(F[1], col0 + 32, rowg) || !send(F[2], col0 + 64, rowg)) {
+                ok = false;
+                break;
             }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) Fd[i] = F[3][i];
+            have_def = true;
+            def_rowg = rowg;
+            def_col = col0 + 96;
         }
+        if (ok && have_def) send(Fd, def_col, def_rowg);
     }
     if (warp >= 4 && lane == 0) bulk_wait0();  // the warp's last reduce-adds are done
     tc_fence_before();
