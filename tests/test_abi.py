@@ -226,3 +226,15 @@ def test_colsum_launch_plan(L):
     assert p(0, 64) == (-1, 0, 0, 0)
     assert L.dgr_diag_colsum_plan(100, 0, 128, 1, 1, 152, 1, 0, plan) == 1
     assert L.dgr_diag_set_schedule(3, 0, 0) == 1 and L.dgr_diag_set_schedule(0, 0, -1) == 1
+
+
+def test_diagnostic_entries_check_their_arguments(L):
+    # refused before any device work: role, stall count and limit out of range,
+    # and the packed-arithmetic pin's pointers
+    f = _p(0x100000)
+    for role, after, limit in ((0, 1, 100), (4, 1, 100), (1, -1, 100), (1, 1, 0), (1, 1, 2000000)):
+        assert L.dgr_diag_wgrad_stall(f, f, f, 2, 1024, 128, 256, f, f, 1 << 20, role, after, limit, None) == 1
+        assert L.dgr_diag_dsrelu_stall(f, f, f, 2, 1024, 64, 256, f, f, f, 1 << 20, role, after, limit, None) == 1
+    assert L.dgr_diag_packed_ops(None, f, 4, f, f, None) == 1           # a null operand
+    assert L.dgr_diag_packed_ops(f, f, -1, f, f, None) == 1             # a negative count
+    assert L.dgr_diag_packed_ops(_p(0x100004), f, 4, f, f, None) == 5  # not 8-byte aligned
