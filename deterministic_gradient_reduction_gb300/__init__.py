@@ -72,6 +72,7 @@ def lib() -> ctypes.CDLL:
             "dgr_diag_wait_timeout": ([I32, I32, P, SZ, P], I32),
             "dgr_diag_wgrad_stall": ([P, P, P, I32, I64, I64, I64, P, P, SZ, I32, I32, I32, P], I32),
             "dgr_diag_packed_ops": ([P, P, I64, P, P, P], I32),
+            "dgr_diag_packed_chain": ([P, P, P, I64, P, P], I32),
             "dgr_diag_dsrelu_stall": ([P, P, P, I32, I64, I64, I64, P, P, P, SZ, I32, I32, I32, P], I32),
             "dgr_ordered_colsum_noalloc": ([P, I32, I64, I64, I64, I64, I64, P, I32, I32, P], I32),
             "dgr_colsum_noalloc_read_status": ([I32, P, P], I32),

@@ -69,10 +69,36 @@ __global__ void __launch_bounds__(256) packed_ops_kernel(const float2 *a, const 
     }
 }
 
+// A packed product feeding binary32 round-to-nearest adds, as the dsReLU
+// leaves feed their tree: chain = c + RN(a * b), two values at a time.
+__global__ void __launch_bounds__(256) packed_chain_kernel(const float2 *a, const float2 *b, const float2 *c, int64_t n,
+                                                           float2 *chain) {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const float2 pr = mul2(a[i], b[i]);
+        chain[i] = make_float2(__fadd_rn(c[i].x, pr.x), __fadd_rn(c[i].y, pr.y));
+    }
+}
+
 }  // namespace
 }  // namespace dgr
 
 using namespace dgr;
+
+extern "C" dgr_status dgr_diag_packed_chain(const float *a, const float *b, const float *c, int64_t n_pairs,
+                                            float *chain, void *stream) {
+    if (n_pairs < 0 || (n_pairs > 0 && (!a || !b || !c || !chain))) return DGR_ERR_INVALID_ARG;
+    if (!aligned(a, 8) || !aligned(b, 8) || !aligned(c, 8) || !aligned(chain, 8)) return DGR_ERR_MISALIGNED;
+    dgr_status st = check_device();
+    if (st != DGR_OK) return st;
+    if (n_pairs == 0) return DGR_OK;
+    const int64_t blocks = (n_pairs + 255) / 256;
+    packed_chain_kernel<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0,
+                          static_cast<cudaStream_t>(stream)>>>(
+        reinterpret_cast<const float2 *>(a), reinterpret_cast<const float2 *>(b), reinterpret_cast<const float2 *>(c),
+        n_pairs, reinterpret_cast<float2 *>(chain));
+    return launch_status();
+}
 
 extern "C" dgr_status dgr_diag_packed_ops(const float *a, const float *b, int64_t n_pairs, float *sum, float *prod,
                                           void *stream) {

@@ -102,6 +102,16 @@ dgr_status dgr_diag_packed_ops(const float *a, const float *b, int64_t n_pairs, 
                                void *stream);
 
 /*
+ * A packed product feeding scalar round-to-nearest adds, the form the dsReLU
+ * leaves take: chain[2i..2i+1] = c + RN(a * b), the product by mul.rn.f32x2,
+ * each add a separate binary32 add. (A packed product feeding a packed add is
+ * not used anywhere: the code generator fuses that pair into a fused
+ * multiply-add, which changes the bits.)
+ */
+dgr_status dgr_diag_packed_chain(const float *a, const float *b, const float *c, int64_t n_pairs, float *chain,
+                                 void *stream);
+
+/*
  * How dgr_ordered_colsum() would launch a call of T tokens and H columns,
  * computed on the host alone (no device needed): plan[0] = path (0: at most
  * 512 tiles of 16-byte-vector shapes, one launch whose last warp folds; 1:

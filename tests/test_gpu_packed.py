@@ -49,3 +49,18 @@ def test_packed_add_and_mul_match_ieee_float32():
         assert not diff.any(), f"{what}: {int(diff.sum())} of {n} differ"
         sub = ((want.view(np.uint32) & 0x7F800000) == 0) & (want != 0)
         assert sub.sum() > n // 50, what  # the draw did reach subnormal results (3 % of products, 19 % of sums)
+
+
+def test_packed_product_feeding_scalar_adds_keeps_both_roundings():
+    # the dsReLU leaves' form: c + RN(a * b) with the product packed and the add
+    # scalar equals two separately rounded float32 operations (no fusion)
+    n = 1 << 22
+    rng = np.random.default_rng(11)
+    a, b, c = (rng.standard_normal(n).astype(np.float32) for _ in range(3))
+    A, B, C = (torch.from_numpy(x).cuda() for x in (a, b, c))
+    out = torch.empty_like(A)
+    assert dgr.lib().dgr_diag_packed_chain(A.data_ptr(), B.data_ptr(), C.data_ptr(), n // 2, out.data_ptr(), None) == 0
+    want = c + (a * b)  # numpy float32: the product rounded, then the sum rounded
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), want.view(np.uint32))
+    fused = (a.astype(np.float64) * b + c).astype(np.float32)  # one rounding, as a fused multiply-add would give
+    assert (fused.view(np.uint32) != want.view(np.uint32)).sum() > n // 20  # the case can tell them apart
