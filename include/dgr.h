@@ -142,8 +142,7 @@ dgr_status dgr_ordered_colsum(const void *x, int32_t dtype, int64_t B, int64_t S
  * Every argument is checked before the array is touched: a refused call
  * enqueues nothing. The first call on a device looks up the array's device
  * address (with that device current; a lookup that fails is tried again on
- * the next call); make that first call before any stream capture. Each call
- * then zeroes the part of the array it uses, the whole
+ * the next call). Each call then zeroes the part of the array it uses, the whole
  * dgr_colsum_workspace_bytes(B*S, H, tile_rows) bytes (one cudaMemsetAsync on
  * `stream` before its kernel), so a call never depends on what an earlier
  * call left there. All calls share the one array: calls that can overlap on
