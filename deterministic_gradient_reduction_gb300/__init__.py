@@ -272,6 +272,11 @@ def topk_canonicalize(ids: torch.Tensor, logits: torch.Tensor, out_ids: torch.Te
         out_ids = torch.empty_like(ids) if out_ids is None else out_ids
         out_logits = torch.empty_like(logits) if out_logits is None else out_logits
         probs = torch.empty_like(logits) if probs is None else probs
+    if R == 0:  # no rows: nothing is read or written, and an empty tensor's strides say nothing
+        _check("dgr_topk_canonicalize", lib().dgr_topk_canonicalize(
+            _ptr(ids), K, _ptr(logits), K, 0, K, _ptr(out_ids), _ptr(out_logits), _ptr(probs), K,
+            _stream(stream)))
+        return out_ids, out_logits, probs
     ld = out_ids.stride(0)
     if out_logits.stride(0) != ld or probs.stride(0) != ld or any(t.stride(1) != 1 for t in
                                                                   (ids, logits, out_ids, out_logits, probs)):

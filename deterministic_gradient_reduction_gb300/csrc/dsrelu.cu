@@ -429,7 +429,7 @@ dgr_status dsrelu_call(const void *A, const void *B, const int64_t *d_offs, int3
     if (E > kMaxExperts || T > INT32_MAX || (K % BK) != 0 || (N % BN) != 0 || N > (1 << 20) ||
         static_cast<int64_t>(E) * K > INT32_MAX)
         return DGR_ERR_UNSUPPORTED;
-    if (!d_offs || !dprob || (T > 0 && (!A || !B || !dY))) return DGR_ERR_INVALID_ARG;
+    if (!d_offs || (T > 0 && (!A || !B || !dY || !dprob))) return DGR_ERR_INVALID_ARG;  // T = 0: dprob is empty
     if (!aligned(d_offs, 8) || !aligned(dprob, 4) || (A && !aligned(A, 16)) || (B && !aligned(B, 16)) ||
         (dY && !aligned(dY, 16)))
         return DGR_ERR_MISALIGNED;

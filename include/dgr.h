@@ -267,6 +267,8 @@ dgr_status dgr_det_index_add(float *out, int64_t R, int64_t D, int64_t ld_out, c
  * Alignment: G, X 16-byte aligned; main_grad 32-byte aligned.
  * ws:       dgr_wgrad_workspace_bytes() bytes, zeroed once (status word).
  * main_grad must not overlap G, X, d_offs or ws.
+ * T_total = 0 (every expert empty): nothing is launched and main_grad stays
+ * as it is; G and X may then be null.
  */
 size_t dgr_wgrad_workspace_bytes(int32_t E, int64_t N, int64_t K);
 dgr_status dgr_grouped_wgrad_accumulate(const void *G, const void *X, const int64_t *d_offs, int32_t E,
@@ -385,6 +387,8 @@ dgr_status dgr_aux_loss(const float *probs, int64_t N, int32_t E, int64_t ld, co
  * ws:       dgr_dsrelu_dprob_workspace_bytes(T, N) bytes, zeroed once (status
  *           word, one FP32 partial per token and N-tile).
  * dprob must not overlap A, B, dY, d_offs or ws.
+ * T = 0 (every expert empty): nothing is launched; A, B, dY, dprob and ws may
+ * then be null.
  */
 size_t dgr_dsrelu_dprob_workspace_bytes(int64_t T, int64_t N);
 dgr_status dgr_dsrelu_dprob(const void *A, const void *B, const int64_t *d_offs, int32_t E, int64_t T, int64_t K,

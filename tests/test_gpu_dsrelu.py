@@ -76,3 +76,11 @@ def test_offsets_outside_the_contract_are_refused_on_the_device():
         dgr.dsrelu_dprob(A, B, torch.tensor(bad, device="cuda"), dY, dp, ws=ws)
         assert dgr.read_device_status(ws) == 1
         assert torch.all(dp == 5.0)
+
+
+def test_no_tokens():
+    """Every expert empty (T = 0): nothing to compute; the call succeeds with an empty dprob."""
+    d = gi.dsrelu_input(3, 0, 64, 256, seed=78, counts=[0, 0, 0])
+    dp = _gpu(d)
+    assert dp.numel() == 0
+    torch.cuda.synchronize()

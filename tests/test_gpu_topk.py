@@ -88,3 +88,9 @@ def test_full_workload_and_replays():
     assert np.array_equal(out[0].cpu().numpy(), want[0])
     assert_bits_equal(out[1].cpu().numpy(), want[1], "topk 65536 x 128 logits")
     assert_bits_equal(probs.view(np.float32), want[2], "topk 65536 x 128 probs")
+
+
+def test_no_rows():
+    """R = 0: nothing to compute; the call succeeds and returns empty outputs."""
+    got = _gpu(np.zeros((0, 8), np.int32), np.zeros((0, 8), np.float32))
+    assert all(a.shape == (0, 8) for a in got)

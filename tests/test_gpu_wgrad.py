@@ -151,3 +151,10 @@ def test_last_wave_of_half_tiles():
     mg0 = gi.f32(wi.main_grad)[e, n, k]
     want = oracle.wgrad_elements(gi.bits(wi.G), gi.bits(wi.X), wi.offs.numpy(), 2560, 2048, e, n, k, mg0)
     assert_bits_equal(got[e, n, k], want, "half-tile tail, sampled")
+
+
+def test_no_tokens_leaves_main_grad_unchanged():
+    """Every expert empty (T_total = 0): the call succeeds and main_grad keeps its bits."""
+    wi = gi.wgrad_input(3, 0, 128, 256, seed=77, dist="ternary", counts=[0, 0, 0])
+    got = _gpu(wi).cpu().numpy()
+    assert_bits_equal(got, gi.f32(wi.main_grad), "wgrad with no tokens")
