@@ -552,12 +552,35 @@ def run_ours(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def host_link_gbs(torch, pinned, host, order, stream):
+    """GB/s of one copy of the largest pinned input to its device tensor, the best of three (untimed
+    by the step; None if it cannot be taken)."""
+    try:
+        n, i = max(((n, i) for n in order for i in range(len(pinned[n]))),
+                   key=lambda ni: pinned[ni[0]][ni[1]].numel() * pinned[ni[0]][ni[1]].element_size())
+        src, dst = pinned[n][i], host[n][1][i]
+        nbytes = src.numel() * src.element_size()
+        best = None
+        for _ in range(3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            dst.copy_(src, non_blocking=True)
+            b.record(stream)
+            b.synchronize()
+            ms = a.elapsed_time(b)
+            best = ms if best is None or ms < best else best
+        return round(nbytes / (best * 1e-3) / 1e9, 1) if best and best > 0 else None
+    except Exception:  # a diagnostic only: the e2e value does not depend on it
+        return None
+
+
 def run_e2e(args, torch, order, ops, host, outs, stream, world, dev):
     pinned = {n: [t.pin_memory() for t in host[n][0]] for n in order}
     res_host = {n: torch.empty(outs[n].shape, dtype=outs[n].dtype, pin_memory=True) for n in order}
     h2d = sum(t.numel() * t.element_size() for n in order for t in pinned[n])
     d2h = sum(t.numel() * t.element_size() for t in res_host.values())
     K = max(1, args.e2e_steps)
+    link = host_link_gbs(torch, pinned, host, order, stream)
     ev = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
           for n in order}
     torch.cuda.synchronize()
@@ -579,6 +602,8 @@ def run_e2e(args, torch, order, ops, host, outs, stream, world, dev):
     val = world * sum(ALGO[n] for n in REDUCTIONS) / (red_ms * 1e-3) / 1e9
     out = {"value": round(val, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "steps": K, "ms_per_step": round(sum(per.values()), 3)}
+    if link is not None:
+        out["h2d_link_gbs"] = link  # this host's pinned-to-device copy rate, which bounds the value
     if "wgrad" in per:
         out["wgrad_tflops"] = round(ALGO["wgrad_flop"] / (per["wgrad"] * 1e-3) / 1e12, 2)
     return out
